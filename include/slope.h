@@ -1,0 +1,176 @@
+/*
+ * slope.h — C ABI of the 2:4-sparse plus low-rank adapter linear layer
+ * (SLoPe) on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation is defined on the page "SLoPe: Double-Pruned Sparse Plus Lazy
+ * Low-Rank Adapter Pretraining of LLMs" (an AI summary of arXiv 2405.16325v3):
+ *   §1 and §2.1 "Double-pruned backward pass" — N:M pruning of the weight and
+ *      a second N:M pruning of its transpose for the input gradient;
+ *   §2.2 "Lazy low-rank adapters" — the rank-r term (X·L)·R;
+ *   §2.3 "Sparse kernels" and App. K "Implementation details" — compressed
+ *      formats for the weight and its transpose, gradients masked with the
+ *      weight's own mask and stored without their zeros;
+ *   §2.4 / App. D — the adapter fused into the sparse product.
+ *
+ * Notation: T tokens, `in` input features, `out` output features, r adapter
+ * rank.  W is out x in.  X is T x in, Y and dY are T x out, L is in x r,
+ * R is r x out.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All matrices are dense, row-major and contiguous, in device memory.
+ *    bf16 means IEEE bfloat16 bit patterns (uint16); f32 is IEEE binary32.
+ *  - Every pointer must be 16-byte aligned (the tensor-memory-access unit's
+ *    rule); otherwise SLOPE_ERR_ALIGNMENT.
+ *  - The caller owns and allocates every buffer; the library allocates no
+ *    device memory and keeps no handle.  Scratch, where a call needs it, is
+ *    passed in (`workspace`, sized by slope_workspace_size()).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  Argument errors are returned synchronously, before any
+ *    launch, and leave every buffer untouched.  Launch failures return
+ *    SLOPE_ERR_CUDA.  Faults inside a kernel surface at the next
+ *    synchronisation as a CUDA error; a device-side wait that gave up (a
+ *    bounded wait ran out) is reported by slope_device_status().
+ *  - Compressed 2:4 format ("vals, meta") of a rows x cols matrix that is 2:4
+ *    along its rows: groups are the aligned column quadruples 4g..4g+3.
+ *      vals: rows x cols/2 bf16, the two kept entries of each group in
+ *            ascending column order;
+ *      meta: rows x cols/8 bytes; group g of a row is the nibble
+ *            (i0 | i1 << 2), i0 < i1 its kept positions; byte b holds group
+ *            2b in its low nibble and group 2b+1 in its high nibble.
+ *    The sparse GEMMs read this format as it is (no reordering pass).
+ *  - Magnitude ranking uses the exact key (bf16 bits & 0x7FFF); ties go to
+ *    the lower index.  No floating-point arithmetic decides a mask.
+ *  - Thread safety: calls may be made from several host threads; the only
+ *    shared state is a per-device capability cache and a device status word.
+ */
+#ifndef SLOPE_H_
+#define SLOPE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SLOPE_OK = 0,
+  SLOPE_ERR_INVALID_ARG = 1, /* NULL pointer, bad flag or dtype, short workspace */
+  SLOPE_ERR_SHAPE = 2,       /* a size breaks the rules of the call */
+  SLOPE_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned */
+  SLOPE_ERR_UNSUPPORTED = 4, /* device is not sm_103, or n:m other than 2:4 */
+  SLOPE_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
+  SLOPE_ERR_TIMEOUT = 6      /* a bounded device-side wait ran out */
+} slope_status;
+
+typedef enum { SLOPE_F32 = 0, SLOPE_BF16 = 1 } slope_dtype;
+
+/* flags of slope_linear_bwd_weight */
+#define SLOPE_DW_DENSE 1u   /* write dW dense (out x in, zeros where pruned) */
+#define SLOPE_ACCUMULATE 2u /* add into dW, dL, dR instead of overwriting */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* slope_status_string(int status);
+
+/* ABI version (major * 10000 + minor * 100 + patch). */
+int slope_version(void);
+
+/*
+ * Bytes of scratch memory the compute calls below need for one linear of
+ * these sizes (T tokens, in, out, rank r).  Passing at least this many bytes
+ * as `workspace` to any of them is always enough; 0 means no scratch.
+ * Returns 0 for invalid sizes as well (the call itself then reports them).
+ */
+size_t slope_workspace_size(int64_t T, int64_t in, int64_t out, int r);
+
+/*
+ * A1 — N:M magnitude prune-and-compress (§1, §2.1, §2.3; App. K, where the
+ * weight is pruned and packed for the sparse product).  For each row of W (rows x cols bf16) and each aligned group
+ * of 4 columns, keep the 2 entries of largest |w| (lower index on ties) and
+ * write them to `vals` (rows x cols/2 bf16) with their positions in `meta`
+ * (rows x cols/8 bytes), in the compressed format above.
+ * Requires n == 2 and m == 4 (else SLOPE_ERR_UNSUPPORTED), rows >= 1 and
+ * cols % 8 == 0 (else SLOPE_ERR_SHAPE).  rows == 0 is a no-op.
+ */
+int slope_prune_nm(const void* W, int64_t rows, int64_t cols, int n, int m, void* vals,
+                   uint8_t* meta, void* stream);
+
+/*
+ * A2 — double pruning (§1, §2.1; §2.3, which keeps compressed copies of both
+ * the weight and its transpose).  Input: the compressed rows x cols (= out x in) weight from
+ * slope_prune_nm.  Output: D = P(Wsᵀ), the cols x rows transpose of the
+ * pruned weight pruned 2:4 again along its rows (the old out dimension, the
+ * reduction dimension of the input gradient), as `t_vals` (cols x rows/2
+ * bf16) and `t_meta` (cols x rows/8 bytes).  Positions removed by the first
+ * pruning count as +0 (key 0), so a group with fewer than two non-zeros
+ * keeps its lowest-index positions and stores +0 there.
+ * Requires rows % 8 == 0 and cols % 16 == 0 (else SLOPE_ERR_SHAPE).
+ */
+int slope_double_prune(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols,
+                       void* t_vals, uint8_t* t_meta, void* stream);
+
+/*
+ * A3 — sparse forward with the fused adapter (§2.1, §2.2, §2.4, App. D):
+ *     Y  = X·Wsᵀ + (X·L)·R          (bf16 inputs, fp32 accumulation)
+ *     XL = X·L                        (kept for the backward)
+ * X: T x in bf16.  (Wv, Wm): the compressed out x in weight.  L: in x r
+ * bf16, R: r x out bf16.  Y: T x out, `y_dtype` SLOPE_F32 or SLOPE_BF16.
+ * XL: T x 2r bf16 output, required when r > 0: row t holds the r values of
+ * (X·L)[t] as bf16 "hi" parts followed by their bf16 "lo" remainders
+ * (hi = bf16(v), lo = bf16(v - hi)); hi + lo keeps about 16 significant
+ * bits, and the adapter product uses both.
+ * Requires in % 128 == 0, out % 128 == 0, T >= 0 (T == 0 is a no-op),
+ * 0 <= r <= 256 and r % 8 == 0; r == 0 disables the adapter (L, R, XL may
+ * then be NULL).
+ */
+int slope_linear_fwd(const void* X, int64_t T, int64_t in, int64_t out, const void* Wv,
+                     const uint8_t* Wm, const void* L, const void* R, int r, void* Y, int y_dtype,
+                     void* XL, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * A4 — sparse input gradient with the fused adapter (§1, §2.1):
+ *     dX = dY·Dᵀ + (dY·Rᵀ)·Lᵀ        G = dY·Rᵀ (kept for dL)
+ * dY: T x out bf16.  (Dv, Dm): the compressed in x out double-pruned matrix
+ * from slope_double_prune.  dX: T x in, `dx_dtype` SLOPE_F32 or SLOPE_BF16.
+ * G: T x 2r bf16 output (hi parts, then lo parts, as XL), required when
+ * r > 0.  Size rules as slope_linear_fwd.
+ */
+int slope_linear_bwd_input(const void* dY, int64_t T, int64_t in, int64_t out, const void* Dv,
+                           const uint8_t* Dm, const void* L, const void* R, int r, void* dX,
+                           int dx_dtype, void* G, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/*
+ * A5 + A6 — masked weight gradient and adapter gradients (§2.3, gradients of
+ * pruned weights are masked; App. K, the gradient stored without the mask's
+ * zeros; §2.2 for the adapter):
+ *     dW = M ⊙ (dYᵀ·X)     M = the weight's own mask (decoded from Wm)
+ *     dL = Xᵀ·G            dR = XLᵀ·dY
+ * dY: T x out bf16, X: T x in bf16, Wm: out x in/8 metadata of the weight.
+ * dW (f32): compressed out x in/2 (the kept entries in Wv's order) by
+ * default, dense out x in with zeros at pruned positions with SLOPE_DW_DENSE.
+ * XL (T x 2r) and G (T x 2r) are the hi/lo outputs of the two calls above;
+ * dL (in x r f32) and dR (r x out f32) are written when r > 0.
+ * SLOPE_ACCUMULATE adds into dW, dL, dR (gradient accumulation) instead of
+ * overwriting them.  T == 0 writes zeros (or leaves them, when accumulating).
+ * Size rules as slope_linear_fwd.
+ */
+int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T, int64_t in, int64_t out,
+                            const uint8_t* Wm, const void* XL, const void* G, int r, float* dW,
+                            uint32_t flags, float* dL, float* dR, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reports and clears the device status word in
+ * which kernels record a bounded wait that ran out (SLOPE_ERR_TIMEOUT), or
+ * returns SLOPE_OK.  A CUDA error seen while synchronising returns
+ * SLOPE_ERR_CUDA.
+ */
+int slope_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SLOPE_H_ */

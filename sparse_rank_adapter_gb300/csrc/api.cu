@@ -1,0 +1,313 @@
+// api.cu — the C ABI declared in include/slope.h: argument validation,
+// device checks, tensor-map encoding and kernel launches.  Every step of
+// the computation runs in this library's kernels; nothing here computes.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/slope.h"
+#include "slope_internal.h"
+
+namespace slope {
+
+// --------------------------------------------------------- device state ---
+
+constexpr int kMaxDevices = 64;
+
+namespace {
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_device_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
+}  // namespace
+
+static int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+int sm_count() {
+  const int dev = current_device();
+  if (dev < 0) return 148;
+  int n = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+// The kernels are built for sm_103a only; any other device is refused.
+static int check_device() {
+  const int dev = current_device();
+  if (dev < 0) return SLOPE_ERR_CUDA;
+  int ok = g_device_ok[dev].load(std::memory_order_relaxed);
+  if (ok == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return SLOPE_ERR_CUDA;
+    ok = (major == 10 && minor == 3) ? 1 : -1;
+    g_device_ok[dev].store(ok, std::memory_order_relaxed);
+  }
+  return ok == 1 ? SLOPE_OK : SLOPE_ERR_UNSUPPORTED;
+}
+
+// ------------------------------------------------------- tensor maps ------
+
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::atomic<EncodeTiledFn> g_encode{nullptr};
+
+EncodeTiledFn encode_fn() {
+  EncodeTiledFn f = g_encode.load(std::memory_order_acquire);
+  if (f) return f;
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || p == nullptr)
+    return nullptr;
+  f = reinterpret_cast<EncodeTiledFn>(p);
+  g_encode.store(f, std::memory_order_release);
+  return f;
+}
+}  // namespace
+
+bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes,
+                  uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                  uint32_t box_outer, Swz swz) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  (void)elem_bytes;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUtensorMapSwizzle s = CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (swz == Swz::B32) s = CU_TENSOR_MAP_SWIZZLE_32B;
+  if (swz == Swz::B64) s = CU_TENSOR_MAP_SWIZZLE_64B;
+  if (swz == Swz::B128) s = CU_TENSOR_MAP_SWIZZLE_128B;
+  std::memset(map, 0, sizeof(*map));
+  const CUresult r =
+      f(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+        CU_TENSOR_MAP_INTERLEAVE_NONE, s, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ----------------------------------------------------- status word --------
+
+namespace {
+__device__ unsigned int g_status_word;
+std::atomic<unsigned int*> g_status_ptr[kMaxDevices];
+}  // namespace
+
+unsigned int* device_status_ptr() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  unsigned int* p = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void* q = nullptr;
+  if (cudaGetSymbolAddress(&q, g_status_word) != cudaSuccess) return nullptr;
+  p = static_cast<unsigned int*>(q);
+  g_status_ptr[dev].store(p, std::memory_order_release);
+  return p;
+}
+
+}  // namespace slope
+
+// ================================================================ C ABI ===
+
+using namespace slope;
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int from_cuda(cudaError_t e) { return e == cudaSuccess ? SLOPE_OK : SLOPE_ERR_CUDA; }
+
+extern "C" const char* slope_status_string(int s) {
+  switch (s) {
+    case SLOPE_OK: return "ok";
+    case SLOPE_ERR_INVALID_ARG: return "invalid argument";
+    case SLOPE_ERR_SHAPE: return "unsupported shape";
+    case SLOPE_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case SLOPE_ERR_UNSUPPORTED: return "unsupported device or n:m pattern";
+    case SLOPE_ERR_CUDA: return "CUDA error";
+    case SLOPE_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int slope_version(void) { return 10000; }
+
+extern "C" size_t slope_workspace_size(int64_t T, int64_t in, int64_t out, int r) {
+  (void)T; (void)in; (void)out; (void)r;
+  return 0;
+}
+
+extern "C" int slope_prune_nm(const void* W, int64_t rows, int64_t cols, int n, int m, void* vals,
+                              uint8_t* meta, void* stream) {
+  if (n != 2 || m != 4) return SLOPE_ERR_UNSUPPORTED;
+  if (rows < 0 || cols <= 0 || cols % 8 != 0) return SLOPE_ERR_SHAPE;
+  if (rows == 0) return SLOPE_OK;
+  if (!W || !vals || !meta) return SLOPE_ERR_INVALID_ARG;
+  if (!aligned16(W) || !aligned16(vals) || !aligned16(meta)) return SLOPE_ERR_ALIGNMENT;
+  if (int s = check_device()) return s;
+  return from_cuda(launch_prune24(W, rows, cols, vals, meta, static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int slope_double_prune(const void* vals, const uint8_t* meta, int64_t rows,
+                                  int64_t cols, void* t_vals, uint8_t* t_meta, void* stream) {
+  if (rows <= 0 || cols <= 0 || rows % 8 != 0 || cols % 16 != 0) return SLOPE_ERR_SHAPE;
+  if (!vals || !meta || !t_vals || !t_meta) return SLOPE_ERR_INVALID_ARG;
+  if (!aligned16(vals) || !aligned16(meta) || !aligned16(t_vals) || !aligned16(t_meta))
+    return SLOPE_ERR_ALIGNMENT;
+  if (int s = check_device()) return s;
+  return from_cuda(launch_double_prune24(vals, meta, rows, cols, t_vals, t_meta,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+// Shared size rules of the three GEMM calls.
+static int check_linear(int64_t T, int64_t in, int64_t out, int r) {
+  if (T < 0 || in <= 0 || out <= 0 || in % 128 != 0 || out % 128 != 0) return SLOPE_ERR_SHAPE;
+  if (r < 0 || r > 256 || r % 8 != 0) return SLOPE_ERR_SHAPE;
+  if (T > (int64_t(1) << 31) - 1 || in > (int64_t(1) << 31) - 1 || out > (int64_t(1) << 31) - 1)
+    return SLOPE_ERR_SHAPE;
+  return SLOPE_OK;
+}
+
+extern "C" int slope_linear_fwd(const void* X, int64_t T, int64_t in, int64_t out, const void* Wv,
+                                const uint8_t* Wm, const void* L, const void* R, int r, void* Y,
+                                int y_dtype, void* XL, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  (void)workspace; (void)workspace_bytes;
+  if (int s = check_linear(T, in, out, r)) return s;
+  if (y_dtype != SLOPE_F32 && y_dtype != SLOPE_BF16) return SLOPE_ERR_INVALID_ARG;
+  if (T == 0) return SLOPE_OK;
+  if (!X || !Wv || !Wm || !Y) return SLOPE_ERR_INVALID_ARG;
+  if (r > 0 && (!L || !R || !XL)) return SLOPE_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Wv) || !aligned16(Wm) || !aligned16(Y)) return SLOPE_ERR_ALIGNMENT;
+  if (r > 0 && (!aligned16(L) || !aligned16(R) || !aligned16(XL))) return SLOPE_ERR_ALIGNMENT;
+  if (int s = check_device()) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (r > 0) {
+    // XL = X·L as hi/lo bf16 (T x 2r): M = T, N = r, K = in; A = X K-major, B = L MN-major.
+    DenseGemmArgs g{};
+    g.a = X; g.b = L; g.a_mn_major = false; g.b_mn_major = true;
+    g.M = T; g.N = r; g.K = in; g.lda = in; g.ldb = r;
+    g.epi = DenseEpi::StoreBf16HiLo; g.out = XL; g.ldo = 2 * r; g.lo_off = r; g.splits = 1;
+    if (cudaError_t e = launch_dense_gemm(g, st)) return SLOPE_ERR_CUDA;
+  }
+  SparseGemmArgs a{};
+  a.a_vals = Wv; a.a_meta = Wm; a.b = X;
+  a.a2 = r > 0 ? R : nullptr; a.b2 = r > 0 ? XL : nullptr; a.a2_mn_major = true;
+  a.M = out; a.N = T; a.K = in; a.r = r; a.out = Y; a.out_bf16 = (y_dtype == SLOPE_BF16);
+  return from_cuda(launch_sparse_gemm(a, st));
+}
+
+extern "C" int slope_linear_bwd_input(const void* dY, int64_t T, int64_t in, int64_t out,
+                                      const void* Dv, const uint8_t* Dm, const void* L,
+                                      const void* R, int r, void* dX, int dx_dtype, void* G,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  (void)workspace; (void)workspace_bytes;
+  if (int s = check_linear(T, in, out, r)) return s;
+  if (dx_dtype != SLOPE_F32 && dx_dtype != SLOPE_BF16) return SLOPE_ERR_INVALID_ARG;
+  if (T == 0) return SLOPE_OK;
+  if (!dY || !Dv || !Dm || !dX) return SLOPE_ERR_INVALID_ARG;
+  if (r > 0 && (!L || !R || !G)) return SLOPE_ERR_INVALID_ARG;
+  if (!aligned16(dY) || !aligned16(Dv) || !aligned16(Dm) || !aligned16(dX))
+    return SLOPE_ERR_ALIGNMENT;
+  if (r > 0 && (!aligned16(L) || !aligned16(R) || !aligned16(G))) return SLOPE_ERR_ALIGNMENT;
+  if (int s = check_device()) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (r > 0) {
+    // G = dY·Rᵀ as hi/lo bf16 (T x 2r): M = T, N = r, K = out; A = dY K-major, B = R K-major.
+    DenseGemmArgs g{};
+    g.a = dY; g.b = R; g.a_mn_major = false; g.b_mn_major = false;
+    g.M = T; g.N = r; g.K = out; g.lda = out; g.ldb = out;
+    g.epi = DenseEpi::StoreBf16HiLo; g.out = G; g.ldo = 2 * r; g.lo_off = r; g.splits = 1;
+    if (cudaError_t e = launch_dense_gemm(g, st)) return SLOPE_ERR_CUDA;
+  }
+  SparseGemmArgs a{};
+  a.a_vals = Dv; a.a_meta = Dm; a.b = dY;
+  a.a2 = r > 0 ? L : nullptr; a.b2 = r > 0 ? G : nullptr; a.a2_mn_major = false;
+  a.M = in; a.N = T; a.K = out; a.r = r; a.out = dX; a.out_bf16 = (dx_dtype == SLOPE_BF16);
+  return from_cuda(launch_sparse_gemm(a, st));
+}
+
+extern "C" int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T, int64_t in,
+                                       int64_t out, const uint8_t* Wm, const void* XL,
+                                       const void* G, int r, float* dW, uint32_t flags, float* dL,
+                                       float* dR, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+  (void)workspace; (void)workspace_bytes;
+  if (int s = check_linear(T, in, out, r)) return s;
+  if (flags & ~(SLOPE_DW_DENSE | SLOPE_ACCUMULATE)) return SLOPE_ERR_INVALID_ARG;
+  if (!Wm || !dW) return SLOPE_ERR_INVALID_ARG;
+  if (T > 0 && (!dY || !X)) return SLOPE_ERR_INVALID_ARG;
+  if (r > 0 && (!dL || !dR || (T > 0 && (!XL || !G)))) return SLOPE_ERR_INVALID_ARG;
+  if (!aligned16(Wm) || !aligned16(dW) || (T > 0 && (!aligned16(dY) || !aligned16(X))))
+    return SLOPE_ERR_ALIGNMENT;
+  if (r > 0 && (!aligned16(dL) || !aligned16(dR) || (T > 0 && (!aligned16(XL) || !aligned16(G)))))
+    return SLOPE_ERR_ALIGNMENT;
+  if (int s = check_device()) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool dense = flags & SLOPE_DW_DENSE, acc = flags & SLOPE_ACCUMULATE;
+  const size_t dw_bytes = static_cast<size_t>(out) * (dense ? in : in / 2) * sizeof(float);
+  if (T == 0) {
+    if (!acc) {
+      if (cudaMemsetAsync(dW, 0, dw_bytes, st) != cudaSuccess) return SLOPE_ERR_CUDA;
+      if (r > 0 && (cudaMemsetAsync(dL, 0, sizeof(float) * in * r, st) != cudaSuccess ||
+                    cudaMemsetAsync(dR, 0, sizeof(float) * out * r, st) != cudaSuccess))
+        return SLOPE_ERR_CUDA;
+    }
+    return SLOPE_OK;
+  }
+  // dW = M ⊙ (dYᵀ·X): M = out, N = in, K = T; A = dY MN-major, B = X MN-major.
+  DenseGemmArgs w{};
+  w.a = dY; w.b = X; w.a_mn_major = true; w.b_mn_major = true;
+  w.M = out; w.N = in; w.K = T; w.lda = out; w.ldb = in;
+  w.epi = DenseEpi::MaskedWeightGrad; w.out = dW; w.ldo = dense ? in : in / 2;
+  w.meta = Wm; w.dense_dw = dense; w.accumulate = acc; w.splits = 1;
+  if (launch_dense_gemm(w, st) != cudaSuccess) return SLOPE_ERR_CUDA;
+  if (r == 0) return SLOPE_OK;
+  if (!acc) {
+    if (cudaMemsetAsync(dL, 0, sizeof(float) * in * r, st) != cudaSuccess ||
+        cudaMemsetAsync(dR, 0, sizeof(float) * out * r, st) != cudaSuccess)
+      return SLOPE_ERR_CUDA;
+  }
+  // dL = Xᵀ·G (in x r): M = in, N = 2r (hi and lo parts of G), K = T;
+  // A = X MN-major, B = G MN-major; column j + r folds onto column j.
+  DenseGemmArgs l{};
+  l.a = X; l.b = G; l.a_mn_major = true; l.b_mn_major = true;
+  l.M = in; l.N = 2 * r; l.K = T; l.lda = in; l.ldb = 2 * r;
+  l.epi = DenseEpi::AddF32; l.out = dL; l.ldo = r; l.fold = r; l.splits = 0;  // 0 = choose
+  if (launch_dense_gemm(l, st) != cudaSuccess) return SLOPE_ERR_CUDA;
+  // dR = XLᵀ·dY (r x out), computed as dRᵀ = dYᵀ·XL: M = out, N = 2r, K = T;
+  // A = dY MN-major, B = XL MN-major, stored transposed and folded onto r rows.
+  DenseGemmArgs q{};
+  q.a = dY; q.b = XL; q.a_mn_major = true; q.b_mn_major = true;
+  q.M = out; q.N = 2 * r; q.K = T; q.lda = out; q.ldb = 2 * r;
+  q.epi = DenseEpi::AddF32Transposed; q.out = dR; q.ldo = out; q.fold = r; q.splits = 0;
+  return from_cuda(launch_dense_gemm(q, st));
+}
+
+extern "C" int slope_device_status(void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SLOPE_ERR_CUDA;
+  unsigned int* p = device_status_ptr();
+  if (!p) return SLOPE_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return SLOPE_ERR_CUDA;
+  if (v == 0) return SLOPE_OK;
+  const unsigned int zero = 0;
+  if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return SLOPE_ERR_CUDA;
+  return SLOPE_ERR_TIMEOUT;
+}

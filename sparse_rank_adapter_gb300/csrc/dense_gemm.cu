@@ -1,0 +1,399 @@
+// dense_gemm.cu — dense tcgen05 GEMMs of the path.
+//
+//   A5  dW  = M ⊙ (dYᵀ·X)   masked weight gradient; the epilogue applies the
+//       weight's own 2:4 mask and writes only the kept entries (or a dense
+//       masked matrix).  Source: "SLoPe: Double-Pruned Sparse Plus Lazy
+//       Low-Rank Adapter Pretraining of LLMs", §2.3 and App. K (gradients of
+//       pruned weights are masked and stored without their zeros).
+//   A6  the adapter products of §2.2: XL = X·L and G = dY·Rᵀ, written as
+//       hi/lo bf16 pairs (hi = bf16(v), lo = bf16(v - hi): about 16
+//       significant bits, so the tensor cores can take them at nearly fp32
+//       accuracy), then dL = Xᵀ·G and dR = XLᵀ·dY over both parts, folded
+//       back onto r columns in the epilogue.
+//
+//   D[m][n] = Σ_k A[m][k]·B[n][k]; A and B are bf16, stored either K-major
+//   (row = m or n) or MN-major (row = k), as the row-major tensors of the
+//   layer happen to be.  Tile 128 x BN x 64, TMA-fed smem ring, fp32 TMEM
+//   accumulator, optional split-K with atomic fp32 accumulation.
+//
+// Roles (192 threads): warp 0 TMA, warp 1 TMEM owner + MMA issuer, warps
+// 2..5 epilogue.  Every mbarrier wait is bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "slope_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace slope {
+namespace {
+
+constexpr int kBM = 128, kBK = 64;
+constexpr int kA_BYTES = kBM * kBK * 2;  // 16 KB
+constexpr int kThreads = 192;
+
+template <int BN>
+struct DnCfg {
+  static constexpr int B_BYTES = BN * kBK * 2;
+  static constexpr int STAGE = kA_BYTES + B_BYTES;
+  static constexpr int STAGES = (192 * 1024) / STAGE > 8 ? 8 : (192 * 1024) / STAGE;
+  static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
+  static constexpr int SMEM = STAGES * STAGE + 1024 + 1024;
+  // MN-major B: swizzle atom width in elements (64 for SW128) and its code.
+  static constexpr int B_ATOM = BN >= 64 ? 64 : BN;
+  static constexpr uint32_t B_SWZ = BN >= 64 ? kSwizzle128 : BN == 32 ? kSwizzle64 : kSwizzle32;
+  static_assert(STAGE % 1024 == 0, "stage must keep 1024-byte alignment");
+};
+
+struct DnParams {
+  int M, N, K;
+  int kb_per_split, num_kb;
+  int64_t ldo;
+  void* out;
+  const uint8_t* meta;  // masked dW: metadata, N/8 bytes per row
+  int dense_dw, accumulate, atomic_out;
+  int lo_off, fold;
+  unsigned int* status;
+};
+
+__device__ __forceinline__ float pick3(uint32_t i, float a, float b, float c) {
+  return i == 0 ? a : (i == 1 ? b : c);
+}
+
+template <bool A_MN, bool B_MN, int BN, DenseEpi EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    dense_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB, const DnParams p) {
+  using C = DnCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  const int m0 = blockIdx.x * kBM;
+  const int n0 = blockIdx.y * BN;
+  const int kb0 = blockIdx.z * p.kb_per_split;
+  const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+  const int total = kb1 - kb0;  // >= 1 by construction of the grid
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------ TMA producer -------
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    int issued = 0;
+    for (int it = 0; it < total; ++it) {
+      const int s = it % C::STAGES;
+      const uint32_t ph = (it / C::STAGES) & 1;
+      if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.status)) break;
+      uint8_t* sA = smem + s * C::STAGE;
+      uint8_t* sB = sA + kA_BYTES;
+      const int k0 = (kb0 + it) * kBK;
+      mbar_arrive_expect_tx(&full[s], C::STAGE);
+      if (A_MN) {
+        tma_load_2d(sA, &tmA, &full[s], m0, k0);
+        tma_load_2d(sA + 8192, &tmA, &full[s], m0 + 64, k0);
+      } else {
+        tma_load_2d(sA, &tmA, &full[s], k0, m0);
+      }
+      if (B_MN) {
+#pragma unroll
+        for (int a = 0; a < BN / C::B_ATOM; ++a)
+          tma_load_2d(sB + a * (C::B_ATOM * kBK * 2), &tmB, &full[s], n0 + a * C::B_ATOM, k0);
+      } else {
+        tma_load_2d(sB, &tmB, &full[s], k0, n0);
+      }
+      ++issued;
+    }
+    for (int it = issued - 1; it >= 0 && it >= issued - C::STAGES; --it) {
+      volatile int no_abort = 0;
+      mbar_wait(&full[it % C::STAGES], (it / C::STAGES) & 1, &no_abort, p.status);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------ MMA issuer ---------
+    const uint32_t idesc = idesc_bf16(kBM, BN, A_MN, B_MN, false);
+    constexpr uint32_t b_swz_bytes = C::B_ATOM * 2;  // MN-major B swizzle span
+    for (int it = 0; it < total; ++it) {
+      const int s = it % C::STAGES;
+      const uint32_t ph = (it / C::STAGES) & 1;
+      if (!mbar_wait(&full[s], ph, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t aA = smem_u32(smem + s * C::STAGE);
+      const uint32_t aB = aA + kA_BYTES;
+#pragma unroll
+      for (int j = 0; j < kBK / 16; ++j) {
+        const uint64_t da = A_MN ? smem_desc(aA + j * 2048, 8192, 1024, kSwizzle128)
+                                 : smem_desc(aA + j * 32, 0, 1024, kSwizzle128);
+        const uint64_t db =
+            B_MN ? smem_desc(aB + j * 16 * b_swz_bytes, C::B_ATOM * kBK * 2, 8 * b_swz_bytes,
+                             C::B_SWZ)
+                 : smem_desc(aB + j * 32, 0, 1024, kSwizzle128);
+        mma_bf16_ss(tmem, da, db, idesc, (it > 0 || j > 0) ? 1u : 0u);
+      }
+      mma_commit(&empty[s]);
+    }
+    mma_commit(acc_full);
+  } else if (warp >= 2) {
+    // ------------------------------------------------ epilogue -----------
+    const int q = warp & 3;
+    const int m = m0 + 32 * q + lane;
+    if (mbar_wait(acc_full, 0, abort_flag, p.status)) {
+      tc_fence_after();
+      const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q) << 16);
+      constexpr int CH = BN < 32 ? BN : 32;
+      uint4 mrow[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+      if constexpr (EPI == DenseEpi::MaskedWeightGrad) {
+        if (m < p.M) {
+          const uint4* mp = reinterpret_cast<const uint4*>(p.meta + static_cast<size_t>(m) * (p.N / 8) + n0 / 8);
+          mrow[0] = mp[0];
+          if (n0 + 128 < p.N) mrow[1] = mp[1];
+        }
+      }
+      for (int c0 = 0; c0 < BN; c0 += CH) {
+        uint32_t v[32];
+        if constexpr (CH == 32) {
+          tmem_ld_32x32b_x32(trow + c0, v);
+        } else {
+          uint32_t w[4];
+#pragma unroll
+          for (int u = 0; u < CH / 4; ++u) {
+            tmem_ld_32x32b_x4(trow + c0 + 4 * u, w);
+            v[4 * u] = w[0]; v[4 * u + 1] = w[1]; v[4 * u + 2] = w[2]; v[4 * u + 3] = w[3];
+          }
+        }
+        tmem_ld_wait();
+        if (m >= p.M) continue;
+        if constexpr (EPI == DenseEpi::StoreBf16HiLo) {
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(m) * p.ldo;
+#pragma unroll
+          for (int j = 0; j < CH; j += 8) {
+            const int n = n0 + c0 + j;
+            if (n < p.N) {  // N % 8 == 0
+              uint4 hi, lo;
+              uint32_t* ph = reinterpret_cast<uint32_t*>(&hi);
+              uint32_t* pl = reinterpret_cast<uint32_t*>(&lo);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float a = __uint_as_float(v[j + 2 * u]), b = __uint_as_float(v[j + 2 * u + 1]);
+                const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+                const __nv_bfloat162 l =
+                    __floats2bfloat162_rn(a - __bfloat162float(h.x), b - __bfloat162float(h.y));
+                ph[u] = *reinterpret_cast<const uint32_t*>(&h);
+                pl[u] = *reinterpret_cast<const uint32_t*>(&l);
+              }
+              *reinterpret_cast<uint4*>(o + n) = hi;
+              *reinterpret_cast<uint4*>(o + p.lo_off + n) = lo;
+            }
+          }
+        } else if constexpr (EPI == DenseEpi::AddF32) {
+          float* o = static_cast<float*>(p.out) + static_cast<size_t>(m) * p.ldo;
+#pragma unroll
+          for (int j = 0; j < CH; ++j) {
+            const int n = n0 + c0 + j;
+            if (n < p.N) red_add_f32(o + (p.fold && n >= p.fold ? n - p.fold : n), __uint_as_float(v[j]));
+          }
+        } else if constexpr (EPI == DenseEpi::AddF32Transposed) {
+          float* o = static_cast<float*>(p.out);
+#pragma unroll
+          for (int j = 0; j < CH; ++j) {
+            const int n = n0 + c0 + j;
+            const int nf = p.fold && n >= p.fold ? n - p.fold : n;
+            if (n < p.N) red_add_f32(o + static_cast<size_t>(nf) * p.ldo + m, __uint_as_float(v[j]));
+          }
+        } else {  // MaskedWeightGrad: 32 columns = 8 groups = one metadata word
+          const int nb = n0 + c0;
+          if (nb >= p.N) continue;
+          const int wi = c0 / 32;
+          const uint32_t* mw = reinterpret_cast<const uint32_t*>(mrow);
+          const uint32_t word = mw[wi];
+          float* orow = static_cast<float*>(p.out) + static_cast<size_t>(m) * p.ldo;
+          if (p.dense_dw) {
+            float d[32];
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              const uint32_t nib = (word >> (4 * g)) & 0xFu;
+              const uint32_t i0 = nib & 3u, i1 = nib >> 2;
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj)
+                d[4 * g + jj] = (jj == static_cast<int>(i0) || jj == static_cast<int>(i1))
+                                    ? __uint_as_float(v[4 * g + jj]) : 0.0f;
+            }
+            float4* dst = reinterpret_cast<float4*>(orow + nb);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              float4 x = make_float4(d[4 * u], d[4 * u + 1], d[4 * u + 2], d[4 * u + 3]);
+              if (p.atomic_out) {
+                red_add_f32(&dst[u].x, x.x); red_add_f32(&dst[u].y, x.y);
+                red_add_f32(&dst[u].z, x.z); red_add_f32(&dst[u].w, x.w);
+              } else {
+                if (p.accumulate) {
+                  const float4 y = dst[u];
+                  x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+                }
+                dst[u] = x;
+              }
+            }
+          } else {
+            float kept[16];
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              const uint32_t nib = (word >> (4 * g)) & 0xFu;
+              const uint32_t i0 = nib & 3u, i1 = nib >> 2;
+              const float a = __uint_as_float(v[4 * g]), b = __uint_as_float(v[4 * g + 1]);
+              const float c = __uint_as_float(v[4 * g + 2]), d = __uint_as_float(v[4 * g + 3]);
+              kept[2 * g] = pick3(i0, a, b, c);
+              kept[2 * g + 1] = i1 == 3 ? d : (i1 == 2 ? c : b);
+            }
+            float4* dst = reinterpret_cast<float4*>(orow + nb / 2);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              float4 x = make_float4(kept[4 * u], kept[4 * u + 1], kept[4 * u + 2], kept[4 * u + 3]);
+              if (p.atomic_out) {
+                red_add_f32(&dst[u].x, x.x); red_add_f32(&dst[u].y, x.y);
+                red_add_f32(&dst[u].z, x.z); red_add_f32(&dst[u].w, x.w);
+              } else {
+                if (p.accumulate) {
+                  const float4 y = dst[u];
+                  x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+                }
+                dst[u] = x;
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    volatile int no_abort = 0;
+    mbar_wait(acc_full, 0, &no_abort, p.status);
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <bool A_MN, bool B_MN, int BN, DenseEpi EPI>
+cudaError_t run(const DenseGemmArgs& a, cudaStream_t stream) {
+  using C = DnCfg<BN>;
+  auto kernel = dense_gemm_kernel<A_MN, B_MN, BN, EPI>;
+  static std::atomic<int> attr_set[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev].load()) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev].store(1);
+  }
+  const uint64_t M = a.M, N = a.N, K = a.K;
+  CUtensorMap tA, tB;
+  bool ok;
+  if (A_MN)  // stored K x M (row stride lda)
+    ok = make_tmap_2d(&tA, a.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, 2 * a.lda, 64, kBK, Swz::B128);
+  else       // stored M x K
+    ok = make_tmap_2d(&tA, a.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, M, 2 * a.lda, kBK, kBM, Swz::B128);
+  if (B_MN) {
+    const Swz sw = C::B_ATOM == 64 ? Swz::B128 : C::B_ATOM == 32 ? Swz::B64 : Swz::B32;
+    ok = ok && make_tmap_2d(&tB, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, 2 * a.ldb, C::B_ATOM, kBK, sw);
+  } else {
+    ok = ok && make_tmap_2d(&tB, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, 2 * a.ldb, kBK, BN, Swz::B128);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+
+  const int num_kb = static_cast<int>((K + kBK - 1) / kBK);
+  const int tiles_m = static_cast<int>((M + kBM - 1) / kBM);
+  const int tiles_n = static_cast<int>((N + BN - 1) / BN);
+  int splits = a.splits;
+  if (splits <= 0) {
+    const int tiles = tiles_m * tiles_n;
+    splits = (2 * sm_count() + tiles - 1) / tiles;
+    const int max_split = num_kb / 4 > 0 ? num_kb / 4 : 1;
+    if (splits > max_split) splits = max_split;
+    if (splits < 1) splits = 1;
+  }
+  if (EPI == DenseEpi::StoreBf16HiLo) splits = 1;
+  const int kbs = (num_kb + splits - 1) / splits;
+  splits = (num_kb + kbs - 1) / kbs;  // every split owns >= 1 K-block
+
+  DnParams p;
+  p.M = static_cast<int>(M); p.N = static_cast<int>(N); p.K = static_cast<int>(K);
+  p.kb_per_split = kbs; p.num_kb = num_kb;
+  p.ldo = a.ldo; p.out = a.out; p.meta = a.meta;
+  p.dense_dw = a.dense_dw ? 1 : 0;
+  p.accumulate = a.accumulate ? 1 : 0;
+  p.atomic_out = 0;
+  p.lo_off = a.lo_off;
+  p.fold = a.fold;
+  if (EPI == DenseEpi::MaskedWeightGrad && splits > 1) {
+    p.atomic_out = 1;
+    if (!a.accumulate) {
+      const size_t bytes = static_cast<size_t>(M) * a.ldo * sizeof(float);
+      if (cudaError_t e = cudaMemsetAsync(a.out, 0, bytes, stream)) return e;
+    }
+  }
+  p.status = device_status_ptr();
+  if (!p.status) return cudaErrorInvalidDevicePointer;
+  dim3 grid(tiles_m, tiles_n, splits);
+  kernel<<<grid, kThreads, C::SMEM, stream>>>(tA, tB, p);
+  return cudaGetLastError();
+}
+
+// N tile for the skinny (rank-wide) products.
+template <bool A_MN, bool B_MN, DenseEpi EPI>
+cudaError_t run_rank(const DenseGemmArgs& a, cudaStream_t stream) {
+  if (a.N <= 16) return run<A_MN, B_MN, 16, EPI>(a, stream);
+  if (a.N <= 32) return run<A_MN, B_MN, 32, EPI>(a, stream);
+  if (a.N <= 64) return run<A_MN, B_MN, 64, EPI>(a, stream);
+  if (a.N <= 128) return run<A_MN, B_MN, 128, EPI>(a, stream);
+  return run<A_MN, B_MN, 256, EPI>(a, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_dense_gemm(const DenseGemmArgs& a, cudaStream_t stream) {
+  switch (a.epi) {
+    case DenseEpi::MaskedWeightGrad:  // dW: A = dY (T x out), B = X (T x in), both MN-major
+      if (a.a_mn_major && a.b_mn_major) return run<true, true, 256, DenseEpi::MaskedWeightGrad>(a, stream);
+      break;
+    case DenseEpi::StoreBf16HiLo:  // XL = X·L (B MN-major) or G = dY·Rᵀ (B K-major)
+      if (!a.a_mn_major && a.b_mn_major) return run_rank<false, true, DenseEpi::StoreBf16HiLo>(a, stream);
+      if (!a.a_mn_major && !a.b_mn_major) return run_rank<false, false, DenseEpi::StoreBf16HiLo>(a, stream);
+      break;
+    case DenseEpi::AddF32:  // dL = Xᵀ·G
+      if (a.a_mn_major && a.b_mn_major) return run_rank<true, true, DenseEpi::AddF32>(a, stream);
+      break;
+    case DenseEpi::AddF32Transposed:  // dRᵀ = dYᵀ·XL
+      if (a.a_mn_major && a.b_mn_major) return run_rank<true, true, DenseEpi::AddF32Transposed>(a, stream);
+      break;
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace slope

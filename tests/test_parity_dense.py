@@ -1,0 +1,49 @@
+"""A5/A6 alone (dense tcgen05 GEMMs only): the weight gradient with its mask
+epilogue and the adapter gradients, on XL and G taken from the oracle in the
+library's hi/lo bf16 form, so this file needs no sparse kernel."""
+
+import numpy as np
+import pytest
+
+from oracle import slope_oracle as O
+from sparse_rank_adapter_gb300 import synth
+from tests.helpers import assert_close_rel, ensure_built, hilo_bits, to_dev, u8_to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def S():
+    ensure_built()
+    from sparse_rank_adapter_gb300 import slope
+
+    return slope
+
+
+@pytest.mark.parametrize("T,inp,out,r", [(64, 256, 256, 8), (200, 384, 512, 16), (1, 128, 128, 8),
+                                         (4096, 1024, 1024, 16), (1000, 640, 896, 64), (333, 256, 384, 24)])
+@pytest.mark.parametrize("dense", [False, True])
+def test_weight_and_adapter_grads(S, T, inp, out, r, dense):
+    import torch
+
+    d = synth.layer_inputs(0, 300 + T + r, T, inp, out, r)
+    vals, meta, mask = O.prune24(d["W"])
+    _, XL = O.linear_fwd(d["X"], vals, meta, d["L"], d["R"])
+    tv, tm, _ = O.double_prune24(vals, meta, out, inp)
+    _, G = O.linear_bwd_input(d["dY"], tv, tm, d["L"], d["R"])
+    dWc, dWd, dL, dR = O.linear_bwd_weight(d["dY"], d["X"], meta, d["L"], d["R"])
+    dW = torch.full((out, inp) if dense else (out, inp // 2), float("nan"), device="cuda")
+    gdL = torch.full((inp, r), float("nan"), device="cuda")
+    gdR = torch.full((r, out), float("nan"), device="cuda")
+    S.slope_linear_bwd_weight(to_dev(d["dY"]), to_dev(d["X"]), u8_to_dev(meta), to_dev(hilo_bits(XL)),
+                              to_dev(hilo_bits(G)), dW, gdL, gdR, flags=S.DW_DENSE if dense else 0)
+    torch.cuda.synchronize()
+    S.slope_device_status()
+    got = dW.double().cpu().numpy()
+    if dense:
+        assert (got[~mask] == 0).all()
+        assert_close_rel("dW dense", got, dWd)
+    else:
+        assert_close_rel("dW", got, dWc)
+    assert_close_rel("dL", gdL.double().cpu().numpy(), dL)
+    assert_close_rel("dR", gdR.double().cpu().numpy(), dR)
