@@ -1,0 +1,508 @@
+"""Benchmark of the 2:4-sparse + low-rank adapter linear path on GB300.
+
+One step = the whole path over one OPT-shaped decoder block (six linears:
+Q, K, V, O, FC1, FC2) for one batch of synthetic tokens:
+    prune (A1) -> double prune (A2) -> forward (A3) -> input gradient (A4)
+    -> masked weight gradient and adapter gradients (A5, A6)
+all through the C ABI (libslope.so), on one stream, captured once as a CUDA
+graph per input set and replayed.  Inputs are seeded synthetic bf16 tensors
+resident in HBM; four input sets are rotated so that consecutive steps never
+find their inputs in L2.
+
+Metric: dense-equivalent TFLOP/s of fwd + bwd (2·T·in·out for each of the
+forward, input-gradient and weight-gradient products plus 6·T·r·(in+out)
+for the adapter), whole job, summed over ranks.
+
+--impl reference times the CPU oracle (the plain fp64 NumPy definition of
+the same step) on the host cores, on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_rank_adapter_gb300 import synth  # noqa: E402
+
+L2_BYTES = 129 * 2**20
+
+
+def flops_per_step(wl) -> float:
+    T, r = wl.tokens, wl.rank
+    f = 0.0
+    for lin in wl.linears:
+        f += 2.0 * T * lin.inp * lin.out * (1 if wl.forward_only else 3)
+        if r:
+            f += (2.0 if wl.forward_only else 6.0) * T * r * (lin.inp + lin.out)
+    return f
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p["bf16_tflops_sustained"], "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------ clocks -------
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- GPU arm ----
+
+
+class BlockStep:
+    """Device buffers and the ordered ABI calls of one block step."""
+
+    def __init__(self, wl, seed: int, device):
+        import torch
+
+        from sparse_rank_adapter_gb300 import slope
+
+        self.S = slope
+        self.wl = wl
+        T, r = wl.tokens, wl.rank
+        self.layers = []
+        for li, lin in enumerate(wl.linears):
+            inp, out = lin.inp, lin.out
+            s = seed * 1000 + li
+            b = dict(
+                W=synth.device_normal_bf16((out, inp), 0.02, s * 8 + 0, device),
+                X=synth.device_normal_bf16((T, inp), 1.0, s * 8 + 1, device),
+                dY=synth.device_normal_bf16((T, out), 1.0, s * 8 + 2, device),
+                L=synth.device_normal_bf16((inp, r), 0.02, s * 8 + 3, device) if r else None,
+                R=synth.device_normal_bf16((r, out), 0.02, s * 8 + 4, device) if r else None,
+                Wv=torch.empty(out, inp // 2, dtype=torch.bfloat16, device=device),
+                Wm=torch.empty(out, inp // 8, dtype=torch.uint8, device=device),
+                Dv=torch.empty(inp, out // 2, dtype=torch.bfloat16, device=device),
+                Dm=torch.empty(inp, out // 8, dtype=torch.uint8, device=device),
+                Y=torch.empty(T, out, dtype=torch.float32, device=device),
+                XL=torch.empty(T, 2 * r, dtype=torch.bfloat16, device=device) if r else None,
+                dX=torch.empty(T, inp, dtype=torch.float32, device=device),
+                G=torch.empty(T, 2 * r, dtype=torch.bfloat16, device=device) if r else None,
+                dW=torch.empty(out, inp // 2, dtype=torch.float32, device=device),
+                dL=torch.empty(inp, r, dtype=torch.float32, device=device) if r else None,
+                dR=torch.empty(r, out, dtype=torch.float32, device=device) if r else None,
+                inp=inp, out=out)
+            self.layers.append(b)
+
+    def input_names(self):
+        return ["W", "X", "dY", "L", "R"]
+
+    def output_names(self):
+        return ["Y", "dX", "dW", "dL", "dR"] if not self.wl.forward_only else ["Y"]
+
+    def run(self, stream, marks=None):
+        """Issues the step on `stream`; `marks` (optional) records an event
+        pair around every ABI call, keyed by call name."""
+        S = self.S
+        for b in self.layers:
+            calls = [
+                ("prune", lambda b=b: S.slope_prune_nm(b["W"], b["Wv"], b["Wm"], stream=stream)),
+                ("double_prune", lambda b=b: S.slope_double_prune(b["Wv"], b["Wm"], b["out"], b["inp"],
+                                                                  b["Dv"], b["Dm"], stream=stream)),
+                ("fwd", lambda b=b: S.slope_linear_fwd(b["X"], b["Wv"], b["Wm"], b["L"], b["R"], b["Y"],
+                                                       b["XL"], stream=stream)),
+            ]
+            if not self.wl.forward_only:
+                calls += [
+                    ("bwd_input", lambda b=b: S.slope_linear_bwd_input(b["dY"], b["Dv"], b["Dm"], b["L"], b["R"],
+                                                                       b["dX"], b["G"], stream=stream)),
+                    ("bwd_weight", lambda b=b: S.slope_linear_bwd_weight(b["dY"], b["X"], b["Wm"], b["XL"], b["G"],
+                                                                         b["dW"], b["dL"], b["dR"], stream=stream)),
+                ]
+            for name, fn in calls:
+                if marks is not None:
+                    e0, e1 = marks.new(name, b)
+                    e0.record(stream)
+                    fn()
+                    e1.record(stream)
+                else:
+                    fn()
+
+    def launches_per_step(self):
+        n = 0
+        for _ in self.layers:
+            n += 2  # prune, double prune
+            n += 2 if self.wl.rank else 1  # fwd: (XL) + sparse
+            if not self.wl.forward_only:
+                n += 2 if self.wl.rank else 1  # bwd_input: (G) + sparse
+                n += 3 if self.wl.rank else 1  # bwd_weight: dW (+ dL, dR)
+        return n
+
+
+class Marks:
+    def __init__(self):
+        self.pairs = []
+
+    def new(self, name, b):
+        import torch
+
+        # external: inside a captured graph these become event-record nodes
+        e0 = torch.cuda.Event(enable_timing=True, external=True)
+        e1 = torch.cuda.Event(enable_timing=True, external=True)
+        self.pairs.append((name, b["inp"], b["out"], e0, e1))
+        return e0, e1
+
+
+def call_flops(name, T, inp, out, r):
+    """Dense-equivalent flops of one ABI call: the main product 2·T·in·out
+    plus the call's two rank-r products, 2·T·r·(in + out)."""
+    if name in ("fwd", "bwd_input", "bwd_weight"):
+        return 2.0 * T * inp * out + 2.0 * T * r * (inp + out)
+    return 0.0
+
+
+def call_bytes(name, T, inp, out, r):
+    if name == "prune":
+        return out * inp * (2 + 1 + 0.125)
+    if name == "double_prune":
+        return out * inp * (1.125 + 1.125)
+    return 0.0
+
+
+def gpu_arm(args):
+    import torch
+    import torch.distributed as dist
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from sparse_rank_adapter_gb300 import build as B
+
+    if rank == 0 or world == 1:
+        B.build()
+    if world > 1:
+        dist.barrier()
+    wl = synth.WORKLOADS[args.workload]
+    stream = torch.cuda.Stream(device=dev)
+    n_sets = max(1, args.sets)
+    sets = [BlockStep(wl, seed=s + 10 * rank, device=dev) for s in range(n_sets)]
+    torch.cuda.synchronize()
+
+    # warm-up (also sets kernel attributes before any capture)
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 1)):
+            sets[i % n_sets].run(stream)
+    stream.synchronize()
+
+    graphs, marks = [], []
+    for st in sets:
+        m = Marks()
+        if args.graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                st.run(stream, m)
+            graphs.append(g)
+        marks.append(m)
+    for i in range(args.warmup):  # warm the graphs too
+        if args.graph:
+            graphs[i % n_sets].replay()
+    torch.cuda.synchronize()
+
+    per_call = {}
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                if args.graph:
+                    graphs[i % n_sets].replay()
+                else:
+                    sets[i % n_sets].run(stream, marks[i % n_sets] if i >= args.steps - n_sets else None)
+        t_end.record(stream)
+        stream.synchronize()
+    if world > 1:
+        dist.barrier()
+    # every graph's event pairs hold the times of its last replay
+    for m in marks[: min(n_sets, args.steps)]:
+        for name, inp, out, e0, e1 in m.pairs:
+            per_call.setdefault(name, []).append((inp, out, e0.elapsed_time(e1)))
+    n_obs = min(n_sets, args.steps)
+    clocks = clk.summary()
+    ms_step = t_start.elapsed_time(t_end) / args.steps
+    calls_ms = {k: sum(x[2] for x in v) / n_obs for k, v in per_call.items()}
+
+    t = torch.tensor([ms_step], device=dev, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_step = float(t.item())
+    fl = flops_per_step(wl)
+    value = fl * world / (ms_step * 1e-3) / 1e12
+
+    # roofline of the dominant call
+    T, r = wl.tokens, wl.rank
+    hbm, bf16, bf16_sus, src = peaks()
+    dom = max(calls_ms, key=calls_ms.get)
+    n_launch = len(per_call[dom]) / n_obs
+    if dom in ("prune", "double_prune"):
+        alg = sum(call_bytes(dom, T, i, o, r) for i, o, _ in per_call[dom]) / n_obs
+        ach = alg / (calls_ms[dom] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm}
+    else:
+        alg = sum(call_flops(dom, T, i, o, r) for i, o, _ in per_call[dom]) / n_obs
+        ach = alg / (calls_ms[dom] * 1e-3) / 1e12
+        peak = bf16_sus * (2.0 if dom in ("fwd", "bwd_input") else 1.0)
+        roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak}
+    roof.update({"kernel": f"slope_{dom}" if dom != "prune" else "slope_prune_nm", "traffic": None,
+                 "peak_source": f"{src} ({'2x ' if dom in ('fwd', 'bwd_input') else ''}bf16 sustained)"
+                 if roof['bound'] == 'tensor' else f"{src} hbm",
+                 "launches_per_step": n_launch})
+
+    e2e = e2e_measure(args, wl, sets[0], stream, dev) if args.e2e else None
+    cpu = None
+    if rank == 0 and args.cpu_baseline:
+        cpu = cpu_baseline(wl, args.cpu_seconds)
+
+    if world > 1:
+        dist.barrier()
+    if rank == 0:
+        line = {
+            "metric": "sparse+LoRA linear fwd+bwd TFLOP/s (dense-equiv) and % of 2:4-sparse bf16 peak",
+            "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "tokens_per_gpu": wl.tokens, "rank": wl.rank,
+                       "linears": [f"{x.name}:{x.inp}->{x.out}" for x in wl.linears],
+                       "l2": f"{n_sets} rotating input sets of {set_bytes(sets[0]) / 2**20:.0f} MiB (> L2 {L2_BYTES // 2**20} MiB)",
+                       "graph": bool(args.graph), "parallelism": f"replicas x{world}"},
+            "pct_of_sparse_peak": round(100 * value / (2 * bf16), 2),
+            "composite_roofline_frac": composite_frac(wl, ms_step, bf16_sus),
+            "calls_ms_per_step": {k: round(v, 4) for k, v in calls_ms.items()},
+            "roofline": roof, "clocks": clocks, "gpu_launches": sets[0].launches_per_step() * args.steps,
+            "e2e": e2e, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def set_bytes(st):
+    tot = 0
+    for b in st.layers:
+        for k, v in b.items():
+            if hasattr(v, "numel"):
+                tot += v.numel() * v.element_size()
+    return tot
+
+
+def composite_frac(wl, ms_step, bf16_sus):
+    """Time the composite roofline allows (sparse products at 2x the dense
+    peak, dense ones at the dense peak) over the measured step time."""
+    T, r = wl.tokens, wl.rank
+    t = 0.0
+    for lin in wl.linears:
+        sparse = 2.0 * T * lin.inp * lin.out * (1 if wl.forward_only else 2)
+        dense = 0.0 if wl.forward_only else 2.0 * T * lin.inp * lin.out
+        if r:
+            dense += (2.0 if wl.forward_only else 6.0) * T * r * (lin.inp + lin.out)
+        t += sparse / (2 * bf16_sus * 1e12) + dense / (bf16_sus * 1e12)
+    return round(t / (ms_step * 1e-3), 4)
+
+
+def e2e_measure(args, wl, st, stream, dev):
+    """The same step through the C ABI with inputs in pinned host memory:
+    host->device copies of every input and device->host copies of every
+    result are inside the timed region."""
+    import torch
+
+    host_in, host_out = [], []
+    for b in st.layers:
+        host_in.append({k: b[k].cpu().pin_memory() for k in st.input_names() if b[k] is not None})
+        host_out.append({k: torch.empty(b[k].shape, dtype=b[k].dtype, pin_memory=True)
+                         for k in st.output_names() if b[k] is not None})
+    h2d = sum(v.numel() * v.element_size() for d in host_in for v in d.values())
+    d2h = sum(v.numel() * v.element_size() for d in host_out for v in d.values())
+
+    def one():
+        with torch.cuda.stream(stream):
+            for b, hi in zip(st.layers, host_in):
+                for k, v in hi.items():
+                    b[k].copy_(v, non_blocking=True)
+            st.run(stream)
+            for b, ho in zip(st.layers, host_out):
+                for k, v in ho.items():
+                    v.copy_(b[k], non_blocking=True)
+
+    for _ in range(2):
+        one()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(3, min(args.steps, 20))
+    e0.record(stream)
+    for _ in range(n):
+        one()
+    e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    return {"value": round(flops_per_step(wl) / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------- CPU arm ----
+
+
+def oracle_sample(wl, budget_s: float):
+    """Times the oracle (as it stands) on the block's linears for a sample of
+    token rows; returns (dense-equivalent flops done, seconds, description)."""
+    import numpy as np
+
+    from oracle import slope_oracle as O
+
+    T = wl.tokens
+    sample_T = min(T, 1024)
+    done, t_total, lins = 0.0, 0.0, 0
+    t0 = time.perf_counter()
+    for li, lin in enumerate(wl.linears):
+        d = synth.layer_inputs(0, li, sample_T, lin.inp, lin.out, wl.rank)
+        L, R = (d["L"], d["R"]) if wl.rank else (None, None)
+        s = time.perf_counter()
+        vals, meta, _ = O.prune24(d["W"])
+        O.linear_fwd(d["X"], vals, meta, L, R)
+        if not wl.forward_only:
+            tv, tm, _ = O.double_prune24(vals, meta, lin.out, lin.inp)
+            O.linear_bwd_input(d["dY"], tv, tm, L, R)
+            O.linear_bwd_weight(d["dY"], d["X"], meta, L, R)
+        t_total += time.perf_counter() - s
+        sub = synth.Workload(wl.name, sample_T, wl.rank, (lin,), wl.forward_only)
+        done += flops_per_step(sub)
+        lins += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    desc = (f"{lins} of {len(wl.linears)} linears of {wl.name}, {sample_T} of {T} tokens each "
+            f"(full prune and double prune of every weight), oracle fp64 NumPy")
+    return done, t_total, desc
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def cpu_baseline(wl, budget_s):
+    done, secs, desc = oracle_sample(wl, budget_s)
+    return {"value": round(done / secs / 1e12, 6), "unit": "TFLOP/s", "cores": cpu_cores(),
+            "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+
+
+def reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = synth.WORKLOADS[args.workload]
+    vals, tot_flops, tot_s, desc = [], 0.0, 0.0, ""
+    for i in range(args.warmup + args.steps):
+        f, s, desc = oracle_sample(wl, args.cpu_seconds)
+        if i >= args.warmup:
+            vals.append(f / s / 1e12)
+            tot_flops += f
+            tot_s += s
+    value = tot_flops / tot_s / 1e12
+    line = {
+        "impl": "reference",
+        "metric": "sparse+LoRA linear fwd+bwd TFLOP/s (dense-equiv) and % of 2:4-sparse bf16 peak",
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * tot_s / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wl.name, "tokens_per_gpu": wl.tokens, "rank": wl.rank},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="slope", choices=["slope", "reference"])
+    ap.add_argument("--workload", default="opt-350m-block", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--sets", type=int, default=4, help="rotating input sets (L2 defeat)")
+    ap.add_argument("--no-graph", dest="graph", action="store_false")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()
