@@ -16,8 +16,10 @@
 //   layer happen to be.  Tile 128 x BN x 64, TMA-fed smem ring, fp32 TMEM
 //   accumulator, optional split-K with atomic fp32 accumulation.
 //
+// Persistent kernel, one CTA per SM, tiles (m, n, split) taken round-robin.
 // Roles (192 threads): warp 0 TMA, warp 1 TMEM owner + MMA issuer, warps
-// 2..5 epilogue.  Every mbarrier wait is bounded.
+// 2..5 epilogue.  The accumulator is double-buffered in TMEM so a tile's
+// epilogue overlaps the next tile's K-loop.  Every mbarrier wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,7 +42,8 @@ struct DnCfg {
   static constexpr int B_BYTES = BN * kBK * 2;
   static constexpr int STAGE = kA_BYTES + B_BYTES;
   static constexpr int STAGES = (192 * 1024) / STAGE > 8 ? 8 : (192 * 1024) / STAGE;
-  static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
+  static constexpr int ACC_COLS = BN < 32 ? 32 : BN;  // one accumulator buffer
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;       // double-buffered
   static constexpr int SMEM = STAGES * STAGE + 1024 + 1024;
   // MN-major B: swizzle atom width in elements (64 for SW128) and its code.
   static constexpr int B_ATOM = BN >= 64 ? 64 : BN;
@@ -51,6 +54,7 @@ struct DnCfg {
 struct DnParams {
   int M, N, K;
   int kb_per_split, num_kb;
+  int tiles_m, tiles_n, num_tiles;  // tiles = tiles_m x tiles_n x splits
   int64_t ldo;
   void* out;
   const uint8_t* meta;  // masked dW: metadata, N/8 bytes per row
@@ -63,6 +67,109 @@ __device__ __forceinline__ float pick3(uint32_t i, float a, float b, float c) {
   return i == 0 ? a : (i == 1 ? b : c);
 }
 
+// One 32-column (or BN-column, when narrower) chunk of a tile row, already in
+// registers: row m of the tile, columns n0 + c0 .. n0 + c0 + CH - 1.
+template <int BN, int CH, DenseEpi EPI>
+__device__ __forceinline__ void epilogue_chunk(const DnParams& p, const uint32_t (&v)[32], int m,
+                                               int n0, int c0, const uint4 (&mrow)[2]) {
+  if constexpr (EPI == DenseEpi::StoreBf16HiLo) {
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(m) * p.ldo;
+#pragma unroll
+    for (int j = 0; j < CH; j += 8) {
+      const int n = n0 + c0 + j;
+      if (n < p.N) {  // N % 8 == 0
+        uint4 hi, lo;
+        uint32_t* ph = reinterpret_cast<uint32_t*>(&hi);
+        uint32_t* pl = reinterpret_cast<uint32_t*>(&lo);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float a = __uint_as_float(v[j + 2 * u]), b = __uint_as_float(v[j + 2 * u + 1]);
+          const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+          const __nv_bfloat162 l =
+              __floats2bfloat162_rn(a - __bfloat162float(h.x), b - __bfloat162float(h.y));
+          ph[u] = *reinterpret_cast<const uint32_t*>(&h);
+          pl[u] = *reinterpret_cast<const uint32_t*>(&l);
+        }
+        *reinterpret_cast<uint4*>(o + n) = hi;
+        *reinterpret_cast<uint4*>(o + p.lo_off + n) = lo;
+      }
+    }
+  } else if constexpr (EPI == DenseEpi::AddF32) {
+    float* o = static_cast<float*>(p.out) + static_cast<size_t>(m) * p.ldo;
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+      const int n = n0 + c0 + j;
+      if (n < p.N) red_add_f32(o + (p.fold && n >= p.fold ? n - p.fold : n), __uint_as_float(v[j]));
+    }
+  } else if constexpr (EPI == DenseEpi::AddF32Transposed) {
+    float* o = static_cast<float*>(p.out);
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+      const int n = n0 + c0 + j;
+      const int nf = p.fold && n >= p.fold ? n - p.fold : n;
+      if (n < p.N) red_add_f32(o + static_cast<size_t>(nf) * p.ldo + m, __uint_as_float(v[j]));
+    }
+  } else {  // MaskedWeightGrad: 32 columns = 8 groups = one metadata word
+    const int nb = n0 + c0;
+    if (nb >= p.N) return;
+    const uint32_t word = reinterpret_cast<const uint32_t*>(mrow)[c0 / 32];
+    float* orow = static_cast<float*>(p.out) + static_cast<size_t>(m) * p.ldo;
+    if (p.dense_dw) {
+      float d[32];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const uint32_t nib = (word >> (4 * g)) & 0xFu;
+        const uint32_t i0 = nib & 3u, i1 = nib >> 2;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+          d[4 * g + jj] = (jj == static_cast<int>(i0) || jj == static_cast<int>(i1))
+                              ? __uint_as_float(v[4 * g + jj]) : 0.0f;
+      }
+      float4* dst = reinterpret_cast<float4*>(orow + nb);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        float4 x = make_float4(d[4 * u], d[4 * u + 1], d[4 * u + 2], d[4 * u + 3]);
+        if (p.atomic_out) {
+          red_add_f32(&dst[u].x, x.x); red_add_f32(&dst[u].y, x.y);
+          red_add_f32(&dst[u].z, x.z); red_add_f32(&dst[u].w, x.w);
+        } else {
+          if (p.accumulate) {
+            const float4 y = dst[u];
+            x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+          }
+          dst[u] = x;
+        }
+      }
+    } else {
+      float kept[16];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const uint32_t nib = (word >> (4 * g)) & 0xFu;
+        const uint32_t i0 = nib & 3u, i1 = nib >> 2;
+        const float a = __uint_as_float(v[4 * g]), b = __uint_as_float(v[4 * g + 1]);
+        const float c = __uint_as_float(v[4 * g + 2]), d = __uint_as_float(v[4 * g + 3]);
+        kept[2 * g] = pick3(i0, a, b, c);
+        kept[2 * g + 1] = i1 == 3 ? d : (i1 == 2 ? c : b);
+      }
+      float4* dst = reinterpret_cast<float4*>(orow + nb / 2);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float4 x = make_float4(kept[4 * u], kept[4 * u + 1], kept[4 * u + 2], kept[4 * u + 3]);
+        if (p.atomic_out) {
+          red_add_f32(&dst[u].x, x.x); red_add_f32(&dst[u].y, x.y);
+          red_add_f32(&dst[u].z, x.z); red_add_f32(&dst[u].w, x.w);
+        } else {
+          if (p.accumulate) {
+            const float4 y = dst[u];
+            x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+          }
+          dst[u] = x;
+        }
+      }
+    }
+  }
+}
+
 template <bool A_MN, bool B_MN, int BN, DenseEpi EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     dense_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -73,23 +180,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
   uint64_t* empty = full + C::STAGES;
-  uint64_t* acc_full = empty + C::STAGES;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
+  uint64_t* acc_full = empty + C::STAGES;  // [2]
+  uint64_t* acc_empty = acc_full + 2;      // [2]
+  uint64_t* mma_done = acc_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = warp_id(), lane = lane_id();
-  const int m0 = blockIdx.x * kBM;
-  const int n0 = blockIdx.y * BN;
-  const int kb0 = blockIdx.z * p.kb_per_split;
-  const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
-  const int total = kb1 - kb0;  // >= 1 by construction of the grid
+  const int tiles_mn = p.tiles_m * p.tiles_n;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(acc_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -102,69 +211,96 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == 0 && lane == 0) {
-    // ------------------------------------------------ TMA producer -------
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-    int issued = 0;
-    for (int it = 0; it < total; ++it) {
-      const int s = it % C::STAGES;
-      const uint32_t ph = (it / C::STAGES) & 1;
-      if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.status)) break;
-      uint8_t* sA = smem + s * C::STAGE;
-      uint8_t* sB = sA + kA_BYTES;
-      const int k0 = (kb0 + it) * kBK;
-      mbar_arrive_expect_tx(&full[s], C::STAGE);
-      if (A_MN) {
-        tma_load_2d(sA, &tmA, &full[s], m0, k0);
-        tma_load_2d(sA + 8192, &tmA, &full[s], m0 + 64, k0);
-      } else {
-        tma_load_2d(sA, &tmA, &full[s], k0, m0);
-      }
-      if (B_MN) {
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------- TMA producer -------
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int it = 0;
+      bool stop = false;
+      for (int tile = blockIdx.x; tile < p.num_tiles && !stop; tile += gridDim.x) {
+        const int mn = tile % tiles_mn, z = tile / tiles_mn;
+        const int m0 = (mn % p.tiles_m) * kBM, n0 = (mn / p.tiles_m) * BN;
+        const int kb0 = z * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.status)) { stop = true; break; }
+          uint8_t* sA = smem + s * C::STAGE;
+          uint8_t* sB = sA + kA_BYTES;
+          const int k0 = kb * kBK;
+          mbar_arrive_expect_tx(&full[s], C::STAGE);
+          if (A_MN) {
+            tma_load_2d(sA, &tmA, &full[s], m0, k0);
+            tma_load_2d(sA + 8192, &tmA, &full[s], m0 + 64, k0);
+          } else {
+            tma_load_2d(sA, &tmA, &full[s], k0, m0);
+          }
+          if (B_MN) {
 #pragma unroll
-        for (int a = 0; a < BN / C::B_ATOM; ++a)
-          tma_load_2d(sB + a * (C::B_ATOM * kBK * 2), &tmB, &full[s], n0 + a * C::B_ATOM, k0);
-      } else {
-        tma_load_2d(sB, &tmB, &full[s], k0, n0);
+            for (int a = 0; a < BN / C::B_ATOM; ++a)
+              tma_load_2d(sB + a * (C::B_ATOM * kBK * 2), &tmB, &full[s], n0 + a * C::B_ATOM, k0);
+          } else {
+            tma_load_2d(sB, &tmB, &full[s], k0, n0);
+          }
+        }
       }
-      ++issued;
+      for (int i = it - 1; i >= 0 && i >= it - C::STAGES; --i) {
+        volatile int no_abort = 0;
+        mbar_wait(&full[i % C::STAGES], (i / C::STAGES) & 1, &no_abort, p.status);
+      }
     }
-    for (int it = issued - 1; it >= 0 && it >= issued - C::STAGES; --it) {
-      volatile int no_abort = 0;
-      mbar_wait(&full[it % C::STAGES], (it / C::STAGES) & 1, &no_abort, p.status);
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------ MMA issuer ---------
-    const uint32_t idesc = idesc_bf16(kBM, BN, A_MN, B_MN, false);
-    constexpr uint32_t b_swz_bytes = C::B_ATOM * 2;  // MN-major B swizzle span
-    for (int it = 0; it < total; ++it) {
-      const int s = it % C::STAGES;
-      const uint32_t ph = (it / C::STAGES) & 1;
-      if (!mbar_wait(&full[s], ph, abort_flag, p.status)) break;
-      tc_fence_after();
-      const uint32_t aA = smem_u32(smem + s * C::STAGE);
-      const uint32_t aB = aA + kA_BYTES;
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------- MMA issuer ---------
+      const uint32_t idesc = idesc_bf16(kBM, BN, A_MN, B_MN, false);
+      constexpr uint32_t b_swz_bytes = C::B_ATOM * 2;  // MN-major B swizzle span
+      int it = 0, local = 0;
+      bool stop = false;
+      for (int tile = blockIdx.x; tile < p.num_tiles && !stop; tile += gridDim.x, ++local) {
+        const int z = tile / tiles_mn;
+        const int kb0 = z * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+        const int buf = local & 1;
+        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * C::ACC_COLS;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1;
+          if (!mbar_wait(&full[s], ph, abort_flag, p.status)) { stop = true; break; }
+          tc_fence_after();
+          const uint32_t aA = smem_u32(smem + s * C::STAGE);
+          const uint32_t aB = aA + kA_BYTES;
 #pragma unroll
-      for (int j = 0; j < kBK / 16; ++j) {
-        const uint64_t da = A_MN ? smem_desc(aA + j * 2048, 8192, 1024, kSwizzle128)
-                                 : smem_desc(aA + j * 32, 0, 1024, kSwizzle128);
-        const uint64_t db =
-            B_MN ? smem_desc(aB + j * 16 * b_swz_bytes, C::B_ATOM * kBK * 2, 8 * b_swz_bytes,
-                             C::B_SWZ)
-                 : smem_desc(aB + j * 32, 0, 1024, kSwizzle128);
-        mma_bf16_ss(tmem, da, db, idesc, (it > 0 || j > 0) ? 1u : 0u);
+          for (int j = 0; j < kBK / 16; ++j) {
+            const uint64_t da = A_MN ? smem_desc(aA + j * 2048, 8192, 1024, kSwizzle128)
+                                     : smem_desc(aA + j * 32, 0, 1024, kSwizzle128);
+            const uint64_t db =
+                B_MN ? smem_desc(aB + j * 16 * b_swz_bytes, C::B_ATOM * kBK * 2, 8 * b_swz_bytes,
+                                 C::B_SWZ)
+                     : smem_desc(aB + j * 32, 0, 1024, kSwizzle128);
+            mma_bf16_ss(d, da, db, idesc, (kb > kb0 || j > 0) ? 1u : 0u);
+          }
+          mma_commit(&empty[s]);
+        }
+        if (!stop) mma_commit(&acc_full[buf]);
       }
-      mma_commit(&empty[s]);
+      mma_commit(mma_done);
     }
-    mma_commit(acc_full);
-  } else if (warp >= 2) {
+  } else {
     // ------------------------------------------------ epilogue -----------
     const int q = warp & 3;
-    const int m = m0 + 32 * q + lane;
-    if (mbar_wait(acc_full, 0, abort_flag, p.status)) {
+    int local = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+      const int mn = tile % tiles_mn;
+      const int m = (mn % p.tiles_m) * kBM + 32 * q + lane;
+      const int n0 = (mn / p.tiles_m) * BN;
+      const int buf = local & 1;
+      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      if (!mbar_wait(&acc_full[buf], use & 1, abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q) << 16);
+      const uint32_t trow = tmem + buf * C::ACC_COLS + (static_cast<uint32_t>(32 * q) << 16);
       constexpr int CH = BN < 32 ? BN : 32;
       uint4 mrow[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
       if constexpr (EPI == DenseEpi::MaskedWeightGrad) {
@@ -174,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (n0 + 128 < p.N) mrow[1] = mp[1];
         }
       }
+#pragma unroll
       for (int c0 = 0; c0 < BN; c0 += CH) {
         uint32_t v[32];
         if constexpr (CH == 32) {
@@ -187,105 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tmem_ld_wait();
-        if (m >= p.M) continue;
-        if constexpr (EPI == DenseEpi::StoreBf16HiLo) {
-          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(m) * p.ldo;
-#pragma unroll
-          for (int j = 0; j < CH; j += 8) {
-            const int n = n0 + c0 + j;
-            if (n < p.N) {  // N % 8 == 0
-              uint4 hi, lo;
-              uint32_t* ph = reinterpret_cast<uint32_t*>(&hi);
-              uint32_t* pl = reinterpret_cast<uint32_t*>(&lo);
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const float a = __uint_as_float(v[j + 2 * u]), b = __uint_as_float(v[j + 2 * u + 1]);
-                const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-                const __nv_bfloat162 l =
-                    __floats2bfloat162_rn(a - __bfloat162float(h.x), b - __bfloat162float(h.y));
-                ph[u] = *reinterpret_cast<const uint32_t*>(&h);
-                pl[u] = *reinterpret_cast<const uint32_t*>(&l);
-              }
-              *reinterpret_cast<uint4*>(o + n) = hi;
-              *reinterpret_cast<uint4*>(o + p.lo_off + n) = lo;
-            }
-          }
-        } else if constexpr (EPI == DenseEpi::AddF32) {
-          float* o = static_cast<float*>(p.out) + static_cast<size_t>(m) * p.ldo;
-#pragma unroll
-          for (int j = 0; j < CH; ++j) {
-            const int n = n0 + c0 + j;
-            if (n < p.N) red_add_f32(o + (p.fold && n >= p.fold ? n - p.fold : n), __uint_as_float(v[j]));
-          }
-        } else if constexpr (EPI == DenseEpi::AddF32Transposed) {
-          float* o = static_cast<float*>(p.out);
-#pragma unroll
-          for (int j = 0; j < CH; ++j) {
-            const int n = n0 + c0 + j;
-            const int nf = p.fold && n >= p.fold ? n - p.fold : n;
-            if (n < p.N) red_add_f32(o + static_cast<size_t>(nf) * p.ldo + m, __uint_as_float(v[j]));
-          }
-        } else {  // MaskedWeightGrad: 32 columns = 8 groups = one metadata word
-          const int nb = n0 + c0;
-          if (nb >= p.N) continue;
-          const int wi = c0 / 32;
-          const uint32_t* mw = reinterpret_cast<const uint32_t*>(mrow);
-          const uint32_t word = mw[wi];
-          float* orow = static_cast<float*>(p.out) + static_cast<size_t>(m) * p.ldo;
-          if (p.dense_dw) {
-            float d[32];
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              const uint32_t nib = (word >> (4 * g)) & 0xFu;
-              const uint32_t i0 = nib & 3u, i1 = nib >> 2;
-#pragma unroll
-              for (int jj = 0; jj < 4; ++jj)
-                d[4 * g + jj] = (jj == static_cast<int>(i0) || jj == static_cast<int>(i1))
-                                    ? __uint_as_float(v[4 * g + jj]) : 0.0f;
-            }
-            float4* dst = reinterpret_cast<float4*>(orow + nb);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              float4 x = make_float4(d[4 * u], d[4 * u + 1], d[4 * u + 2], d[4 * u + 3]);
-              if (p.atomic_out) {
-                red_add_f32(&dst[u].x, x.x); red_add_f32(&dst[u].y, x.y);
-                red_add_f32(&dst[u].z, x.z); red_add_f32(&dst[u].w, x.w);
-              } else {
-                if (p.accumulate) {
-                  const float4 y = dst[u];
-                  x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
-                }
-                dst[u] = x;
-              }
-            }
-          } else {
-            float kept[16];
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              const uint32_t nib = (word >> (4 * g)) & 0xFu;
-              const uint32_t i0 = nib & 3u, i1 = nib >> 2;
-              const float a = __uint_as_float(v[4 * g]), b = __uint_as_float(v[4 * g + 1]);
-              const float c = __uint_as_float(v[4 * g + 2]), d = __uint_as_float(v[4 * g + 3]);
-              kept[2 * g] = pick3(i0, a, b, c);
-              kept[2 * g + 1] = i1 == 3 ? d : (i1 == 2 ? c : b);
-            }
-            float4* dst = reinterpret_cast<float4*>(orow + nb / 2);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              float4 x = make_float4(kept[4 * u], kept[4 * u + 1], kept[4 * u + 2], kept[4 * u + 3]);
-              if (p.atomic_out) {
-                red_add_f32(&dst[u].x, x.x); red_add_f32(&dst[u].y, x.y);
-                red_add_f32(&dst[u].z, x.z); red_add_f32(&dst[u].w, x.w);
-              } else {
-                if (p.accumulate) {
-                  const float4 y = dst[u];
-                  x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
-                }
-                dst[u] = x;
-              }
-            }
-          }
+        if (c0 + CH >= BN) {  // last chunk read: hand the buffer back early
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
         }
+        if (m >= p.M) continue;
+        epilogue_chunk<BN, CH, EPI>(p, v, m, n0, c0, mrow);
       }
     }
   }
@@ -295,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     volatile int no_abort = 0;
-    mbar_wait(acc_full, 0, &no_abort, p.status);
+    mbar_wait(mma_done, 0, &no_abort, p.status);
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
@@ -360,7 +405,9 @@ cudaError_t run(const DenseGemmArgs& a, cudaStream_t stream) {
   }
   p.status = device_status_ptr();
   if (!p.status) return cudaErrorInvalidDevicePointer;
-  dim3 grid(tiles_m, tiles_n, splits);
+  p.tiles_m = tiles_m; p.tiles_n = tiles_n;
+  p.num_tiles = tiles_m * tiles_n * splits;
+  const int grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
   kernel<<<grid, kThreads, C::SMEM, stream>>>(tA, tB, p);
   return cudaGetLastError();
 }

@@ -6,7 +6,8 @@
 // sparse backward) and §2.4 / App. D (the adapter concatenated with the
 // sparse weight and fused with the result addition, so one accumulator takes
 // both).  Here the adapter is an extra dense K-segment: after the sparse
-// K-loop, dense MMAs add A2·B2ᵀ into the same TMEM tile.
+// K-loop, dense MMAs add A2·B2ᵀ into the same TMEM tile, once for the hi and
+// once for the lo bf16 part of the rank-r intermediate.
 //
 //   D[m][n] = Σ_k A[m][k]·B[n][k] + Σ_j A2[m][j]·B2[n][j],   out[n][m] = D[m][n]
 //
@@ -15,15 +16,21 @@
 // the epilogue writes directly (lane = m, so a warp's stores of one column
 // n are 128 contiguous bytes).
 //
-// Roles (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues
-// the MMAs (one elected thread), warps 2..5 move each stage's 2:4 metadata
-// from shared memory into TMEM during the K-loop and drain the accumulator
-// after it.  Every mbarrier wait is bounded.
+// Persistent kernel, one CTA per SM, tiles taken round-robin.  Roles (320
+// threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues the MMAs
+// (one thread), warps 2..5 drain the accumulator, warps 6..9 move each
+// stage's 2:4 metadata from shared memory into TMEM.  The accumulator is
+// double-buffered in TMEM, so the epilogue of one tile overlaps the K-loop
+// of the next.  Every mbarrier wait is bounded.
 //
-// Metadata in TMEM: lane m holds row m; k-step j (32 logical columns = 8
-// groups = one 32-bit word of the row's metadata) of stage s sits in its own
-// column META_COL + 16 s + 4 j, so every sparse MMA reads a 4-column-aligned
-// address with sparsity selector 0.
+// Metadata in TMEM: k-step j (32 logical columns = 8 groups = one 32-bit
+// word per row) of stage s sits in its own column META_COL + 16 s + 4 j, so
+// every sparse MMA reads a 4-column-aligned address with sparsity selector 0.
+// Within each 16-row block the hardware pairs rows i and i + 8 (i < 8) by
+// 16-bit halves: lane i holds [row i groups 0-3 | row i+8 groups 0-3] and
+// lane i + 8 holds [row i groups 4-7 | row i+8 groups 4-7] (measured with
+// identity inputs on sm_103a).  One shuffle per word turns the row-major
+// metadata into that arrangement.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -37,27 +44,39 @@
 namespace slope {
 namespace {
 
-constexpr int kBM = 128;            // weight rows per tile (MMA M)
-constexpr int kBKc = 64;            // compressed A columns per stage (= 128 logical K)
-constexpr int kA_BYTES = kBM * 128;  // 16 KB: 128 rows x 128 B (SW128)
+constexpr int kBM = 128;               // weight rows per tile (MMA M)
+constexpr int kBKc = 64;               // compressed A columns per stage (= 128 logical K)
+constexpr int kA_BYTES = kBM * 128;    // 16 KB: 128 rows x 128 B (SW128)
 constexpr int kMETA_BYTES = kBM * 16;  // 2 KB: 128 rows x 16 B (32 groups)
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 
 template <int BN>
 struct SpCfg {
   static constexpr int B_BYTES = BN * 256;  // two 64-column SW128 atoms of BN rows
   static constexpr int STAGE = kA_BYTES + B_BYTES + kMETA_BYTES;
-  static constexpr int STAGES = BN >= 256 ? 2 : BN >= 128 ? 4 : BN >= 64 ? 6 : 8;
-  static constexpr int META_COL = BN < 32 ? 32 : BN;  // TMEM column of stage 0's metadata
+  static constexpr int STAGES_FIT = (200 * 1024) / STAGE;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int ACC_COLS = BN < 32 ? 32 : BN;  // one accumulator buffer
+  static constexpr int META_COL = 2 * ACC_COLS;        // after the two buffers
   static constexpr int TMEM_NEED = META_COL + 16 * STAGES;
   static constexpr int TMEM_COLS =
       TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
   static constexpr int SMEM = STAGES * STAGE + 1024 /*barriers*/ + 1024 /*align slack*/;
   static_assert(STAGE % 1024 == 0, "stage must keep 1024-byte alignment");
+  static_assert(TMEM_NEED <= 512, "TMEM budget");
+  static_assert(STAGES >= 2, "pipeline depth");
 };
+
+// Row-major metadata word of this lane's row -> the word the sparse MMA
+// expects in this lane (rows i and i+8 of a 16-row block exchange halves).
+__device__ __forceinline__ uint32_t pair_rows(uint32_t w, int lane) {
+  const uint32_t p = __shfl_xor_sync(0xFFFFFFFFu, w, 8);
+  return (lane & 8) ? ((p >> 16) | (w & 0xFFFF0000u)) : ((w & 0xFFFFu) | (p << 16));
+}
 
 struct SpParams {
   int M, N, K, r;
+  int tiles_m, num_tiles;
   int num_kb;      // sparse K-blocks (K / 128)
   int num_ab;      // adapter blocks per part (ceil(r / 64)); parts: hi, lo
   int out_bf16;
@@ -79,14 +98,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
   uint64_t* empty = full + C::STAGES;
   uint64_t* meta_full = empty + C::STAGES;
-  uint64_t* acc_full = meta_full + C::STAGES;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
+  uint64_t* acc_full = meta_full + C::STAGES;  // [2]
+  uint64_t* acc_empty = acc_full + 2;          // [2]
+  uint64_t* mma_done = acc_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = warp_id(), lane = lane_id();
-  const int m0 = blockIdx.x * kBM;
-  const int n0 = blockIdx.y * BN;
-  const int total = p.num_kb + 2 * p.num_ab;
+  const int per_tile = p.num_kb + 2 * p.num_ab;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -94,7 +113,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], 1);
       mbar_init(&meta_full[s], 4);  // one arrival per metadata warp
     }
-    mbar_init(acc_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -107,114 +130,117 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == 0 && lane == 0) {
-    // ------------------------------------------------ TMA producer -------
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-    tma_prefetch_desc(&tmMeta);
-    int issued = 0;
-    for (int it = 0; it < total; ++it) {
-      const int s = it % C::STAGES;
-      const uint32_t ph = (it / C::STAGES) & 1;
-      if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.status)) break;
-      uint8_t* sA = smem + s * C::STAGE;
-      uint8_t* sB = sA + kA_BYTES;
-      uint8_t* sMeta = sB + C::B_BYTES;
-      if (it < p.num_kb) {
-        mbar_arrive_expect_tx(&full[s], kA_BYTES + C::B_BYTES + kMETA_BYTES);
-        tma_load_2d(sA, &tmA, &full[s], it * kBKc, m0);
-        tma_load_2d(sB, &tmB, &full[s], it * 128, n0);
-        tma_load_2d(sB + BN * 128, &tmB, &full[s], it * 128 + 64, n0);
-        tma_load_2d(sMeta, &tmMeta, &full[s], it * 16, m0);
-      } else {
-        // adapter block c of part `part` (0 = hi, 1 = lo): rank columns
-        // 64c .. 64c+63 of A2, and the same columns of that part of B2.
-        // A2 rows/columns past r are zero-filled, so whatever B2 holds past
-        // the part's r columns adds nothing.
-        const int a = it - p.num_kb;
-        const int part = a / p.num_ab, c = a % p.num_ab;
-        mbar_arrive_expect_tx(&full[s], kA_BYTES + BN * 128);
-        if (A2_MN) {  // R: r x M, two 64-wide M atoms of 64 rank rows
-          tma_load_2d(sA, &tmA2, &full[s], m0, c * 64);
-          tma_load_2d(sA + 8192, &tmA2, &full[s], m0 + 64, c * 64);
-        } else {      // L: M x r, 128 rows of 64 rank columns
-          tma_load_2d(sA, &tmA2, &full[s], c * 64, m0);
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------- TMA producer -------
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      tma_prefetch_desc(&tmMeta);
+      int it = 0;
+      bool stop = false;
+      for (int tile = blockIdx.x; tile < p.num_tiles && !stop; tile += gridDim.x) {
+        const int m0 = (tile % p.tiles_m) * kBM;
+        const int n0 = (tile / p.tiles_m) * BN;
+        for (int kb = 0; kb < per_tile; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.status)) { stop = true; break; }
+          uint8_t* sA = smem + s * C::STAGE;
+          uint8_t* sB = sA + kA_BYTES;
+          uint8_t* sMeta = sB + C::B_BYTES;
+          if (kb < p.num_kb) {
+            mbar_arrive_expect_tx(&full[s], kA_BYTES + C::B_BYTES + kMETA_BYTES);
+            tma_load_2d(sA, &tmA, &full[s], kb * kBKc, m0);
+            tma_load_2d(sB, &tmB, &full[s], kb * 128, n0);
+            tma_load_2d(sB + BN * 128, &tmB, &full[s], kb * 128 + 64, n0);
+            tma_load_2d(sMeta, &tmMeta, &full[s], kb * 16, m0);
+          } else {
+            // adapter block c of part `part` (0 = hi, 1 = lo): rank columns
+            // 64c .. 64c+63 of A2, and the same columns of that part of B2.
+            // A2 rows/columns past r are zero-filled, so whatever B2 holds
+            // past the part's r columns adds nothing.
+            const int a = kb - p.num_kb;
+            const int part = a / p.num_ab, c = a % p.num_ab;
+            mbar_arrive_expect_tx(&full[s], kA_BYTES + BN * 128);
+            if (A2_MN) {  // R: r x M, two 64-wide M atoms of 64 rank rows
+              tma_load_2d(sA, &tmA2, &full[s], m0, c * 64);
+              tma_load_2d(sA + 8192, &tmA2, &full[s], m0 + 64, c * 64);
+            } else {      // L: M x r, 128 rows of 64 rank columns
+              tma_load_2d(sA, &tmA2, &full[s], c * 64, m0);
+            }
+            tma_load_2d(sB, &tmB2, &full[s], part * p.r + c * 64, n0);
+          }
         }
-        tma_load_2d(sB, &tmB2, &full[s], part * p.r + c * 64, n0);
       }
-      ++issued;
+      // Leave no copy in flight: wait (bounded) for the last fill of each stage.
+      for (int i = it - 1; i >= 0 && i >= it - C::STAGES; --i) {
+        volatile int no_abort = 0;
+        mbar_wait(&full[i % C::STAGES], (i / C::STAGES) & 1, &no_abort, p.status);
+      }
     }
-    // Leave no copy in flight: wait (bounded) for the last fill of each stage.
-    for (int it = issued - 1; it >= 0 && it >= issued - C::STAGES; --it) {
-      volatile int no_abort = 0;
-      mbar_wait(&full[it % C::STAGES], (it / C::STAGES) & 1, &no_abort, p.status);
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------ MMA issuer ---------
-    const uint32_t id_sp = idesc_bf16(kBM, BN, false, false, true);
-    const uint32_t id_ad = idesc_bf16(kBM, BN, A2_MN, false, false);
-    const int r16 = (p.r + 15) / 16;  // dense K=16 steps of the adapter
-    for (int it = 0; it < total; ++it) {
-      const int s = it % C::STAGES;
-      const uint32_t ph = (it / C::STAGES) & 1;
-      if (!mbar_wait(&full[s], ph, abort_flag, p.status)) break;
-      if (it < p.num_kb && !mbar_wait(&meta_full[s], ph, abort_flag, p.status)) break;
-      tc_fence_after();
-      const uint32_t aA = smem_u32(smem + s * C::STAGE);
-      const uint32_t aB = aA + kA_BYTES;
-      if (it < p.num_kb) {
-        const uint32_t tmeta = tmem + C::META_COL + 16 * s;
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------- MMA issuer ---------
+      const uint32_t id_sp = idesc_bf16(kBM, BN, false, false, true);
+      const uint32_t id_ad = idesc_bf16(kBM, BN, A2_MN, false, false);
+      const int r16 = (p.r + 15) / 16;  // dense K=16 steps of the adapter
+      int it = 0, local = 0;
+      bool stop = false;
+      for (int tile = blockIdx.x; tile < p.num_tiles && !stop; tile += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * C::ACC_COLS;
+        for (int kb = 0; kb < per_tile; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1;
+          // meta_full[s] completes once per fill of stage s (metadata or not),
+          // so its phase parity always matches full[s]'s.
+          if (!mbar_wait(&full[s], ph, abort_flag, p.status)) { stop = true; break; }
+          if (!mbar_wait(&meta_full[s], ph, abort_flag, p.status)) { stop = true; break; }
+          tc_fence_after();
+          const uint32_t aA = smem_u32(smem + s * C::STAGE);
+          const uint32_t aB = aA + kA_BYTES;
+          if (kb < p.num_kb) {
+            const uint32_t tmeta = tmem + C::META_COL + 16 * s;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {  // 4 x (K = 32 logical)
-          const uint64_t da = smem_desc(aA + j * 32, 0, 1024, kSwizzle128);
-          const uint64_t db = smem_desc(aB + (j >> 1) * (BN * 128) + (j & 1) * 64, 0, 1024,
-                                        kSwizzle128);
-          mma_sp_bf16_ss(tmem, da, db, tmeta + 4 * j, id_sp, (it > 0 || j > 0) ? 1u : 0u);
+            for (int j = 0; j < 4; ++j) {  // 4 x (K = 32 logical)
+              const uint64_t da = smem_desc(aA + j * 32, 0, 1024, kSwizzle128);
+              const uint64_t db = smem_desc(aB + (j >> 1) * (BN * 128) + (j & 1) * 64, 0, 1024,
+                                            kSwizzle128);
+              mma_sp_bf16_ss(d, da, db, tmeta + 4 * j, id_sp, (kb > 0 || j > 0) ? 1u : 0u);
+            }
+          } else {
+            const int c = (kb - p.num_kb) % p.num_ab;
+            const int steps = min(4, r16 - 4 * c);
+            for (int j = 0; j < steps; ++j) {
+              const uint64_t da = A2_MN ? smem_desc(aA + j * 2048, 8192, 1024, kSwizzle128)
+                                        : smem_desc(aA + j * 32, 0, 1024, kSwizzle128);
+              const uint64_t db = smem_desc(aB + j * 32, 0, 1024, kSwizzle128);
+              mma_bf16_ss(d, da, db, id_ad, 1u);
+            }
+          }
+          mma_commit(&empty[s]);
         }
-      } else {
-        const int c = (it - p.num_kb) % p.num_ab;
-        const int steps = min(4, r16 - 4 * c);
-        for (int j = 0; j < steps; ++j) {
-          const uint64_t da = A2_MN ? smem_desc(aA + j * 2048, 8192, 1024, kSwizzle128)
-                                    : smem_desc(aA + j * 32, 0, 1024, kSwizzle128);
-          const uint64_t db = smem_desc(aB + j * 32, 0, 1024, kSwizzle128);
-          mma_bf16_ss(tmem, da, db, id_ad, 1u);
-        }
+        if (!stop) mma_commit(&acc_full[buf]);
       }
-      mma_commit(&empty[s]);
+      mma_commit(mma_done);
     }
-    mma_commit(acc_full);
-  } else if (warp >= 2) {
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
-    const int m = m0 + 32 * q + lane;
-    // ------------------------------------------------ metadata -> TMEM ---
-    // Row m's 16 metadata bytes of stage s (4 k-steps) go to the 4 aligned
-    // columns of that stage.  The stage's previous metadata is no longer in
-    // use once its TMA fill has landed again (the refill waited for the
-    // MMAs of the previous use).
-    const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
-    bool ok = true;
-    for (int it = 0; it < p.num_kb; ++it) {
-      const int s = it % C::STAGES;
-      const uint32_t ph = (it / C::STAGES) & 1;
-      if (!mbar_wait(&full[s], ph, abort_flag, p.status)) { ok = false; break; }
-      const uint4 w = *reinterpret_cast<const uint4*>(smem + s * C::STAGE + kA_BYTES + C::B_BYTES +
-                                                      16 * (32 * q + lane));
-      const uint32_t col = tq + C::META_COL + 16 * s;
-      tmem_st_32x32b_x1(col + 0, w.x);
-      tmem_st_32x32b_x1(col + 4, w.y);
-      tmem_st_32x32b_x1(col + 8, w.z);
-      tmem_st_32x32b_x1(col + 12, w.w);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&meta_full[s]);
-    }
+  } else if (warp < 6) {
     // ------------------------------------------------ epilogue -----------
-    if (ok && mbar_wait(acc_full, 0, abort_flag, p.status)) {
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    int local = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+      const int buf = local & 1;
+      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      const int m = (tile % p.tiles_m) * kBM + 32 * q + lane;
+      const int n0 = (tile / p.tiles_m) * BN;
+      if (!mbar_wait(&acc_full[buf], use & 1, abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q) << 16);
+      const uint32_t trow = tmem + buf * C::ACC_COLS + (static_cast<uint32_t>(32 * q) << 16);
       constexpr int CH = BN < 32 ? BN : 32;
+#pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += CH) {
         uint32_t v[32];
         if constexpr (CH == 32) {
@@ -228,20 +254,55 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tmem_ld_wait();
-        if (m < p.M) {
-#pragma unroll
-          for (int j = 0; j < CH; ++j) {
-            const int n = n0 + c0 + j;
-            if (n < p.N) {
-              const float f = __uint_as_float(v[j]);
-              const size_t off = static_cast<size_t>(n) * p.M + m;
-              if (p.out_bf16)
-                static_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(f);
-              else
-                static_cast<float*>(p.out)[off] = f;
-            }
-          }
+        if (c0 + CH >= BN) {  // last chunk read: hand the buffer back early
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
         }
+        const int nlim = p.N - (n0 + c0);
+        if (p.out_bf16) {
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(n0 + c0) * p.M + m;
+#pragma unroll
+          for (int j = 0; j < CH; ++j)
+            if (j < nlim) o[static_cast<size_t>(j) * p.M] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        } else {
+          float* o = static_cast<float*>(p.out) + static_cast<size_t>(n0 + c0) * p.M + m;
+#pragma unroll
+          for (int j = 0; j < CH; ++j)
+            if (j < nlim) o[static_cast<size_t>(j) * p.M] = __uint_as_float(v[j]);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------ metadata -> TMEM ---
+    // Row m's 16 metadata bytes of stage s (4 k-steps) go to the 4 aligned
+    // columns of that stage.  The stage's previous metadata is no longer in
+    // use once its TMA fill has landed again (the refill waited for the
+    // MMAs of the previous use).  Every fill of a stage is acknowledged on
+    // meta_full, adapter fills (no metadata) included, so both barriers of a
+    // stage move through the same phases.
+    const int q = warp & 3;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::META_COL;
+    int it = 0;
+    bool stop = false;
+    for (int tile = blockIdx.x; tile < p.num_tiles && !stop; tile += gridDim.x) {
+      for (int kb = 0; kb < per_tile; ++kb, ++it) {
+        const int s = it % C::STAGES;
+        const uint32_t ph = (it / C::STAGES) & 1;
+        if (!mbar_wait(&full[s], ph, abort_flag, p.status)) { stop = true; break; }
+        if (kb < p.num_kb) {  // adapter stages carry no metadata
+          const uint4 w = *reinterpret_cast<const uint4*>(smem + s * C::STAGE + kA_BYTES +
+                                                          C::B_BYTES + 16 * (32 * q + lane));
+          const uint32_t col = tq + 16 * s;
+          tmem_st_32x32b_x1(col + 0, pair_rows(w.x, lane));
+          tmem_st_32x32b_x1(col + 4, pair_rows(w.y, lane));
+          tmem_st_32x32b_x1(col + 8, pair_rows(w.z, lane));
+          tmem_st_32x32b_x1(col + 12, pair_rows(w.w, lane));
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&meta_full[s]);
       }
     }
   }
@@ -250,9 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    // the accumulator must be idle before its columns are released
+    // every MMA this CTA issued must be complete before its columns are released
     volatile int no_abort = 0;
-    mbar_wait(acc_full, 0, &no_abort, p.status);
+    mbar_wait(mma_done, 0, &no_abort, p.status);
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
@@ -292,31 +353,37 @@ cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
   SpParams p;
   p.M = static_cast<int>(M); p.N = static_cast<int>(N); p.K = static_cast<int>(K);
   p.r = static_cast<int>(r);
+  p.tiles_m = static_cast<int>(M / kBM);
+  p.num_tiles = p.tiles_m * static_cast<int>((N + BN - 1) / BN);
   p.num_kb = static_cast<int>(K / 128);
   p.num_ab = static_cast<int>((r + 63) / 64);
   p.out_bf16 = a.out_bf16 ? 1 : 0;
   p.out = a.out;
   p.status = device_status_ptr();
   if (!p.status) return cudaErrorInvalidDevicePointer;
-  dim3 grid(static_cast<unsigned>(M / kBM), static_cast<unsigned>((N + BN - 1) / BN));
+  const int grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
   kernel<<<grid, kThreads, C::SMEM, stream>>>(tA, tB, tMeta, tA2, tB2, p);
   return cudaGetLastError();
+}
+
+// N tile by token count: the smallest tile that covers small batches; for
+// large ones 192 (the widest that still double-buffers in TMEM beside the
+// metadata) unless 128 gives the grid noticeably more tiles per SM.
+template <bool A2_MN>
+cudaError_t dispatch(const SparseGemmArgs& a, cudaStream_t stream) {
+  if (a.N <= 16) return run<16, A2_MN>(a, stream);
+  if (a.N <= 64) return run<64, A2_MN>(a, stream);
+  if (a.N <= 128) return run<128, A2_MN>(a, stream);
+  const int64_t tiles_m = a.M / kBM;
+  const int64_t t192 = tiles_m * ((a.N + 191) / 192);
+  if (t192 < 2 * sm_count()) return run<128, A2_MN>(a, stream);
+  return run<192, A2_MN>(a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_sparse_gemm(const SparseGemmArgs& a, cudaStream_t stream) {
-  // N tile: the smallest of 16 / 64 / 128 / 256 that covers the tokens.
-  if (a.a2_mn_major) {
-    if (a.N <= 16) return run<16, true>(a, stream);
-    if (a.N <= 64) return run<64, true>(a, stream);
-    if (a.N <= 128) return run<128, true>(a, stream);
-    return run<256, true>(a, stream);
-  }
-  if (a.N <= 16) return run<16, false>(a, stream);
-  if (a.N <= 64) return run<64, false>(a, stream);
-  if (a.N <= 128) return run<128, false>(a, stream);
-  return run<256, false>(a, stream);
+  return a.a2_mn_major ? dispatch<true>(a, stream) : dispatch<false>(a, stream);
 }
 
 }  // namespace slope
