@@ -137,9 +137,11 @@ class BlockStep:
                 Wm=torch.empty(out, inp // 8, dtype=torch.uint8, device=device),
                 Dv=torch.empty(inp, out // 2, dtype=torch.bfloat16, device=device),
                 Dm=torch.empty(inp, out // 8, dtype=torch.uint8, device=device),
-                Y=torch.empty(T, out, dtype=torch.float32, device=device),
+                # activations and their gradients in bf16, the mixed-precision
+                # convention; weight and adapter gradients in fp32
+                Y=torch.empty(T, out, dtype=torch.bfloat16, device=device),
                 XL=torch.empty(T, 2 * r, dtype=torch.bfloat16, device=device) if r else None,
-                dX=torch.empty(T, inp, dtype=torch.float32, device=device),
+                dX=torch.empty(T, inp, dtype=torch.bfloat16, device=device),
                 G=torch.empty(T, 2 * r, dtype=torch.bfloat16, device=device) if r else None,
                 dW=torch.empty(out, inp // 2, dtype=torch.float32, device=device),
                 dL=torch.empty(inp, r, dtype=torch.float32, device=device) if r else None,
@@ -332,6 +334,7 @@ def gpu_arm(args):
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": wl.name, "tokens_per_gpu": wl.tokens, "rank": wl.rank,
+                       "outputs": "Y, dX bf16; dW (compressed), dL, dR fp32",
                        "linears": [f"{x.name}:{x.inp}->{x.out}" for x in wl.linears],
                        "l2": f"{n_sets} rotating input sets of {set_bytes(sets[0]) / 2**20:.0f} MiB (> L2 {L2_BYTES // 2**20} MiB)",
                        "graph": bool(args.graph), "parallelism": f"replicas x{world}"},

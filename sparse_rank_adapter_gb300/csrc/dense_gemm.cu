@@ -17,6 +17,10 @@
 //   accumulator, optional split-K with atomic fp32 accumulation.
 //
 // Persistent kernel, one CTA per SM, tiles (m, n, split) taken round-robin.
+// With PAIR (the dW product), CTAs run in clusters of two on M-adjacent
+// tiles with the same N tile and K range; each loads half of the shared B
+// tile and multicasts it to both, and a stage is refilled only after both
+// CTAs' MMAs released it.
 // Roles (192 threads): warp 0 TMA, warp 1 TMEM owner + MMA issuer, warps
 // 2..5 epilogue.  The accumulator is double-buffered in TMEM so a tile's
 // epilogue overlaps the next tile's K-loop.  Every mbarrier wait is bounded.
@@ -170,7 +174,7 @@ __device__ __forceinline__ void epilogue_chunk(const DnParams& p, const uint32_t
   }
 }
 
-template <bool A_MN, bool B_MN, int BN, DenseEpi EPI>
+template <bool A_MN, bool B_MN, int BN, DenseEpi EPI, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     dense_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const DnParams p) {
@@ -188,11 +192,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = warp_id(), lane = lane_id();
   const int tiles_mn = p.tiles_m * p.tiles_n;
+  // Work units: tiles, or (with PAIR) pairs of M-adjacent tiles per cluster.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int pairs_m = p.tiles_m / 2;
+  const int units = PAIR ? p.num_tiles / 2 : p.num_tiles;
+  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int ustep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  // unit -> (tile m0, n0, split z)
+  auto decode = [&](int u, int& m0, int& n0, int& z) {
+    if (PAIR) {
+      const int per = pairs_m * p.tiles_n;
+      const int mn = u % per;
+      z = u / per;
+      m0 = (2 * (mn % pairs_m) + static_cast<int>(rank)) * kBM;
+      n0 = (mn / pairs_m) * BN;
+    } else {
+      const int mn = u % tiles_mn;
+      z = u / tiles_mn;
+      m0 = (mn % p.tiles_m) * kBM;
+      n0 = (mn / p.tiles_m) * BN;
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], PAIR ? 2 : 1);  // both CTAs' MMAs release a stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -207,7 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync();  // the peer's barriers exist before any multicast reaches them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
@@ -218,9 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmB);
       int it = 0;
       bool stop = false;
-      for (int tile = blockIdx.x; tile < p.num_tiles && !stop; tile += gridDim.x) {
-        const int mn = tile % tiles_mn, z = tile / tiles_mn;
-        const int m0 = (mn % p.tiles_m) * kBM, n0 = (mn / p.tiles_m) * BN;
+      for (int u = unit0; u < units && !stop; u += ustep) {
+        int m0, n0, z;
+        decode(u, m0, n0, z);
         const int kb0 = z * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % C::STAGES;
@@ -236,7 +264,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             tma_load_2d(sA, &tmA, &full[s], k0, m0);
           }
-          if (B_MN) {
+          if (PAIR) {  // this CTA's half of the B atoms, to both CTAs
+            constexpr int half = BN / C::B_ATOM / 2;
+#pragma unroll
+            for (int a = static_cast<int>(rank) * half; a < (static_cast<int>(rank) + 1) * half; ++a)
+              tma_load_2d_mc(sB + a * (C::B_ATOM * kBK * 2), &tmB, &full[s], n0 + a * C::B_ATOM, k0, 3);
+          } else if (B_MN) {
 #pragma unroll
             for (int a = 0; a < BN / C::B_ATOM; ++a)
               tma_load_2d(sB + a * (C::B_ATOM * kBK * 2), &tmB, &full[s], n0 + a * C::B_ATOM, k0);
@@ -257,8 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t b_swz_bytes = C::B_ATOM * 2;  // MN-major B swizzle span
       int it = 0, local = 0;
       bool stop = false;
-      for (int tile = blockIdx.x; tile < p.num_tiles && !stop; tile += gridDim.x, ++local) {
-        const int z = tile / tiles_mn;
+      for (int u = unit0; u < units && !stop; u += ustep, ++local) {
+        int m0, n0, z;
+        decode(u, m0, n0, z);
         const int kb0 = z * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         const int buf = local & 1;
         const uint32_t use = static_cast<uint32_t>(local >> 1);
@@ -282,7 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : smem_desc(aB + j * 32, 0, 1024, kSwizzle128);
             mma_bf16_ss(d, da, db, idesc, (kb > kb0 || j > 0) ? 1u : 0u);
           }
-          mma_commit(&empty[s]);
+          if (PAIR)
+            mma_commit_mc(&empty[s], 3);  // release the stage in both CTAs
+          else
+            mma_commit(&empty[s]);
         }
         if (!stop) mma_commit(&acc_full[buf]);
       }
@@ -292,10 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ epilogue -----------
     const int q = warp & 3;
     int local = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
-      const int mn = tile % tiles_mn;
-      const int m = (mn % p.tiles_m) * kBM + 32 * q + lane;
-      const int n0 = (mn / p.tiles_m) * BN;
+    for (int u = unit0; u < units; u += ustep, ++local) {
+      int m0, n0, z;
+      decode(u, m0, n0, z);
+      const int m = m0 + 32 * q + lane;
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       if (!mbar_wait(&acc_full[buf], use & 1, abort_flag, p.status)) break;
@@ -343,18 +380,285 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(mma_done, 0, &no_abort, p.status);
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+  // No CTA leaves while its peer may still multicast into it or arrive on
+  // its barriers.
+  if (PAIR) cluster_sync();
 }
 
-template <bool A_MN, bool B_MN, int BN, DenseEpi EPI>
-cudaError_t run(const DenseGemmArgs& a, cudaStream_t stream) {
-  using C = DnCfg<BN>;
-  auto kernel = dense_gemm_kernel<A_MN, B_MN, BN, EPI>;
+// ---------------------------------------------------------------------------
+// dW on CTA pairs: the pair-wide MMA (M = 256 = two 128-row weight tiles, one
+// per CTA, N = 256 input columns, half of them in each CTA's shared memory)
+// halves the bytes each SM takes in per flop.  The even CTA issues the MMAs
+// and owns the full barriers, which both CTAs' TMA loads signal; its MMA
+// commits release the stages and the accumulators in both CTAs; both CTAs'
+// epilogue warps hand accumulator buffers back to the even CTA.
+// ---------------------------------------------------------------------------
+
+constexpr int kPairBN = 256;          // N of the pair tile
+constexpr int kPairHalfB = kPairBN / 2;  // B columns each CTA holds
+constexpr int kPairStage = kA_BYTES + kPairHalfB * kBK * 2;  // 32 KB
+constexpr int kPairStages = 6;
+constexpr int kPairSmem = kPairStages * kPairStage + 1024 + 1024;
+constexpr int kPairTmemCols = 2 * kPairBN;  // double-buffered 256-column accumulator
+
+__global__ void __launch_bounds__(kThreads, 1)
+    dw_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const DnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kPairStages * kPairStage);
+  uint64_t* empty = full + kPairStages;
+  uint64_t* acc_full = empty + kPairStages;  // [2]
+  uint64_t* acc_empty = acc_full + 2;        // [2], counted in the even CTA
+  uint64_t* mma_done = acc_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  const uint32_t rank = cluster_ctarank();
+  const int pairs_m = p.tiles_m / 2;
+  const int per_split = pairs_m * p.tiles_n;
+  const int units = per_split * (p.num_tiles / (p.tiles_m * p.tiles_n));
+  const int unit0 = static_cast<int>(blockIdx.x >> 1);
+  const int ustep = static_cast<int>(gridDim.x >> 1);
+  auto decode = [&](int u, int& m0, int& n0, int& z) {
+    const int mn = u % per_split;
+    z = u / per_split;
+    m0 = (2 * (mn % pairs_m) + static_cast<int>(rank)) * kBM;  // this CTA's 128 rows
+    n0 = (mn / pairs_m) * kPairBN;                             // the pair's 256 columns
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 8);  // four epilogue warps in each CTA
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_holder, kPairTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------- TMA producer -------
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int it = 0;
+      bool stop = false;
+      for (int u = unit0; u < units && !stop; u += ustep) {
+        int m0, n0, z;
+        decode(u, m0, n0, z);
+        const int nb = n0 + static_cast<int>(rank) * kPairHalfB;  // this CTA's half of B
+        const int kb0 = z * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % kPairStages;
+          const uint32_t ph = (it / kPairStages) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.status)) { stop = true; break; }
+          uint8_t* sA = smem + s * kPairStage;
+          uint8_t* sB = sA + kA_BYTES;
+          const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);  // the even CTA's barrier
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * kPairStage);
+          const int k0 = kb * kBK;
+          tma_load_2d_pair(sA, &tmA, bar, m0, k0);
+          tma_load_2d_pair(sA + 8192, &tmA, bar, m0 + 64, k0);
+          tma_load_2d_pair(sB, &tmB, bar, nb, k0);
+          tma_load_2d_pair(sB + 8192, &tmB, bar, nb + 64, k0);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------------------------------------- MMA issuer ---------
+      const uint32_t idesc = idesc_bf16(2 * kBM, kPairBN, true, true, false);
+      int it = 0, local = 0;
+      bool stop = false;
+      for (int u = unit0; u < units && !stop; u += ustep, ++local) {
+        int m0, n0, z;
+        decode(u, m0, n0, z);
+        const int kb0 = z * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+        const int buf = local & 1;
+        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * kPairBN;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % kPairStages;
+          const uint32_t ph = (it / kPairStages) & 1;
+          if (!mbar_wait(&full[s], ph, abort_flag, p.status)) { stop = true; break; }
+          tc_fence_after();
+          const uint32_t aA = smem_u32(smem + s * kPairStage);
+          const uint32_t aB = aA + kA_BYTES;
+#pragma unroll
+          for (int j = 0; j < kBK / 16; ++j) {
+            const uint64_t da = smem_desc(aA + j * 2048, 8192, 1024, kSwizzle128);
+            const uint64_t db = smem_desc(aB + j * 2048, 8192, 1024, kSwizzle128);
+            mma_bf16_ss_pair(d, da, db, idesc, (kb > kb0 || j > 0) ? 1u : 0u);
+          }
+          mma_commit_pair_mc(&empty[s], 3);
+        }
+        if (!stop) mma_commit_pair_mc(&acc_full[buf], 3);
+      }
+      mma_commit_pair_mc(mma_done, 3);
+    }
+  } else {
+    // ------------------------------------------------ epilogue -----------
+    const int q = warp & 3;
+    const uint32_t acc_empty0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
+    int local = 0;
+    for (int u = unit0; u < units; u += ustep, ++local) {
+      int m0, n0, z;
+      decode(u, m0, n0, z);
+      const int m = m0 + 32 * q + lane;
+      const int buf = local & 1;
+      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      if (!mbar_wait(&acc_full[buf], use & 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t trow = tmem + buf * kPairBN + (static_cast<uint32_t>(32 * q) << 16);
+      uint4 mrow[2];
+      {
+        const uint4* mp = reinterpret_cast<const uint4*>(p.meta + static_cast<size_t>(m) * (p.N / 8) + n0 / 8);
+        mrow[0] = mp[0];
+        mrow[1] = (n0 + 128 < p.N) ? mp[1] : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int c0 = 0; c0 < kPairBN; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(trow + c0, v);
+        tmem_ld_wait();
+        if (c0 + 32 >= kPairBN) {  // last chunk read: hand the buffer back early
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8 * buf);
+        }
+        epilogue_chunk<kPairBN, 32, DenseEpi::MaskedWeightGrad>(p, v, m, n0, c0, mrow);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    volatile int no_abort = 0;
+    mbar_wait(mma_done, 0, &no_abort, p.status);
+    tmem_dealloc_pair(tmem, kPairTmemCols);
+  }
+  cluster_sync();  // no CTA leaves while its peer may still signal it
+}
+
+cudaError_t run_dw_pair(const DenseGemmArgs& a, cudaStream_t stream) {
   static std::atomic<int> attr_set[64];
+  static std::atomic<int> max_clusters[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev].load()) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kPairSmem;
+  cfg.stream = stream;
+  if (!attr_set[dev].load()) {
+    cudaError_t e = cudaFuncSetAttribute(dw_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    cfg.gridDim = dim3(2 * (sm_count() / 2));
+    e = cudaOccupancyMaxActiveClusters(&n, dw_pair_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    max_clusters[dev].store(n > 0 ? n : 1);
+    attr_set[dev].store(1);
+  }
+  const uint64_t M = a.M, N = a.N, K = a.K;
+  CUtensorMap tA, tB;  // dY (K x M) and X (K x N), both MN-major, 64 x 64 boxes
+  bool ok = make_tmap_2d(&tA, a.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, 2 * a.lda, 64, kBK, Swz::B128) &&
+            make_tmap_2d(&tB, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, 2 * a.ldb, 64, kBK, Swz::B128);
+  if (!ok) return cudaErrorInvalidValue;
+  const int num_kb = static_cast<int>((K + kBK - 1) / kBK);
+  const int tiles_m = static_cast<int>(M / kBM);  // even
+  const int tiles_n = static_cast<int>((N + kPairBN - 1) / kPairBN);
+  const int clusters_max = max_clusters[dev].load();
+  const int pair_tiles = (tiles_m / 2) * tiles_n;
+  int splits = (clusters_max + pair_tiles - 1) / pair_tiles;
+  const int max_split = num_kb / 4 > 0 ? num_kb / 4 : 1;
+  if (splits > max_split) splits = max_split;
+  if (splits < 1) splits = 1;
+  const int kbs = (num_kb + splits - 1) / splits;
+  splits = (num_kb + kbs - 1) / kbs;
+
+  DnParams p = {};
+  p.M = static_cast<int>(M); p.N = static_cast<int>(N); p.K = static_cast<int>(K);
+  p.kb_per_split = kbs; p.num_kb = num_kb;
+  p.tiles_m = tiles_m; p.tiles_n = tiles_n;
+  p.num_tiles = tiles_m * tiles_n * splits;
+  p.ldo = a.ldo; p.out = a.out; p.meta = a.meta;
+  p.dense_dw = a.dense_dw ? 1 : 0;
+  p.accumulate = a.accumulate ? 1 : 0;
+  p.atomic_out = splits > 1 ? 1 : 0;
+  if (p.atomic_out && !a.accumulate) {
+    if (cudaError_t e = cudaMemsetAsync(a.out, 0, static_cast<size_t>(M) * a.ldo * sizeof(float), stream))
+      return e;
+  }
+  p.status = device_status_ptr();
+  if (!p.status) return cudaErrorInvalidDevicePointer;
+  const int units = pair_tiles * splits;
+  const int clusters = units < clusters_max ? units : clusters_max;
+  cfg.gridDim = dim3(2 * clusters);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, dw_pair_kernel, tA, tB, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <bool A_MN, bool B_MN, int BN, DenseEpi EPI, bool PAIR = false>
+cudaError_t run(const DenseGemmArgs& a, cudaStream_t stream) {
+  using C = DnCfg<BN>;
+  static_assert(!PAIR || (B_MN && BN / C::B_ATOM >= 2), "pairs split the B atoms");
+  auto kernel = dense_gemm_kernel<A_MN, B_MN, BN, EPI, PAIR>;
+  static std::atomic<int> attr_set[64];
+  static std::atomic<int> max_clusters[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  if (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  if (!attr_set[dev].load()) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
+    if (PAIR) {
+      int n = 0;
+      cfg.gridDim = dim3(2 * (sm_count() / 2));
+      e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+      if (e != cudaSuccess) return e;
+      max_clusters[dev].store(n > 0 ? n : 1);
+    }
     attr_set[dev].store(1);
   }
   const uint64_t M = a.M, N = a.N, K = a.K;
@@ -407,8 +711,17 @@ cudaError_t run(const DenseGemmArgs& a, cudaStream_t stream) {
   if (!p.status) return cudaErrorInvalidDevicePointer;
   p.tiles_m = tiles_m; p.tiles_n = tiles_n;
   p.num_tiles = tiles_m * tiles_n * splits;
-  const int grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
-  kernel<<<grid, kThreads, C::SMEM, stream>>>(tA, tB, p);
+  int grid;
+  if (PAIR) {
+    const int units = p.num_tiles / 2;
+    const int clusters = units < max_clusters[dev].load() ? units : max_clusters[dev].load();
+    grid = 2 * clusters;
+  } else {
+    grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
+  }
+  cfg.gridDim = dim3(grid);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tA, tB, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -427,7 +740,10 @@ cudaError_t run_rank(const DenseGemmArgs& a, cudaStream_t stream) {
 cudaError_t launch_dense_gemm(const DenseGemmArgs& a, cudaStream_t stream) {
   switch (a.epi) {
     case DenseEpi::MaskedWeightGrad:  // dW: A = dY (T x out), B = X (T x in), both MN-major
-      if (a.a_mn_major && a.b_mn_major) return run<true, true, 256, DenseEpi::MaskedWeightGrad>(a, stream);
+      if (a.a_mn_major && a.b_mn_major) {
+        if ((a.M / kBM) % 2 == 0) return run_dw_pair(a, stream);  // CTA pairs on M-adjacent tiles
+        return run<true, true, 256, DenseEpi::MaskedWeightGrad, false>(a, stream);
+      }
       break;
     case DenseEpi::StoreBf16HiLo:  // XL = X·L (B MN-major) or G = dY·Rᵀ (B K-major)
       if (!a.a_mn_major && a.b_mn_major) return run_rank<false, true, DenseEpi::StoreBf16HiLo>(a, stream);

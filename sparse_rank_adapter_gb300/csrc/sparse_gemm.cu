@@ -16,7 +16,11 @@
 // the epilogue writes directly (lane = m, so a warp's stores of one column
 // n are 128 contiguous bytes).
 //
-// Persistent kernel, one CTA per SM, tiles taken round-robin.  Roles (320
+// Persistent kernel, one CTA per SM, tiles taken round-robin.  With PAIR,
+// CTAs run in clusters of two on adjacent M tiles with the same N tile: each
+// loads half of the shared B tile (the tokens) and multicasts it to both, so
+// an SM pulls 2/3 of the bytes per K-block it would alone; a stage is
+// refilled only after both CTAs' MMAs released it.  Roles (320
 // threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues the MMAs
 // (one thread), warps 2..5 drain the accumulator, warps 6..9 move each
 // stage's 2:4 metadata from shared memory into TMEM.  The accumulator is
@@ -84,7 +88,7 @@ struct SpParams {
   unsigned int* status;
 };
 
-template <int BN, bool A2_MN>
+template <int BN, bool A2_MN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
@@ -106,11 +110,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = warp_id(), lane = lane_id();
   const int per_tile = p.num_kb + 2 * p.num_ab;
+  // Work units: tiles, or (with PAIR) pairs of M-adjacent tiles per cluster.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int units = PAIR ? p.num_tiles / 2 : p.num_tiles;
+  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int ustep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int pairs_m = p.tiles_m / 2;
+  auto tile_m0 = [&](int u) {
+    return PAIR ? (2 * (u % pairs_m) + static_cast<int>(rank)) * kBM : (u % p.tiles_m) * kBM;
+  };
+  auto tile_n0 = [&](int u) { return PAIR ? (u / pairs_m) * BN : (u / p.tiles_m) * BN; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], PAIR ? 2 : 1);  // both CTAs' MMAs release a stage
       mbar_init(&meta_full[s], 4);  // one arrival per metadata warp
     }
     for (int b = 0; b < 2; ++b) {
@@ -126,7 +140,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync();  // the peer's barriers exist before any multicast reaches them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
@@ -138,9 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmMeta);
       int it = 0;
       bool stop = false;
-      for (int tile = blockIdx.x; tile < p.num_tiles && !stop; tile += gridDim.x) {
-        const int m0 = (tile % p.tiles_m) * kBM;
-        const int n0 = (tile / p.tiles_m) * BN;
+      for (int u = unit0; u < units && !stop; u += ustep) {
+        const int m0 = tile_m0(u);
+        const int n0 = tile_n0(u);
         for (int kb = 0; kb < per_tile; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
@@ -151,8 +168,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kb < p.num_kb) {
             mbar_arrive_expect_tx(&full[s], kA_BYTES + C::B_BYTES + kMETA_BYTES);
             tma_load_2d(sA, &tmA, &full[s], kb * kBKc, m0);
-            tma_load_2d(sB, &tmB, &full[s], kb * 128, n0);
-            tma_load_2d(sB + BN * 128, &tmB, &full[s], kb * 128 + 64, n0);
+            if (PAIR) {  // this CTA's half of the B rows, to both CTAs
+              const int h = static_cast<int>(rank) * (BN / 2);
+              tma_load_2d_mc(sB + h * 128, &tmB, &full[s], kb * 128, n0 + h, 3);
+              tma_load_2d_mc(sB + BN * 128 + h * 128, &tmB, &full[s], kb * 128 + 64, n0 + h, 3);
+            } else {
+              tma_load_2d(sB, &tmB, &full[s], kb * 128, n0);
+              tma_load_2d(sB + BN * 128, &tmB, &full[s], kb * 128 + 64, n0);
+            }
             tma_load_2d(sMeta, &tmMeta, &full[s], kb * 16, m0);
           } else {
             // adapter block c of part `part` (0 = hi, 1 = lo): rank columns
@@ -168,7 +191,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {      // L: M x r, 128 rows of 64 rank columns
               tma_load_2d(sA, &tmA2, &full[s], c * 64, m0);
             }
-            tma_load_2d(sB, &tmB2, &full[s], part * p.r + c * 64, n0);
+            if (PAIR) {
+              const int h = static_cast<int>(rank) * (BN / 2);
+              tma_load_2d_mc(sB + h * 128, &tmB2, &full[s], part * p.r + c * 64, n0 + h, 3);
+            } else {
+              tma_load_2d(sB, &tmB2, &full[s], part * p.r + c * 64, n0);
+            }
           }
         }
       }
@@ -186,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r16 = (p.r + 15) / 16;  // dense K=16 steps of the adapter
       int it = 0, local = 0;
       bool stop = false;
-      for (int tile = blockIdx.x; tile < p.num_tiles && !stop; tile += gridDim.x, ++local) {
+      for (int u = unit0; u < units && !stop; u += ustep, ++local) {
         const int buf = local & 1;
         const uint32_t use = static_cast<uint32_t>(local >> 1);
         if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort_flag, p.status)) break;
@@ -221,7 +249,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_bf16_ss(d, da, db, id_ad, 1u);
             }
           }
-          mma_commit(&empty[s]);
+          if (PAIR)
+            mma_commit_mc(&empty[s], 3);  // release the stage in both CTAs
+          else
+            mma_commit(&empty[s]);
         }
         if (!stop) mma_commit(&acc_full[buf]);
       }
@@ -231,11 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ epilogue -----------
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     int local = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+    for (int u = unit0; u < units; u += ustep, ++local) {
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
-      const int m = (tile % p.tiles_m) * kBM + 32 * q + lane;
-      const int n0 = (tile / p.tiles_m) * BN;
+      const int m = tile_m0(u) + 32 * q + lane;
+      const int n0 = tile_n0(u);
       if (!mbar_wait(&acc_full[buf], use & 1, abort_flag, p.status)) break;
       tc_fence_after();
       const uint32_t trow = tmem + buf * C::ACC_COLS + (static_cast<uint32_t>(32 * q) << 16);
@@ -285,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::META_COL;
     int it = 0;
     bool stop = false;
-    for (int tile = blockIdx.x; tile < p.num_tiles && !stop; tile += gridDim.x) {
+    for (int u = unit0; u < units && !stop; u += ustep) {
       for (int kb = 0; kb < per_tile; ++kb, ++it) {
         const int s = it % C::STAGES;
         const uint32_t ph = (it / C::STAGES) & 1;
@@ -316,25 +347,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(mma_done, 0, &no_abort, p.status);
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+  // No CTA leaves while its peer may still multicast into it or arrive on
+  // its barriers.
+  if (PAIR) cluster_sync();
 }
 
-template <int BN, bool A2_MN>
+template <int BN, bool A2_MN, bool PAIR>
 cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
   using C = SpCfg<BN>;
-  auto kernel = sparse_gemm_kernel<BN, A2_MN>;
+  auto kernel = sparse_gemm_kernel<BN, A2_MN, PAIR>;
   static std::atomic<int> attr_set[64];
+  static std::atomic<int> max_clusters[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev].load()) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  if (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  if (!attr_set[dev].load()) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
+    if (PAIR) {
+      int n = 0;
+      cfg.gridDim = dim3(2 * (sm_count() / 2));
+      e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+      if (e != cudaSuccess) return e;
+      max_clusters[dev].store(n > 0 ? n : 1);
+    }
     attr_set[dev].store(1);
   }
   CUtensorMap tA, tB, tMeta, tA2, tB2;
   const uint64_t M = a.M, N = a.N, K = a.K, r = a.r;
+  const uint32_t b_rows = PAIR ? BN / 2 : BN;  // rows of B one TMA box brings
   bool ok = make_tmap_2d(&tA, a.a_vals, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K / 2, M, K, 64, kBM,
                          Swz::B128) &&
-            make_tmap_2d(&tB, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, 2 * K, 64, BN,
+            make_tmap_2d(&tB, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, 2 * K, 64, b_rows,
                          Swz::B128) &&
             make_tmap_2d(&tMeta, a.a_meta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 8, M, K / 8, 16,
                          kBM, Swz::None);
@@ -344,7 +401,7 @@ cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
                       : make_tmap_2d(&tA2, a.a2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, r, M, 2 * r,
                                      64, kBM, Swz::B128));
     ok = ok && make_tmap_2d(&tB2, a.b2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2 * r, N, 4 * r, 64,
-                            BN, Swz::B128);
+                            b_rows, Swz::B128);
   } else {
     tA2 = tA;  // unused
     tB2 = tB;
@@ -361,8 +418,17 @@ cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
   p.out = a.out;
   p.status = device_status_ptr();
   if (!p.status) return cudaErrorInvalidDevicePointer;
-  const int grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
-  kernel<<<grid, kThreads, C::SMEM, stream>>>(tA, tB, tMeta, tA2, tB2, p);
+  int grid;
+  if (PAIR) {
+    const int units = p.num_tiles / 2;
+    const int clusters = units < max_clusters[dev].load() ? units : max_clusters[dev].load();
+    grid = 2 * clusters;
+  } else {
+    grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
+  }
+  cfg.gridDim = dim3(grid);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tA, tB, tMeta, tA2, tB2, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -371,13 +437,16 @@ cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
 // metadata) unless 128 gives the grid noticeably more tiles per SM.
 template <bool A2_MN>
 cudaError_t dispatch(const SparseGemmArgs& a, cudaStream_t stream) {
-  if (a.N <= 16) return run<16, A2_MN>(a, stream);
-  if (a.N <= 64) return run<64, A2_MN>(a, stream);
-  if (a.N <= 128) return run<128, A2_MN>(a, stream);
+  if (a.N <= 16) return run<16, A2_MN, false>(a, stream);
+  if (a.N <= 64) return run<64, A2_MN, false>(a, stream);
   const int64_t tiles_m = a.M / kBM;
+  const bool pair = tiles_m % 2 == 0;  // clusters pair M-adjacent tiles
+  if (a.N <= 128)
+    return pair ? run<128, A2_MN, true>(a, stream) : run<128, A2_MN, false>(a, stream);
   const int64_t t192 = tiles_m * ((a.N + 191) / 192);
-  if (t192 < 2 * sm_count()) return run<128, A2_MN>(a, stream);
-  return run<192, A2_MN>(a, stream);
+  if (t192 < 2 * sm_count())
+    return pair ? run<128, A2_MN, true>(a, stream) : run<128, A2_MN, false>(a, stream);
+  return pair ? run<192, A2_MN, true>(a, stream) : run<192, A2_MN, false>(a, stream);
 }
 
 }  // namespace
