@@ -46,6 +46,23 @@ def flops_per_step(wl) -> float:
     return f
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest of every rank's x (x itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: float, world: int, ms_step_max: float) -> float:
+    """Every rank's work over the slowest rank's step time (weak scaling)."""
+    return flops_per_rank * world / (ms_step_max * 1e-3) / 1e12
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -294,12 +311,9 @@ def gpu_arm(args):
     ms_step = t_start.elapsed_time(t_end) / args.steps
     calls_ms = {k: sum(x[2] for x in v) / n_obs for k, v in per_call.items()}
 
-    t = torch.tensor([ms_step], device=dev, dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_step = float(t.item())
+    ms_step = max_over_ranks(ms_step, dev)
     fl = flops_per_step(wl)
-    value = fl * world / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(fl, world, ms_step)
 
     # roofline of the dominant call
     T, r = wl.tokens, wl.rank
@@ -415,34 +429,34 @@ def e2e_measure(args, wl, st, stream, dev):
 
 
 def oracle_sample(wl, budget_s: float):
-    """Times the oracle (as it stands) on the block's linears for a sample of
-    token rows; returns (dense-equivalent flops done, seconds, description)."""
-    import numpy as np
-
+    """Times the oracle (as it stands) on the block: full passes over its
+    linears (prune, double prune, forward, both gradients) for up to 2048
+    tokens, repeated until `budget_s` seconds of CPU work; returns
+    (dense-equivalent flops done, seconds, description)."""
     from oracle import slope_oracle as O
 
     T = wl.tokens
-    sample_T = min(T, 1024)
+    sample_T = min(T, 2048)
+    inputs = [synth.layer_inputs(0, li, sample_T, lin.inp, lin.out, wl.rank)
+              for li, lin in enumerate(wl.linears)]
     done, t_total, lins = 0.0, 0.0, 0
-    t0 = time.perf_counter()
-    for li, lin in enumerate(wl.linears):
-        d = synth.layer_inputs(0, li, sample_T, lin.inp, lin.out, wl.rank)
-        L, R = (d["L"], d["R"]) if wl.rank else (None, None)
-        s = time.perf_counter()
-        vals, meta, _ = O.prune24(d["W"])
-        O.linear_fwd(d["X"], vals, meta, L, R)
-        if not wl.forward_only:
-            tv, tm, _ = O.double_prune24(vals, meta, lin.out, lin.inp)
-            O.linear_bwd_input(d["dY"], tv, tm, L, R)
-            O.linear_bwd_weight(d["dY"], d["X"], meta, L, R)
-        t_total += time.perf_counter() - s
-        sub = synth.Workload(wl.name, sample_T, wl.rank, (lin,), wl.forward_only)
-        done += flops_per_step(sub)
-        lins += 1
-        if time.perf_counter() - t0 > budget_s:
-            break
-    desc = (f"{lins} of {len(wl.linears)} linears of {wl.name}, {sample_T} of {T} tokens each "
-            f"(full prune and double prune of every weight), oracle fp64 NumPy")
+    while t_total < budget_s:
+        for lin, d in zip(wl.linears, inputs):
+            L, R = (d["L"], d["R"]) if wl.rank else (None, None)
+            s = time.perf_counter()
+            vals, meta, _ = O.prune24(d["W"])
+            O.linear_fwd(d["X"], vals, meta, L, R)
+            if not wl.forward_only:
+                tv, tm, _ = O.double_prune24(vals, meta, lin.out, lin.inp)
+                O.linear_bwd_input(d["dY"], tv, tm, L, R)
+                O.linear_bwd_weight(d["dY"], d["X"], meta, L, R)
+            t_total += time.perf_counter() - s
+            done += flops_per_step(synth.Workload(wl.name, sample_T, wl.rank, (lin,), wl.forward_only))
+            lins += 1
+            if t_total >= budget_s:
+                break
+    desc = (f"{lins} linear passes over {wl.name} ({len(wl.linears)} linears), {sample_T} of {T} tokens "
+            f"each, full prune and double prune of every weight; oracle fp64 NumPy")
     return done, t_total, desc
 
 

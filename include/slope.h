@@ -169,6 +169,17 @@ int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T, int64_t in
  */
 int slope_device_status(void* stream);
 
+/*
+ * Failure-detection self test (no counterpart in the method: it exercises
+ * the library's own bounded waits).  Launches one kernel whose single wait
+ * can never be satisfied, bounded by `limit_cycles` SM clocks (1 .. 2^34;
+ * about 2e6 is one millisecond).  The kernel then records a timeout in the
+ * device status word and returns, leaving the context usable; a following
+ * slope_device_status() returns SLOPE_ERR_TIMEOUT and clears the word.
+ * Returns SLOPE_ERR_INVALID_ARG for a limit outside the range.
+ */
+int slope_selftest_wait_timeout(int64_t limit_cycles, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

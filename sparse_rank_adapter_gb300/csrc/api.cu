@@ -10,6 +10,7 @@
 
 #include "../../include/slope.h"
 #include "slope_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace slope {
 
@@ -119,6 +120,21 @@ unsigned int* device_status_ptr() {
   p = static_cast<unsigned int*>(q);
   g_status_ptr[dev].store(p, std::memory_order_release);
   return p;
+}
+
+// A wait that nothing will end: one thread waits, with the given limit, on
+// a fresh mbarrier no one arrives on, through the same bounded wait every
+// pipeline kernel uses, which records the timeout in the status word.
+__global__ void wait_timeout_probe_kernel(unsigned int* status, long long limit_cycles) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, status, limit_cycles);
 }
 
 }  // namespace slope
@@ -296,6 +312,15 @@ extern "C" int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T,
   q.M = out; q.N = 2 * r; q.K = T; q.lda = out; q.ldb = 2 * r;
   q.epi = DenseEpi::AddF32Transposed; q.out = dR; q.ldo = out; q.fold = r; q.splits = 0;
   return from_cuda(launch_dense_gemm(q, st));
+}
+
+extern "C" int slope_selftest_wait_timeout(int64_t limit_cycles, void* stream) {
+  if (limit_cycles <= 0 || limit_cycles > (int64_t(1) << 34)) return SLOPE_ERR_INVALID_ARG;
+  if (int s = check_device()) return s;
+  unsigned int* status = device_status_ptr();
+  if (!status) return SLOPE_ERR_CUDA;
+  wait_timeout_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, limit_cycles);
+  return from_cuda(cudaGetLastError());
 }
 
 extern "C" int slope_device_status(void* stream) {

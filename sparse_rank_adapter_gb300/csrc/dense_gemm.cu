@@ -17,10 +17,6 @@
 //   accumulator, optional split-K with atomic fp32 accumulation.
 //
 // Persistent kernel, one CTA per SM, tiles (m, n, split) taken round-robin.
-// With PAIR (the dW product), CTAs run in clusters of two on M-adjacent
-// tiles with the same N tile and K range; each loads half of the shared B
-// tile and multicasts it to both, and a stage is refilled only after both
-// CTAs' MMAs released it.
 // Roles (192 threads): warp 0 TMA, warp 1 TMEM owner + MMA issuer, warps
 // 2..5 epilogue.  The accumulator is double-buffered in TMEM so a tile's
 // epilogue overlaps the next tile's K-loop.  Every mbarrier wait is bounded.
@@ -174,7 +170,7 @@ __device__ __forceinline__ void epilogue_chunk(const DnParams& p, const uint32_t
   }
 }
 
-template <bool A_MN, bool B_MN, int BN, DenseEpi EPI, bool PAIR>
+template <bool A_MN, bool B_MN, int BN, DenseEpi EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     dense_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const DnParams p) {
@@ -192,32 +188,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = warp_id(), lane = lane_id();
   const int tiles_mn = p.tiles_m * p.tiles_n;
-  // Work units: tiles, or (with PAIR) pairs of M-adjacent tiles per cluster.
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-  const int pairs_m = p.tiles_m / 2;
-  const int units = PAIR ? p.num_tiles / 2 : p.num_tiles;
-  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int ustep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int units = p.num_tiles;
+  const int unit0 = static_cast<int>(blockIdx.x);
+  const int ustep = static_cast<int>(gridDim.x);
   // unit -> (tile m0, n0, split z)
   auto decode = [&](int u, int& m0, int& n0, int& z) {
-    if (PAIR) {
-      const int per = pairs_m * p.tiles_n;
-      const int mn = u % per;
-      z = u / per;
-      m0 = (2 * (mn % pairs_m) + static_cast<int>(rank)) * kBM;
-      n0 = (mn / pairs_m) * BN;
-    } else {
-      const int mn = u % tiles_mn;
-      z = u / tiles_mn;
-      m0 = (mn % p.tiles_m) * kBM;
-      n0 = (mn / p.tiles_m) * BN;
-    }
+    const int mn = u % tiles_mn;
+    z = u / tiles_mn;
+    m0 = (mn % p.tiles_m) * kBM;
+    n0 = (mn / p.tiles_m) * BN;
   };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], PAIR ? 2 : 1);  // both CTAs' MMAs release a stage
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -232,10 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  if (PAIR)
-    cluster_sync();  // the peer's barriers exist before any multicast reaches them
-  else
-    __syncthreads();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
@@ -264,12 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             tma_load_2d(sA, &tmA, &full[s], k0, m0);
           }
-          if (PAIR) {  // this CTA's half of the B atoms, to both CTAs
-            constexpr int half = BN / C::B_ATOM / 2;
-#pragma unroll
-            for (int a = static_cast<int>(rank) * half; a < (static_cast<int>(rank) + 1) * half; ++a)
-              tma_load_2d_mc(sB + a * (C::B_ATOM * kBK * 2), &tmB, &full[s], n0 + a * C::B_ATOM, k0, 3);
-          } else if (B_MN) {
+          if (B_MN) {
 #pragma unroll
             for (int a = 0; a < BN / C::B_ATOM; ++a)
               tma_load_2d(sB + a * (C::B_ATOM * kBK * 2), &tmB, &full[s], n0 + a * C::B_ATOM, k0);
@@ -316,10 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : smem_desc(aB + j * 32, 0, 1024, kSwizzle128);
             mma_bf16_ss(d, da, db, idesc, (kb > kb0 || j > 0) ? 1u : 0u);
           }
-          if (PAIR)
-            mma_commit_mc(&empty[s], 3);  // release the stage in both CTAs
-          else
-            mma_commit(&empty[s]);
+          mma_commit(&empty[s]);
         }
         if (!stop) mma_commit(&acc_full[buf]);
       }
@@ -380,9 +354,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(mma_done, 0, &no_abort, p.status);
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
-  // No CTA leaves while its peer may still multicast into it or arrive on
-  // its barriers.
-  if (PAIR) cluster_sync();
 }
 
 // ---------------------------------------------------------------------------
@@ -626,39 +597,17 @@ cudaError_t run_dw_pair(const DenseGemmArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <bool A_MN, bool B_MN, int BN, DenseEpi EPI, bool PAIR = false>
+template <bool A_MN, bool B_MN, int BN, DenseEpi EPI>
 cudaError_t run(const DenseGemmArgs& a, cudaStream_t stream) {
   using C = DnCfg<BN>;
-  static_assert(!PAIR || (B_MN && BN / C::B_ATOM >= 2), "pairs split the B atoms");
-  auto kernel = dense_gemm_kernel<A_MN, B_MN, BN, EPI, PAIR>;
+  auto kernel = dense_gemm_kernel<A_MN, B_MN, BN, EPI>;
   static std::atomic<int> attr_set[64];
-  static std::atomic<int> max_clusters[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = C::SMEM;
-  cfg.stream = stream;
-  if (PAIR) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  }
   if (!attr_set[dev].load()) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    if (PAIR) {
-      int n = 0;
-      cfg.gridDim = dim3(2 * (sm_count() / 2));
-      e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
-      if (e != cudaSuccess) return e;
-      max_clusters[dev].store(n > 0 ? n : 1);
-    }
     attr_set[dev].store(1);
   }
   const uint64_t M = a.M, N = a.N, K = a.K;
@@ -711,17 +660,8 @@ cudaError_t run(const DenseGemmArgs& a, cudaStream_t stream) {
   if (!p.status) return cudaErrorInvalidDevicePointer;
   p.tiles_m = tiles_m; p.tiles_n = tiles_n;
   p.num_tiles = tiles_m * tiles_n * splits;
-  int grid;
-  if (PAIR) {
-    const int units = p.num_tiles / 2;
-    const int clusters = units < max_clusters[dev].load() ? units : max_clusters[dev].load();
-    grid = 2 * clusters;
-  } else {
-    grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
-  }
-  cfg.gridDim = dim3(grid);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tA, tB, p);
-  if (e != cudaSuccess) return e;
+  const int grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
+  kernel<<<grid, kThreads, C::SMEM, stream>>>(tA, tB, p);
   return cudaGetLastError();
 }
 
@@ -742,7 +682,7 @@ cudaError_t launch_dense_gemm(const DenseGemmArgs& a, cudaStream_t stream) {
     case DenseEpi::MaskedWeightGrad:  // dW: A = dY (T x out), B = X (T x in), both MN-major
       if (a.a_mn_major && a.b_mn_major) {
         if ((a.M / kBM) % 2 == 0) return run_dw_pair(a, stream);  // CTA pairs on M-adjacent tiles
-        return run<true, true, 256, DenseEpi::MaskedWeightGrad, false>(a, stream);
+        return run<true, true, 256, DenseEpi::MaskedWeightGrad>(a, stream);
       }
       break;
     case DenseEpi::StoreBf16HiLo:  // XL = X·L (B MN-major) or G = dY·Rᵀ (B K-major)

@@ -59,13 +59,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // false, without waiting further, when `abort` is already set or the clock
 // limit runs out (then it sets `abort` and ORs kStatusTimeout into *status).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          unsigned int* status) {
+                                          unsigned int* status,
+                                          long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       *abort = 1;
       atomicOr(status, kStatusTimeout);
       return false;
@@ -110,10 +111,11 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
-// Whole-cluster barrier (every thread of every CTA of the cluster).
+// Whole-cluster barrier (every thread of every CTA of the cluster).  The
+// non-.aligned form: a warp may reach it with some lanes still finishing a
+// role loop; each thread arrives and waits on its own.
 __device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // Shared-memory address of the same variable in CTA `rank` of the cluster.

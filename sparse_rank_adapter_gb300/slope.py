@@ -33,6 +33,7 @@ SIGNATURES = (
     ("slope_linear_bwd_input", _i, (_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _vp, _sz, _vp)),
     ("slope_linear_bwd_weight", _i, (_vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _i, _vp, _u32, _vp, _vp, _vp, _sz, _vp)),
     ("slope_device_status", _i, (_vp,)),
+    ("slope_selftest_wait_timeout", _i, (_i64, _vp)),
 )
 
 _lib = None
@@ -188,3 +189,9 @@ def slope_linear_bwd_weight(dY, X, Wm, XL, G, dW, dL=None, dR=None, flags: int =
 
 def slope_device_status(stream=None):
     _check(lib().slope_device_status(_stream(stream)), "slope_device_status")
+
+
+def slope_selftest_wait_timeout(limit_cycles: int, stream=None):
+    """Launch the bounded-wait self test (a wait nothing ends, limited to
+    `limit_cycles` SM clocks); slope_device_status() then reports the timeout."""
+    _check(lib().slope_selftest_wait_timeout(limit_cycles, _stream(stream)), "slope_selftest_wait_timeout")

@@ -110,6 +110,14 @@ def test_linear_argument_checks(L):
     assert bw(A, A, 64, 256, 256, A, A, A, 8, MIS, 0, A, A, None, 0, None) == L.ERR_ALIGNMENT
 
 
+@cpu_only
+def test_selftest_argument_checks(L):
+    f = L.lib().slope_selftest_wait_timeout
+    assert f(0, None) == L.ERR_INVALID_ARG
+    assert f(-5, None) == L.ERR_INVALID_ARG
+    assert f(1 << 40, None) == L.ERR_INVALID_ARG
+
+
 def test_workspace_size_is_a_query(L):
     assert L.slope_workspace_size(4096, 1024, 1024, 16) >= 0
 
