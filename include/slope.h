@@ -67,8 +67,10 @@ typedef enum {
 typedef enum { SLOPE_F32 = 0, SLOPE_BF16 = 1 } slope_dtype;
 
 /* flags of slope_linear_bwd_weight */
-#define SLOPE_DW_DENSE 1u   /* write dW dense (out x in, zeros where pruned) */
-#define SLOPE_ACCUMULATE 2u /* add into dW, dL, dR instead of overwriting */
+#define SLOPE_DW_DENSE 1u     /* write dW dense (out x in, zeros where pruned) */
+#define SLOPE_ACCUMULATE 2u   /* add into dW, dL, dR instead of overwriting */
+#define SLOPE_SKIP_DW 4u      /* compute dL, dR only (dW is not touched) */
+#define SLOPE_SKIP_ADAPTER 8u /* compute dW only (dL, dR are not touched) */
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* slope_status_string(int status);
@@ -153,8 +155,10 @@ int slope_linear_bwd_input(const void* dY, int64_t T, int64_t in, int64_t out, c
  * XL (T x 2r) and G (T x 2r) are the hi/lo outputs of the two calls above;
  * dL (in x r f32) and dR (r x out f32) are written when r > 0.
  * SLOPE_ACCUMULATE adds into dW, dL, dR (gradient accumulation) instead of
- * overwriting them.  T == 0 writes zeros (or leaves them, when accumulating).
- * Size rules as slope_linear_fwd.
+ * overwriting them.  SLOPE_SKIP_DW computes only dL and dR (dW and Wm may be
+ * NULL); SLOPE_SKIP_ADAPTER computes only dW (XL, G, dL, dR may be NULL);
+ * both together are SLOPE_ERR_INVALID_ARG.  T == 0 writes zeros (or leaves
+ * them, when accumulating).  Size rules as slope_linear_fwd.
  */
 int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T, int64_t in, int64_t out,
                             const uint8_t* Wm, const void* XL, const void* G, int r, float* dW,

@@ -264,13 +264,17 @@ extern "C" int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T,
                                        void* stream) {
   (void)workspace; (void)workspace_bytes;
   if (int s = check_linear(T, in, out, r)) return s;
-  if (flags & ~(SLOPE_DW_DENSE | SLOPE_ACCUMULATE)) return SLOPE_ERR_INVALID_ARG;
-  if (!Wm || !dW) return SLOPE_ERR_INVALID_ARG;
+  const uint32_t known = SLOPE_DW_DENSE | SLOPE_ACCUMULATE | SLOPE_SKIP_DW | SLOPE_SKIP_ADAPTER;
+  if (flags & ~known) return SLOPE_ERR_INVALID_ARG;
+  if ((flags & SLOPE_SKIP_DW) && (flags & SLOPE_SKIP_ADAPTER)) return SLOPE_ERR_INVALID_ARG;
+  const bool do_dw = !(flags & SLOPE_SKIP_DW);
+  const bool do_ad = r > 0 && !(flags & SLOPE_SKIP_ADAPTER);
+  if (do_dw && (!Wm || !dW)) return SLOPE_ERR_INVALID_ARG;
   if (T > 0 && (!dY || !X)) return SLOPE_ERR_INVALID_ARG;
-  if (r > 0 && (!dL || !dR || (T > 0 && (!XL || !G)))) return SLOPE_ERR_INVALID_ARG;
-  if (!aligned16(Wm) || !aligned16(dW) || (T > 0 && (!aligned16(dY) || !aligned16(X))))
-    return SLOPE_ERR_ALIGNMENT;
-  if (r > 0 && (!aligned16(dL) || !aligned16(dR) || (T > 0 && (!aligned16(XL) || !aligned16(G)))))
+  if (do_ad && (!dL || !dR || (T > 0 && (!XL || !G)))) return SLOPE_ERR_INVALID_ARG;
+  if (do_dw && (!aligned16(Wm) || !aligned16(dW))) return SLOPE_ERR_ALIGNMENT;
+  if (T > 0 && (!aligned16(dY) || !aligned16(X))) return SLOPE_ERR_ALIGNMENT;
+  if (do_ad && (!aligned16(dL) || !aligned16(dR) || (T > 0 && (!aligned16(XL) || !aligned16(G)))))
     return SLOPE_ERR_ALIGNMENT;
   if (int s = check_device()) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -278,21 +282,23 @@ extern "C" int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T,
   const size_t dw_bytes = static_cast<size_t>(out) * (dense ? in : in / 2) * sizeof(float);
   if (T == 0) {
     if (!acc) {
-      if (cudaMemsetAsync(dW, 0, dw_bytes, st) != cudaSuccess) return SLOPE_ERR_CUDA;
-      if (r > 0 && (cudaMemsetAsync(dL, 0, sizeof(float) * in * r, st) != cudaSuccess ||
+      if (do_dw && cudaMemsetAsync(dW, 0, dw_bytes, st) != cudaSuccess) return SLOPE_ERR_CUDA;
+      if (do_ad && (cudaMemsetAsync(dL, 0, sizeof(float) * in * r, st) != cudaSuccess ||
                     cudaMemsetAsync(dR, 0, sizeof(float) * out * r, st) != cudaSuccess))
         return SLOPE_ERR_CUDA;
     }
     return SLOPE_OK;
   }
-  // dW = M ⊙ (dYᵀ·X): M = out, N = in, K = T; A = dY MN-major, B = X MN-major.
-  DenseGemmArgs w{};
-  w.a = dY; w.b = X; w.a_mn_major = true; w.b_mn_major = true;
-  w.M = out; w.N = in; w.K = T; w.lda = out; w.ldb = in;
-  w.epi = DenseEpi::MaskedWeightGrad; w.out = dW; w.ldo = dense ? in : in / 2;
-  w.meta = Wm; w.dense_dw = dense; w.accumulate = acc; w.splits = 1;
-  if (launch_dense_gemm(w, st) != cudaSuccess) return SLOPE_ERR_CUDA;
-  if (r == 0) return SLOPE_OK;
+  if (do_dw) {
+    // dW = M ⊙ (dYᵀ·X): M = out, N = in, K = T; A = dY MN-major, B = X MN-major.
+    DenseGemmArgs w{};
+    w.a = dY; w.b = X; w.a_mn_major = true; w.b_mn_major = true;
+    w.M = out; w.N = in; w.K = T; w.lda = out; w.ldb = in;
+    w.epi = DenseEpi::MaskedWeightGrad; w.out = dW; w.ldo = dense ? in : in / 2;
+    w.meta = Wm; w.dense_dw = dense; w.accumulate = acc; w.splits = 0;
+    if (launch_dense_gemm(w, st) != cudaSuccess) return SLOPE_ERR_CUDA;
+  }
+  if (!do_ad) return SLOPE_OK;
   if (!acc) {
     if (cudaMemsetAsync(dL, 0, sizeof(float) * in * r, st) != cudaSuccess ||
         cudaMemsetAsync(dR, 0, sizeof(float) * out * r, st) != cudaSuccess)

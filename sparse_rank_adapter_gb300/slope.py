@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(PKG, "libslope.so")
 
 OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(7)
 F32, BF16 = 0, 1
-DW_DENSE, ACCUMULATE = 1, 2
+DW_DENSE, ACCUMULATE, SKIP_DW, SKIP_ADAPTER = 1, 2, 4, 8
 
 # (name, restype, argtypes) of every exported function, in header order.
 _vp, _i64, _i, _u32, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32, ctypes.c_size_t
@@ -175,6 +175,8 @@ def slope_linear_bwd_weight(dY, X, Wm, XL, G, dW, dL=None, dR=None, flags: int =
     T, out = dY.shape
     inp = X.shape[1]
     r = 0 if XL is None else XL.shape[1] // 2
+    if r == 0 and dL is not None:
+        r = dL.shape[1]
     dw_shape = (out, inp) if flags & DW_DENSE else (out, inp // 2)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib().slope_linear_bwd_weight(

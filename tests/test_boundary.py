@@ -104,7 +104,9 @@ def test_linear_argument_checks(L):
     assert fwd(A, 0, 256, 256, A, A, A, A, 8, A, 0, A, None, 0, None) == L.OK  # T == 0
     assert bi(A, 64, 256, 384, A, A, A, A, 16, A, 1, None, None, 0, None) == L.ERR_INVALID_ARG
     assert bi(A, 64, 256, 130, A, A, A, A, 16, A, 1, A, None, 0, None) == L.ERR_SHAPE
-    assert bw(A, A, 64, 256, 256, A, A, A, 8, A, 4, A, A, None, 0, None) == L.ERR_INVALID_ARG  # bad flag
+    assert bw(A, A, 64, 256, 256, A, A, A, 8, A, 16, A, A, None, 0, None) == L.ERR_INVALID_ARG  # unknown flag
+    assert bw(A, A, 64, 256, 256, A, A, A, 8, A, 4 | 8, A, A, None, 0, None) == L.ERR_INVALID_ARG  # skip both
+    assert bw(A, A, 64, 256, 256, A, A, A, 8, None, 4, None, A, None, 0, None) == L.ERR_INVALID_ARG  # no dL
     assert bw(A, A, 64, 256, 256, None, A, A, 8, A, 0, A, A, None, 0, None) == L.ERR_INVALID_ARG
     assert bw(A, A, 64, 256, 256, A, A, A, 8, A, 0, None, A, None, 0, None) == L.ERR_INVALID_ARG
     assert bw(A, A, 64, 256, 256, A, A, A, 8, MIS, 0, A, A, None, 0, None) == L.ERR_ALIGNMENT

@@ -160,3 +160,27 @@ def test_identity_inputs_expose_layout(S):
     ref = ws.T + O.bf16_to_f64(d["L"]) @ O.bf16_to_f64(d["R"])
     got = np64(g["Y"])
     np.testing.assert_allclose(got, ref, rtol=2e-6, atol=1e-7)
+
+
+def test_weight_grad_skip_flags(S):
+    """SLOPE_SKIP_ADAPTER computes dW alone and leaves dL, dR untouched;
+    SLOPE_SKIP_DW computes dL, dR alone and leaves dW untouched."""
+    import torch
+
+    T, inp, out, r = 300, 512, 256, 16
+    d = synth.layer_inputs(0, 21, T, inp, out, r)
+    g = run_layer(S, d, T, inp, out, r)
+    X, dY = to_dev(d["X"]), to_dev(d["dY"])
+    dW = torch.full_like(g["dW"], 7.0)
+    dL = torch.full_like(g["dL"], 7.0)
+    dR = torch.full_like(g["dR"], 7.0)
+    S.slope_linear_bwd_weight(dY, X, g["Wm"], g["XL"], g["G"], dW, dL, dR, flags=S.SKIP_ADAPTER)
+    torch.cuda.synchronize()
+    torch.testing.assert_close(dW, g["dW"], rtol=0, atol=0)
+    assert (dL == 7.0).all() and (dR == 7.0).all()
+    dW.fill_(7.0)
+    S.slope_linear_bwd_weight(dY, X, g["Wm"], g["XL"], g["G"], dW, dL, dR, flags=S.SKIP_DW)
+    torch.cuda.synchronize()
+    assert (dW == 7.0).all()
+    torch.testing.assert_close(dL, g["dL"], rtol=1e-5, atol=1e-6)
+    torch.testing.assert_close(dR, g["dR"], rtol=1e-5, atol=1e-6)
