@@ -41,6 +41,23 @@ int sm_count() {
   return n;
 }
 
+int choose_splits(int tiles, int slots, int num_kb) {
+  if (tiles <= 0 || slots <= 0 || num_kb <= 0) return 1;
+  const int max_split = num_kb / 4 > 0 ? num_kb / 4 : 1;
+  int best = 1;
+  long long best_cost = -1;
+  for (int s = 1; s <= max_split; ++s) {
+    const long long waves = (static_cast<long long>(tiles) * s + slots - 1) / slots;
+    const long long per_unit = (num_kb + s - 1) / s + (s > 1 ? 8 : 4);
+    const long long cost = waves * per_unit + (s > 1 ? 8 : 0);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
 // The kernels are built for sm_103a only; any other device is refused.
 static int check_device() {
   const int dev = current_device();

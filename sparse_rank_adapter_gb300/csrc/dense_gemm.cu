@@ -130,8 +130,7 @@ __device__ __forceinline__ void epilogue_chunk(const DnParams& p, const uint32_t
       for (int u = 0; u < 8; ++u) {
         float4 x = make_float4(d[4 * u], d[4 * u + 1], d[4 * u + 2], d[4 * u + 3]);
         if (p.atomic_out) {
-          red_add_f32(&dst[u].x, x.x); red_add_f32(&dst[u].y, x.y);
-          red_add_f32(&dst[u].z, x.z); red_add_f32(&dst[u].w, x.w);
+          red_add_f32x4(reinterpret_cast<float*>(&dst[u]), x);
         } else {
           if (p.accumulate) {
             const float4 y = dst[u];
@@ -156,8 +155,7 @@ __device__ __forceinline__ void epilogue_chunk(const DnParams& p, const uint32_t
       for (int u = 0; u < 4; ++u) {
         float4 x = make_float4(kept[4 * u], kept[4 * u + 1], kept[4 * u + 2], kept[4 * u + 3]);
         if (p.atomic_out) {
-          red_add_f32(&dst[u].x, x.x); red_add_f32(&dst[u].y, x.y);
-          red_add_f32(&dst[u].z, x.z); red_add_f32(&dst[u].w, x.w);
+          red_add_f32x4(reinterpret_cast<float*>(&dst[u]), x);
         } else {
           if (p.accumulate) {
             const float4 y = dst[u];
@@ -567,10 +565,7 @@ cudaError_t run_dw_pair(const DenseGemmArgs& a, cudaStream_t stream) {
   const int tiles_n = static_cast<int>((N + kPairBN - 1) / kPairBN);
   const int clusters_max = max_clusters[dev].load();
   const int pair_tiles = (tiles_m / 2) * tiles_n;
-  int splits = (clusters_max + pair_tiles - 1) / pair_tiles;
-  const int max_split = num_kb / 4 > 0 ? num_kb / 4 : 1;
-  if (splits > max_split) splits = max_split;
-  if (splits < 1) splits = 1;
+  int splits = choose_splits(pair_tiles, clusters_max, num_kb);
   const int kbs = (num_kb + splits - 1) / splits;
   splits = (num_kb + kbs - 1) / kbs;
 
@@ -629,13 +624,7 @@ cudaError_t run(const DenseGemmArgs& a, cudaStream_t stream) {
   const int tiles_m = static_cast<int>((M + kBM - 1) / kBM);
   const int tiles_n = static_cast<int>((N + BN - 1) / BN);
   int splits = a.splits;
-  if (splits <= 0) {
-    const int tiles = tiles_m * tiles_n;
-    splits = (2 * sm_count() + tiles - 1) / tiles;
-    const int max_split = num_kb / 4 > 0 ? num_kb / 4 : 1;
-    if (splits > max_split) splits = max_split;
-    if (splits < 1) splits = 1;
-  }
+  if (splits <= 0) splits = choose_splits(tiles_m * tiles_n, sm_count(), num_kb);
   if (EPI == DenseEpi::StoreBf16HiLo) splits = 1;
   const int kbs = (num_kb + splits - 1) / splits;
   splits = (num_kb + kbs - 1) / kbs;  // every split owns >= 1 K-block

@@ -13,6 +13,13 @@ namespace slope {
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Split-K factor for `tiles` output tiles of `num_kb` K-blocks each, run on
+// `slots` concurrent CTAs (or CTA pairs): the s that minimises
+//   ceil(tiles * s / slots) * (ceil(num_kb / s) + epilogue) (+ zero-fill),
+// in K-block units, with a dearer epilogue once partial sums are added
+// atomically.  At most max(num_kb / 4, 1).
+int choose_splits(int tiles, int slots, int num_kb);
+
 // Device address of the status word that bounded waits report into (per
 // device, resolved once with the device current), or NULL on error.
 unsigned int* device_status_ptr();

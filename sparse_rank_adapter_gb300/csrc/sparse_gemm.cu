@@ -18,12 +18,14 @@
 //
 // Persistent kernel, one CTA per SM, tiles taken round-robin.  With PAIR,
 // CTAs run in clusters of two on adjacent M tiles with the same N tile: each
-// loads half of the shared B tile (the tokens) and multicasts it to both, so
-// an SM pulls 2/3 of the bytes per K-block it would alone; a stage is
-// refilled only after both CTAs' MMAs released it.  Roles (320
-// threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues the MMAs
-// (one thread), warps 2..5 drain the accumulator, warps 6..9 move each
-// stage's 2:4 metadata from shared memory into TMEM.  The accumulator is
+// loads half of the shared B tile (the tokens) and multicasts it to both,
+// and a stage is refilled only after both CTAs' MMAs released it.
+//
+// Roles (448 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues
+// the MMAs (one thread), warps 2..5 drain the accumulator, and two groups of
+// four warps (6..9 for the even stages of the ring, 10..13 for the odd ones)
+// move each stage's 2:4 metadata from shared memory into TMEM, so the short
+// stages of narrow tiles do not wait on it.  The accumulator is
 // double-buffered in TMEM, so the epilogue of one tile overlaps the K-loop
 // of the next.  Every mbarrier wait is bounded.
 //
@@ -52,7 +54,7 @@ constexpr int kBM = 128;               // weight rows per tile (MMA M)
 constexpr int kBKc = 64;               // compressed A columns per stage (= 128 logical K)
 constexpr int kA_BYTES = kBM * 128;    // 16 KB: 128 rows x 128 B (SW128)
 constexpr int kMETA_BYTES = kBM * 16;  // 2 KB: 128 rows x 16 B (32 groups)
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 
 template <int BN>
 struct SpCfg {
@@ -313,12 +315,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // meta_full, adapter fills (no metadata) included, so both barriers of a
     // stage move through the same phases.
     const int q = warp & 3;
+    // Group g owns the stages of parity g and takes every fill of them in
+    // order, so it never waits on a barrier more than one phase ahead (a
+    // parity wait cannot tell phase p from phase p + 2).
+    const int group = (warp - 6) >> 2;
     const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::META_COL;
     int it = 0;
     bool stop = false;
     for (int u = unit0; u < units && !stop; u += ustep) {
       for (int kb = 0; kb < per_tile; ++kb, ++it) {
         const int s = it % C::STAGES;
+        if ((s & 1) != group) continue;
         const uint32_t ph = (it / C::STAGES) & 1;
         if (!mbar_wait(&full[s], ph, abort_flag, p.status)) { stop = true; break; }
         if (kb < p.num_kb) {  // adapter stages carry no metadata
