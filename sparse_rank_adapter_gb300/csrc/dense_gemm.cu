@@ -55,6 +55,7 @@ struct DnParams {
   int M, N, K;
   int kb_per_split, num_kb;
   int tiles_m, tiles_n, num_tiles;  // tiles = tiles_m x tiles_n x splits
+  int group_n;                      // pair kernel: N tiles per raster band
   int64_t ldo;
   void* out;
   const uint8_t* meta;  // masked dW: metadata, N/8 bytes per row
@@ -391,11 +392,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int units = per_split * (p.num_tiles / (p.tiles_m * p.tiles_n));
   const int unit0 = static_cast<int>(blockIdx.x >> 1);
   const int ustep = static_cast<int>(gridDim.x >> 1);
+  // Raster order within a split: bands of group_n N tiles; within a band the
+  // N tiles turn fastest, then the M pairs, so the band's X tiles stay in L2
+  // while each dY tile is used by the whole band as soon as it is loaded.
   auto decode = [&](int u, int& m0, int& n0, int& z) {
     const int mn = u % per_split;
     z = u / per_split;
-    m0 = (2 * (mn % pairs_m) + static_cast<int>(rank)) * kBM;  // this CTA's 128 rows
-    n0 = (mn / pairs_m) * kPairBN;                             // the pair's 256 columns
+    const int per_band = p.group_n * pairs_m;
+    const int b = mn / per_band, w = mn % per_band;
+    const int first = b * p.group_n;
+    const int gn = min(p.group_n, p.tiles_n - first);
+    m0 = (2 * (w / gn) + static_cast<int>(rank)) * kBM;  // this CTA's 128 rows
+    n0 = (first + w % gn) * kPairBN;                       // the pair's 256 columns
   };
 
   if (threadIdx.x == 0) {
@@ -574,6 +582,11 @@ cudaError_t run_dw_pair(const DenseGemmArgs& a, cudaStream_t stream) {
   p.kb_per_split = kbs; p.num_kb = num_kb;
   p.tiles_m = tiles_m; p.tiles_n = tiles_n;
   p.num_tiles = tiles_m * tiles_n * splits;
+  {  // a band of X tiles (256 columns over the split's K range) of about 40 MB
+    const double tile_bytes = 2.0 * kPairBN * kBK * kbs;
+    int g = static_cast<int>(40.0e6 / tile_bytes);
+    p.group_n = g < 1 ? 1 : (g > tiles_n ? tiles_n : g);
+  }
   p.ldo = a.ldo; p.out = a.out; p.meta = a.meta;
   p.dense_dw = a.dense_dw ? 1 : 0;
   p.accumulate = a.accumulate ? 1 : 0;

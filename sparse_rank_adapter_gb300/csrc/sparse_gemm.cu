@@ -83,6 +83,7 @@ __device__ __forceinline__ uint32_t pair_rows(uint32_t w, int lane) {
 struct SpParams {
   int M, N, K, r;
   int tiles_m, num_tiles;
+  int group_m;     // M tiles (or pairs) per raster group: a band of weight tiles kept in L2
   int num_kb;      // sparse K-blocks (K / 128)
   int num_ab;      // adapter blocks per part (ceil(r / 64)); parts: hi, lo
   int out_bf16;
@@ -117,11 +118,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int units = PAIR ? p.num_tiles / 2 : p.num_tiles;
   const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int ustep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-  const int pairs_m = p.tiles_m / 2;
-  auto tile_m0 = [&](int u) {
-    return PAIR ? (2 * (u % pairs_m) + static_cast<int>(rank)) * kBM : (u % p.tiles_m) * kBM;
+  // Raster order: bands of group_m M tiles (pairs with PAIR); within a band
+  // the M tiles turn fastest, then the N tiles, so the band's weight tiles
+  // stay in L2 while every token tile passes over them once.
+  const int rows_m = PAIR ? p.tiles_m / 2 : p.tiles_m;
+  const int tiles_n = units / rows_m;
+  auto band = [&](int u, int& mi, int& ni) {
+    const int per_band = p.group_m * tiles_n;
+    const int b = u / per_band, w = u % per_band;
+    const int first = b * p.group_m;
+    const int gm = min(p.group_m, rows_m - first);
+    mi = first + w % gm;
+    ni = w / gm;
   };
-  auto tile_n0 = [&](int u) { return PAIR ? (u / pairs_m) * BN : (u / p.tiles_m) * BN; };
+  auto tile_m0 = [&](int u) {
+    int mi, ni;
+    band(u, mi, ni);
+    return PAIR ? (2 * mi + static_cast<int>(rank)) * kBM : mi * kBM;
+  };
+  auto tile_n0 = [&](int u) {
+    int mi, ni;
+    band(u, mi, ni);
+    return ni * BN;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -421,6 +440,12 @@ cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
   p.num_tiles = p.tiles_m * static_cast<int>((N + BN - 1) / BN);
   p.num_kb = static_cast<int>(K / 128);
   p.num_ab = static_cast<int>((r + 63) / 64);
+  {  // a band of weight tiles (values + metadata, all of K) of about 40 MB
+    const double tile_bytes = static_cast<double>(kBM) * K * 1.125 * (PAIR ? 2 : 1);
+    int g = static_cast<int>(40.0e6 / tile_bytes);
+    const int rows = PAIR ? p.tiles_m / 2 : p.tiles_m;
+    p.group_m = g < 1 ? 1 : (g > rows ? rows : g);
+  }
   p.out_bf16 = a.out_bf16 ? 1 : 0;
   p.out = a.out;
   p.status = device_status_ptr();
