@@ -1,8 +1,12 @@
 // prune.cu — the two memory-bound kernels of the path.
 //
 //   prune24_kernel            2:4 magnitude prune-and-compress of W (A1).
-//   double_prune24_kernel     transpose of the pruned W, pruned 2:4 again
-//                             along the old out dimension (A2).
+//   double_prune24_staged_kernel / double_prune24_kernel
+//                             transpose of the pruned W, pruned 2:4 again
+//                             along the old out dimension (A2); the staged
+//                             kernel (cols % 128 == 0) moves its tiles
+//                             through shared memory, the other reads global
+//                             memory directly and takes any legal shape.
 //
 // Source: "SLoPe: Double-Pruned Sparse Plus Lazy Low-Rank Adapter Pretraining
 // of LLMs", §1 and §2.1 (N:M pruning of the weight, then of its transpose)
@@ -11,6 +15,7 @@
 // compressed format is the one slope.h documents.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "slope_internal.h"
@@ -88,62 +93,229 @@ __global__ void __launch_bounds__(kPruneThreads) prune24_kernel(const uint4* __r
 }
 
 // ---------------------------------------------------------------- A2 ------
-// Work item: 8 consecutive rows (one "octet" h8) x 16 consecutive columns
-// (chunk c16) of the rows x cols pruned weight.  It reads 8 x 16 B of kept
-// values and 8 x 2 B of metadata, rebuilds the 8 x 16 block (pruned = +0),
-// and for each of the 16 columns i prunes the two row-quadruples along the
-// old row dimension: 4 kept values (8 B) and one metadata byte for row i of
-// the transposed output, at column octet h8.  Lanes of a warp take
-// consecutive octets of the same chunk, so each output row segment a warp
-// writes is 256 B (values) / 32 B (metadata) contiguous.
 
-constexpr int kDpThreads = 256;  // 8 warps = 8 column chunks per tile
+constexpr int kDpThreads = 256;  // direct kernel: 8 warps = 8 column chunks per tile
 
-__device__ __forceinline__ uint32_t expanded(uint32_t pair, uint32_t nib, uint32_t j) {
+// Byte-permute selectors that expand a compressed group (kept pair: lower
+// column in bytes 0-1, upper in 2-3 of one word; the permute's second word
+// is zero) into its four columns, two per output word: .x builds columns
+// 0-1, .y columns 2-3.  Indexed by the metadata nibble.
+__device__ __forceinline__ uint2 expand_selectors(uint32_t nib) {
   const uint32_t i0 = nib & 3u, i1 = nib >> 2;
-  return (j == i0) ? (pair & 0xFFFFu) : ((j == i1) ? (pair >> 16) : 0u);
+  uint32_t sel = 0;
+#pragma unroll
+  for (uint32_t pos = 0; pos < 4; ++pos) {
+    const uint32_t src = pos == i0 ? 0u : (pos == i1 ? 2u : 4u);  // 4: a zero byte
+    sel |= (src | ((src + 1) << 4)) << (8 * pos);
+  }
+  return make_uint2(sel & 0xFFFFu, sel >> 16);
 }
 
+// Output of a transposed group from the in-quadruple codes (3 - row) of its
+// two winners, first and second by rank: the low 16 bits are the permute
+// selector that packs the kept pair in ascending row order (candidate k
+// sits in bytes 2k, 2k+1 of the two candidate words); bits 16 + nib_shift
+// and up hold the metadata nibble i0 | i1 << 2.
+__device__ __forceinline__ uint32_t output_entry(uint32_t code_first, uint32_t code_second,
+                                                 uint32_t nib_shift) {
+  const uint32_t j1 = 3u - code_first, j2 = 3u - code_second;
+  const uint32_t lo = j1 < j2 ? j1 : j2, hi = j1 < j2 ? j2 : j1;
+  const uint32_t sel = (2 * lo) | ((2 * lo + 1) << 4) | ((2 * hi) << 8) | ((2 * hi + 1) << 12);
+  return sel | ((lo | (hi << 2)) << (16 + nib_shift));
+}
+
+struct DpTables {
+  uint2 expand[16];     // by metadata nibble
+  uint32_t out[2][16];  // [upper / lower quadruple of the octet][code_first * 4 + code_second]
+};
+
+__device__ __forceinline__ void fill_tables(DpTables& t) {
+  if (threadIdx.x < 16) t.expand[threadIdx.x] = expand_selectors(threadIdx.x);
+  if (threadIdx.x < 32) {
+    const uint32_t g = threadIdx.x >> 4, idx = threadIdx.x & 15;
+    t.out[g][idx] = output_entry(idx >> 2, idx & 3, 4 * g);
+  }
+}
+
+// Top two of the four candidates of a transposed group, packed as two rows
+// per word (w01: rows 0 and 1, w23: rows 2 and 3, lower row in the low
+// half).  Rank keys are magnitude << 2 | (3 - row): larger magnitude first,
+// then the lower row.  Returns the table entry of the two winners.
+__device__ __forceinline__ uint32_t top2_entry(uint32_t w01, uint32_t w23, const uint32_t* out) {
+  const uint32_t c0 = (w01 & 0x7FFFu) * 4u + 3u;
+  const uint32_t c1 = __umulhi((w01 & 0x7FFF0000u) | 0x8000u, 1u << 18);  // (mag << 2) | 2
+  const uint32_t c2 = (w23 & 0x7FFFu) * 4u + 1u;
+  const uint32_t c3 = __umulhi(w23 & 0x7FFF0000u, 1u << 18);              // (mag << 2) | 0
+  const uint32_t a = max(c0, c1), b = min(c0, c1);
+  const uint32_t c = max(c2, c3), d = min(c2, c3);
+  const uint32_t first = max(a, c);
+  const uint32_t second = max(min(a, c), max(b, d));
+  return out[(first & 3u) * 4u + (second & 3u)];
+}
+
+// Work item: 8 consecutive rows (one "octet" h8) x 16 consecutive columns
+// (chunk c16) of the rows x cols pruned weight, given as each row's 16 B of
+// kept values v[k] and 16 bits of metadata m[k].  It expands each row's four
+// groups with byte permutes (pruned positions become +0) and, for each of
+// the 16 columns, prunes the two row-quadruples along the old row
+// dimension: 4 kept values (8 B) and one metadata byte for row i of the
+// transposed output, at column octet h8.  Lanes of a warp take consecutive
+// octets of the same chunk, so each output row segment a warp writes is
+// 256 B (values) / 32 B (metadata) contiguous.
+__device__ __forceinline__ void transpose_prune_octet(const uint4 (&v)[8], const uint32_t (&m)[8],
+                                                      const DpTables& tab,
+                                                      uint2* __restrict__ t_vals,
+                                                      uint8_t* __restrict__ t_meta,
+                                                      int64_t out_stride, uint32_t h8,
+                                                      uint32_t c16) {
+  uint2* tv = t_vals + 16 * static_cast<int64_t>(c16) * out_stride + h8;
+  uint8_t* tm = t_meta + 16 * static_cast<int64_t>(c16) * out_stride + h8;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {  // group of 4 columns within the chunk
+    uint32_t e0[8], e1[8];        // row k, columns 0-1 / 2-3 of the group
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t pair = (q == 0) ? v[k].x : (q == 1) ? v[k].y : (q == 2) ? v[k].z : v[k].w;
+      const uint2 sel = tab.expand[(m[k] >> (4 * q)) & 0xFu];
+      e0[k] = __byte_perm(pair, 0u, sel.x);
+      e1[k] = __byte_perm(pair, 0u, sel.y);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t* e = (j < 2) ? e0 : e1;
+      const uint32_t pick = (j & 1) ? 0x7632u : 0x5410u;  // high or low halves of two words
+      const uint32_t a01 = __byte_perm(e[0], e[1], pick), a23 = __byte_perm(e[2], e[3], pick);
+      const uint32_t b01 = __byte_perm(e[4], e[5], pick), b23 = __byte_perm(e[6], e[7], pick);
+      const uint32_t ea = top2_entry(a01, a23, tab.out[0]);
+      const uint32_t eb = top2_entry(b01, b23, tab.out[1]);
+      const int64_t i = 4 * q + j;
+      __stcs(tv + i * out_stride, make_uint2(__byte_perm(a01, a23, ea), __byte_perm(b01, b23, eb)));
+      // the selectors stay below 0x8000, so the sum carries nothing into the nibbles
+      tm[i * out_stride] = static_cast<uint8_t>((ea + eb) >> 16);
+    }
+  }
+}
+
+// Any shape (rows % 8 == 0, cols % 16 == 0): each thread loads its octet's
+// rows straight from global memory; the eight warps of a block take
+// adjacent chunks, whose loads share sectors in L1.
 __global__ void __launch_bounds__(kDpThreads) double_prune24_kernel(
     const uint4* __restrict__ vals, const uint16_t* __restrict__ meta, uint2* __restrict__ t_vals,
     uint8_t* __restrict__ t_meta, int64_t rows, int64_t cols) {
-  const int64_t n_h8 = rows / 8, n_c16 = cols / 16;
-  const int64_t tiles_h = (n_h8 + 31) / 32, tiles_c = (n_c16 + 7) / 8;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int64_t tile = blockIdx.x; tile < tiles_h * tiles_c; tile += gridDim.x) {
-    const int64_t h8 = (tile % tiles_h) * 32 + lane;
-    const int64_t c16 = (tile / tiles_h) * 8 + warp;
+  __shared__ DpTables tab;
+  fill_tables(tab);
+  __syncthreads();
+  const uint32_t n_h8 = static_cast<uint32_t>(rows / 8), n_c16 = static_cast<uint32_t>(cols / 16);
+  const uint32_t tiles_h = (n_h8 + 31) / 32, tiles_c = (n_c16 + 7) / 8;
+  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (uint32_t tile = blockIdx.x; tile < tiles_h * tiles_c; tile += gridDim.x) {
+    const uint32_t h8 = (tile % tiles_h) * 32 + lane;
+    const uint32_t c16 = (tile / tiles_h) * 8 + warp;
     if (h8 >= n_h8 || c16 >= n_c16) continue;
     uint4 v[8];
     uint32_t m[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const int64_t row = 8 * h8 + k;
-      v[k] = __ldcs(vals + row * n_c16 + c16);
-      m[k] = __ldcs(meta + row * n_c16 + c16);
+      const int64_t at = (static_cast<int64_t>(8) * h8 + k) * n_c16 + c16;
+      v[k] = __ldg(vals + at);
+      m[k] = __ldg(meta + at);
     }
-    const int64_t out_stride = rows / 8;  // uint2 / bytes per output row
+    transpose_prune_octet(v, m, tab, t_vals, t_meta, rows / 8, h8, c16);
+  }
+}
+
+// cols % 128 == 0: tiles of 256 rows x 16·CH columns staged through shared
+// memory.  Global reads are whole row segments (16·CH bytes of values,
+// 2·CH bytes of metadata per row) copied with cp.async into a layout where
+// the per-thread reads of the compute phase are free of bank conflicts:
+// values of row 8·o + k, chunk c at k·plane + o·16·CH + 16·(c ^ f(o)) with
+// f(o) = (o / (8 / CH)) % CH, so any 8 consecutive lanes (octets o) reading
+// chunk c hit 8 different 16 B bank groups; metadata of that row at
+// k·(32·16) + o·16 + 2·c.  Two stages: the copies of the next tile are in
+// flight while the current one is pruned.
+template <int CH>
+__device__ __forceinline__ uint32_t swz(uint32_t o) { return (o / (8 / CH)) % CH; }
+
+template <int CH>
+struct DpStaged {
+  static constexpr int kThreads = 32 * CH;
+  static constexpr int kValPitch = 16 * CH;
+  static constexpr int kValPlane = 32 * kValPitch;
+  static constexpr int kValBytes = 8 * kValPlane;
+  static constexpr int kMetaBytes = 256 * 16;
+  static constexpr int kStage = kValBytes + kMetaBytes;
+  static constexpr int kSmem = 2 * kStage;
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+
+template <int CH>
+__global__ void __launch_bounds__(32 * CH) double_prune24_staged_kernel(
+    const uint8_t* __restrict__ vals, const uint8_t* __restrict__ meta, uint2* __restrict__ t_vals,
+    uint8_t* __restrict__ t_meta, int64_t rows, int64_t cols) {
+  using C = DpStaged<CH>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ DpTables tab;
+  fill_tables(tab);
+  const uint32_t n_h8 = static_cast<uint32_t>(rows / 8);
+  const uint32_t tiles_h = (static_cast<uint32_t>(rows) + 255) / 256;
+  const uint32_t tiles_c = static_cast<uint32_t>(cols / (16 * CH));
+  const uint32_t ntiles = tiles_h * tiles_c;
+  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t val_pitch = cols, meta_pitch = cols / 8;  // bytes per input row
+  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+
+  auto issue = [&](uint32_t tile, int stage) {
+    const uint32_t row0 = (tile % tiles_h) * 256, ch0 = (tile / tiles_h) * CH;
+    const uint32_t st = sbase + stage * C::kStage;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {  // group of 4 columns within the chunk
-      uint32_t pair[8], nib[8];
+    for (int i = 0; i < 8; ++i) {  // 256 rows x CH chunks of 16 B values
+      const uint32_t u = threadIdx.x + i * C::kThreads;
+      const uint32_t r = u / CH, c = u % CH;
+      if (row0 + r < rows)
+        cp_async16(st + (r & 7) * C::kValPlane + (r >> 3) * C::kValPitch + 16 * (c ^ swz<CH>(r >> 3)),
+                   vals + (row0 + r) * val_pitch + 16 * (ch0 + c));
+    }
+    // One 16 B piece of metadata per row, holding the tile's 2·CH bytes
+    // (and, for CH < 8, neighbouring bytes that are never read).
+    for (uint32_t r = threadIdx.x; r < 256; r += C::kThreads)
+      if (row0 + r < rows) {
+        const int64_t off = (row0 + r) * meta_pitch + 2 * ch0;
+        cp_async16(st + C::kValBytes + (r & 7) * 512 + (r >> 3) * 16, meta + (off & ~int64_t(15)));
+      }
+  };
+
+  uint32_t tile = blockIdx.x;
+  if (tile < ntiles) issue(tile, 0);
+  cp_async_commit();
+  int stage = 0;
+  for (; tile < ntiles; tile += gridDim.x, stage ^= 1) {
+    const uint32_t next = tile + gridDim.x;
+    if (next < ntiles) issue(next, stage ^ 1);
+    cp_async_commit();
+    cp_async_wait_1();
+    __syncthreads();
+    const uint32_t h8 = (tile % tiles_h) * 32 + lane;
+    const uint32_t ch0 = (tile / tiles_h) * CH;
+    if (h8 < n_h8) {
+      const uint8_t* st = smem + stage * C::kStage;
+      // offset of this tile's metadata inside the 16 B piece that was copied
+      const uint32_t moff = static_cast<uint32_t>((2 * ch0) & 15);
+      uint4 v[8];
+      uint32_t m[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        pair[k] = (q == 0) ? v[k].x : (q == 1) ? v[k].y : (q == 2) ? v[k].z : v[k].w;
-        nib[k] = (m[k] >> (4 * q)) & 0xFu;
+        v[k] = *reinterpret_cast<const uint4*>(st + k * C::kValPlane + lane * C::kValPitch +
+                                               16 * (warp ^ swz<CH>(lane)));
+        m[k] = *reinterpret_cast<const uint16_t*>(st + C::kValBytes + k * 512 + lane * 16 + moff + 2 * warp);
       }
-#pragma unroll
-      for (uint32_t j = 0; j < 4; ++j) {
-        uint32_t e[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) e[k] = expanded(pair[k], nib[k], j);
-        uint32_t na, nb;
-        const uint32_t pa = top2of4(e[0], e[1], e[2], e[3], na);
-        const uint32_t pb = top2of4(e[4], e[5], e[6], e[7], nb);
-        const int64_t i = 16 * c16 + 4 * q + j;
-        __stcs(t_vals + i * out_stride + h8, make_uint2(pa, pb));
-        t_meta[i * out_stride + h8] = static_cast<uint8_t>(na | (nb << 4));
-      }
+      transpose_prune_octet(v, m, tab, t_vals, t_meta, rows / 8, h8, ch0 + warp);
     }
+    __syncthreads();
   }
 }
 
@@ -162,11 +334,46 @@ cudaError_t launch_prune24(const void* W, int64_t rows, int64_t cols, void* vals
   return cudaGetLastError();
 }
 
+template <int CH>
+static cudaError_t run_staged(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols,
+                              void* t_vals, uint8_t* t_meta, cudaStream_t stream) {
+  using C = DpStaged<CH>;
+  auto kernel = double_prune24_staged_kernel<CH>;
+  static std::atomic<int> per_sm[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int blocks_per_sm = per_sm[dev].load();
+  if (!blocks_per_sm) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kernel, C::kThreads, C::kSmem);
+    if (e != cudaSuccess) return e;
+    if (blocks_per_sm < 1) blocks_per_sm = 1;
+    per_sm[dev].store(blocks_per_sm);
+  }
+  const int64_t tiles = ((rows + 255) / 256) * (cols / (16 * CH));
+  const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm;
+  const int64_t blocks = tiles < cap ? tiles : cap;
+  kernel<<<static_cast<unsigned>(blocks), C::kThreads, C::kSmem, stream>>>(
+      static_cast<const uint8_t*>(vals), meta, static_cast<uint2*>(t_vals), t_meta, rows, cols);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_double_prune24(const void* vals, const uint8_t* meta, int64_t rows,
                                   int64_t cols, void* t_vals, uint8_t* t_meta,
                                   cudaStream_t stream) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  if (cols % 128 == 0) {
+    // the widest tile that still gives every SM a tile
+    const int64_t tiles_h = (rows + 255) / 256;
+    if (tiles_h * (cols / 128) >= sm_count())
+      return run_staged<8>(vals, meta, rows, cols, t_vals, t_meta, stream);
+    if (tiles_h * (cols / 64) >= sm_count())
+      return run_staged<4>(vals, meta, rows, cols, t_vals, t_meta, stream);
+    return run_staged<2>(vals, meta, rows, cols, t_vals, t_meta, stream);
+  }
   const int64_t tiles = ((rows / 8 + 31) / 32) * ((cols / 16 + 7) / 8);
-  if (tiles == 0) return cudaSuccess;
   int64_t blocks = tiles;
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
   if (blocks > cap) blocks = cap;

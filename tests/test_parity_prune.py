@@ -41,8 +41,11 @@ def gpu_double(S, vals, meta, rows, cols):
     return tv, tm
 
 
+# cols % 128 == 0 takes the shared-memory staged A2 kernel (32-, 64- or
+# 128-column tiles by size), other widths the direct one; 520 and 2312 rows
+# leave a ragged 256-row tile.
 SHAPES = [(8, 16), (1, 8), (40, 48), (264, 144), (256, 256), (1000, 1040), (1024, 1024),
-          (4096, 1024), (1024, 4096)]
+          (4096, 1024), (1024, 4096), (520, 384), (2312, 2048)]
 
 
 @pytest.mark.parametrize("rows,cols", SHAPES)
