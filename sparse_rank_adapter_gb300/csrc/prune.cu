@@ -139,18 +139,28 @@ __device__ __forceinline__ void fill_tables(DpTables& t) {
 
 // Top two of the four candidates of a transposed group, packed as two rows
 // per word (w01: rows 0 and 1, w23: rows 2 and 3, lower row in the low
-// half).  Rank keys are magnitude << 2 | (3 - row): larger magnitude first,
-// then the lower row.  Returns the table entry of the two winners.
-__device__ __forceinline__ uint32_t top2_entry(uint32_t w01, uint32_t w23, const uint32_t* out) {
-  const uint32_t c0 = (w01 & 0x7FFFu) * 4u + 3u;
-  const uint32_t c1 = __umulhi((w01 & 0x7FFF0000u) | 0x8000u, 1u << 18);  // (mag << 2) | 2
-  const uint32_t c2 = (w23 & 0x7FFFu) * 4u + 1u;
-  const uint32_t c3 = __umulhi(w23 & 0x7FFF0000u, 1u << 18);              // (mag << 2) | 0
+// half).  Rank key of row k: magnitude in bits 17-31, 3 - k in bits 15-16,
+// zeros below: larger magnitude first, then the lower row.  Multiplying a
+// word by 2^17 moves its low half's magnitude to the top and drops the sign
+// and the high half; the high half is shifted by one and masked.  Returns
+// the table entry of the two winners.  `k17` = 2^17 and `k1` = 2 come in at
+// run time: as unknown factors they stay integer multiply-adds, on a pipe
+// this kernel otherwise leaves idle, instead of becoming shifts on the logic
+// pipe, which is its bottleneck.
+__device__ __forceinline__ uint32_t top2_entry(uint32_t w01, uint32_t w23, const uint32_t* out,
+                                               uint32_t k17, uint32_t k1) {
+  const uint32_t c0 = w01 * k17 + 0x18000u;
+  const uint32_t c1 = ((w01 * k1) & 0xFFFE0000u) | 0x10000u;
+  const uint32_t c2 = w23 * k17 + 0x08000u;
+  const uint32_t c3 = (w23 * k1) & 0xFFFE0000u;
   const uint32_t a = max(c0, c1), b = min(c0, c1);
   const uint32_t c = max(c2, c3), d = min(c2, c3);
   const uint32_t first = max(a, c);
   const uint32_t second = max(min(a, c), max(b, d));
-  return out[(first & 3u) * 4u + (second & 3u)];
+  // byte offset 16·code_first + 4·code_second; bits 0-14 of the keys are
+  // zero, so the +1 in each multiplier never reaches the bits kept
+  const uint32_t off = (__umulhi(first, 0x200001u) & 0x30u) | (__umulhi(second, 0x80001u) & 0x0Cu);
+  return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(out) + off);
 }
 
 // Work item: 8 consecutive rows (one "octet" h8) x 16 consecutive columns
@@ -167,7 +177,8 @@ __device__ __forceinline__ void transpose_prune_octet(const uint4 (&v)[8], const
                                                       uint2* __restrict__ t_vals,
                                                       uint8_t* __restrict__ t_meta,
                                                       int64_t out_stride, uint32_t h8,
-                                                      uint32_t c16) {
+                                                      uint32_t c16, uint32_t k17) {
+  const uint32_t k1 = k17 >> 16, k8 = k17 >> 14;
   uint2* tv = t_vals + 16 * static_cast<int64_t>(c16) * out_stride + h8;
   uint8_t* tm = t_meta + 16 * static_cast<int64_t>(c16) * out_stride + h8;
 #pragma unroll
@@ -176,7 +187,10 @@ __device__ __forceinline__ void transpose_prune_octet(const uint4 (&v)[8], const
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const uint32_t pair = (q == 0) ? v[k].x : (q == 1) ? v[k].y : (q == 2) ? v[k].z : v[k].w;
-      const uint2 sel = tab.expand[(m[k] >> (4 * q)) & 0xFu];
+      // byte offset 8·nibble: the shift comes from a multiply-high, whose
+      // +1 term only adds below bit 3
+      const uint32_t m8 = (q == 0) ? m[k] * k8 : __umulhi(m[k], (1u << (35 - 4 * q)) + 1u);
+      const uint2 sel = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(tab.expand) + (m8 & 0x78u));
       e0[k] = __byte_perm(pair, 0u, sel.x);
       e1[k] = __byte_perm(pair, 0u, sel.y);
     }
@@ -186,8 +200,8 @@ __device__ __forceinline__ void transpose_prune_octet(const uint4 (&v)[8], const
       const uint32_t pick = (j & 1) ? 0x7632u : 0x5410u;  // high or low halves of two words
       const uint32_t a01 = __byte_perm(e[0], e[1], pick), a23 = __byte_perm(e[2], e[3], pick);
       const uint32_t b01 = __byte_perm(e[4], e[5], pick), b23 = __byte_perm(e[6], e[7], pick);
-      const uint32_t ea = top2_entry(a01, a23, tab.out[0]);
-      const uint32_t eb = top2_entry(b01, b23, tab.out[1]);
+      const uint32_t ea = top2_entry(a01, a23, tab.out[0], k17, k1);
+      const uint32_t eb = top2_entry(b01, b23, tab.out[1], k17, k1);
       const int64_t i = 4 * q + j;
       __stcs(tv + i * out_stride, make_uint2(__byte_perm(a01, a23, ea), __byte_perm(b01, b23, eb)));
       // the selectors stay below 0x8000, so the sum carries nothing into the nibbles
@@ -201,7 +215,7 @@ __device__ __forceinline__ void transpose_prune_octet(const uint4 (&v)[8], const
 // adjacent chunks, whose loads share sectors in L1.
 __global__ void __launch_bounds__(kDpThreads) double_prune24_kernel(
     const uint4* __restrict__ vals, const uint16_t* __restrict__ meta, uint2* __restrict__ t_vals,
-    uint8_t* __restrict__ t_meta, int64_t rows, int64_t cols) {
+    uint8_t* __restrict__ t_meta, int64_t rows, int64_t cols, uint32_t k17) {
   __shared__ DpTables tab;
   fill_tables(tab);
   __syncthreads();
@@ -220,7 +234,7 @@ __global__ void __launch_bounds__(kDpThreads) double_prune24_kernel(
       v[k] = __ldg(vals + at);
       m[k] = __ldg(meta + at);
     }
-    transpose_prune_octet(v, m, tab, t_vals, t_meta, rows / 8, h8, c16);
+    transpose_prune_octet(v, m, tab, t_vals, t_meta, rows / 8, h8, c16, k17);
   }
 }
 
@@ -256,7 +270,7 @@ __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_
 template <int CH>
 __global__ void __launch_bounds__(32 * CH) double_prune24_staged_kernel(
     const uint8_t* __restrict__ vals, const uint8_t* __restrict__ meta, uint2* __restrict__ t_vals,
-    uint8_t* __restrict__ t_meta, int64_t rows, int64_t cols) {
+    uint8_t* __restrict__ t_meta, int64_t rows, int64_t cols, uint32_t k17) {
   using C = DpStaged<CH>;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ DpTables tab;
@@ -264,13 +278,12 @@ __global__ void __launch_bounds__(32 * CH) double_prune24_staged_kernel(
   const uint32_t n_h8 = static_cast<uint32_t>(rows / 8);
   const uint32_t tiles_h = (static_cast<uint32_t>(rows) + 255) / 256;
   const uint32_t tiles_c = static_cast<uint32_t>(cols / (16 * CH));
-  const uint32_t ntiles = tiles_h * tiles_c;
   const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t val_pitch = cols, meta_pitch = cols / 8;  // bytes per input row
   const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
 
-  auto issue = [&](uint32_t tile, int stage) {
-    const uint32_t row0 = (tile % tiles_h) * 256, ch0 = (tile / tiles_h) * CH;
+  auto issue = [&](uint32_t th, uint32_t tc, int stage) {
+    const uint32_t row0 = th * 256, ch0 = tc * CH;
     const uint32_t st = sbase + stage * C::kStage;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {  // 256 rows x CH chunks of 16 B values
@@ -289,18 +302,27 @@ __global__ void __launch_bounds__(32 * CH) double_prune24_staged_kernel(
       }
   };
 
-  uint32_t tile = blockIdx.x;
-  if (tile < ntiles) issue(tile, 0);
+  // tile t covers row tile t % tiles_h and chunk tile t / tiles_h; the
+  // (row, chunk) pair of the next tile is stepped without dividing
+  const uint32_t step_c = gridDim.x / tiles_h, step_h = gridDim.x % tiles_h;
+  auto advance = [&](uint32_t& th, uint32_t& tc) {
+    th += step_h;
+    tc += step_c;
+    if (th >= tiles_h) { th -= tiles_h; ++tc; }
+  };
+  uint32_t th = blockIdx.x % tiles_h, tc = blockIdx.x / tiles_h;
+  if (tc < tiles_c) issue(th, tc, 0);
   cp_async_commit();
   int stage = 0;
-  for (; tile < ntiles; tile += gridDim.x, stage ^= 1) {
-    const uint32_t next = tile + gridDim.x;
-    if (next < ntiles) issue(next, stage ^ 1);
+  for (; tc < tiles_c; stage ^= 1) {
+    uint32_t nh = th, nc = tc;
+    advance(nh, nc);
+    if (nc < tiles_c) issue(nh, nc, stage ^ 1);
     cp_async_commit();
     cp_async_wait_1();
     __syncthreads();
-    const uint32_t h8 = (tile % tiles_h) * 32 + lane;
-    const uint32_t ch0 = (tile / tiles_h) * CH;
+    const uint32_t h8 = th * 32 + lane;
+    const uint32_t ch0 = tc * CH;
     if (h8 < n_h8) {
       const uint8_t* st = smem + stage * C::kStage;
       // offset of this tile's metadata inside the 16 B piece that was copied
@@ -313,9 +335,11 @@ __global__ void __launch_bounds__(32 * CH) double_prune24_staged_kernel(
                                                16 * (warp ^ swz<CH>(lane)));
         m[k] = *reinterpret_cast<const uint16_t*>(st + C::kValBytes + k * 512 + lane * 16 + moff + 2 * warp);
       }
-      transpose_prune_octet(v, m, tab, t_vals, t_meta, rows / 8, h8, ch0 + warp);
+      transpose_prune_octet(v, m, tab, t_vals, t_meta, rows / 8, h8, ch0 + warp, k17);
     }
     __syncthreads();
+    th = nh;
+    tc = nc;
   }
 }
 
@@ -333,6 +357,8 @@ cudaError_t launch_prune24(const void* W, int64_t rows, int64_t cols, void* vals
       static_cast<const uint4*>(W), static_cast<uint2*>(vals), meta, nchunks);
   return cudaGetLastError();
 }
+
+constexpr uint32_t kKeyShift = 1u << 17;  // the k17 argument of the A2 kernels
 
 template <int CH>
 static cudaError_t run_staged(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols,
@@ -356,7 +382,8 @@ static cudaError_t run_staged(const void* vals, const uint8_t* meta, int64_t row
   const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm;
   const int64_t blocks = tiles < cap ? tiles : cap;
   kernel<<<static_cast<unsigned>(blocks), C::kThreads, C::kSmem, stream>>>(
-      static_cast<const uint8_t*>(vals), meta, static_cast<uint2*>(t_vals), t_meta, rows, cols);
+      static_cast<const uint8_t*>(vals), meta, static_cast<uint2*>(t_vals), t_meta, rows, cols,
+      kKeyShift);
   return cudaGetLastError();
 }
 
@@ -379,7 +406,7 @@ cudaError_t launch_double_prune24(const void* vals, const uint8_t* meta, int64_t
   if (blocks > cap) blocks = cap;
   double_prune24_kernel<<<static_cast<unsigned>(blocks), kDpThreads, 0, stream>>>(
       static_cast<const uint4*>(vals), reinterpret_cast<const uint16_t*>(meta),
-      static_cast<uint2*>(t_vals), t_meta, rows, cols);
+      static_cast<uint2*>(t_vals), t_meta, rows, cols, kKeyShift);
   return cudaGetLastError();
 }
 
