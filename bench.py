@@ -306,18 +306,27 @@ def gpu_arm(args):
             sets[i % n_sets].run(stream)
     stream.synchronize()
 
-    graphs, marks = [], []
+    # Two graphs per input set: a plain one for the timed steps, and one with
+    # an event pair around every ABI call (event-record nodes between the
+    # kernels), replayed after the timed steps for the per-call breakdown, so
+    # that the headline time carries no timing nodes.
+    graphs, mgraphs, marks = [], [], []
     for st in sets:
         m = Marks()
         if args.graph:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                st.run(stream, m)
+                st.run(stream)
             graphs.append(g)
+            gm = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gm, stream=stream):
+                st.run(stream, m)
+            mgraphs.append(gm)
         marks.append(m)
     for i in range(args.warmup):  # warm the graphs too
         if args.graph:
             graphs[i % n_sets].replay()
+            mgraphs[i % n_sets].replay()
     torch.cuda.synchronize()
 
     per_call = {}
@@ -333,16 +342,22 @@ def gpu_arm(args):
                 if args.graph:
                     graphs[i % n_sets].replay()
                 else:
-                    sets[i % n_sets].run(stream, marks[i % n_sets] if i >= args.steps - n_sets else None)
+                    sets[i % n_sets].run(stream)
         t_end.record(stream)
+        # per-call breakdown: one marked pass over every input set
+        with torch.cuda.stream(stream):
+            for i in range(n_sets):
+                if args.graph:
+                    mgraphs[i].replay()
+                else:
+                    sets[i].run(stream, marks[i])
         stream.synchronize()
     if world > 1:
         dist.barrier()
-    # every graph's event pairs hold the times of its last replay
-    for m in marks[: min(n_sets, args.steps)]:
+    for m in marks:
         for name, inp, out, e0, e1 in m.pairs:
             per_call.setdefault(name, []).append((inp, out, e0.elapsed_time(e1)))
-    n_obs = min(n_sets, args.steps)
+    n_obs = n_sets
     clocks = clk.summary()
     ms_step = t_start.elapsed_time(t_end) / args.steps
     calls_ms = {k: sum(x[2] for x in v) / n_obs for k, v in per_call.items()}

@@ -219,6 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  grid_dependency_wait();  // the previous kernel's outputs are visible from here
+  allow_dependents_launch();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -427,6 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  grid_dependency_wait();  // the previous kernel's outputs are visible from here
+  allow_dependents_launch();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -543,7 +547,7 @@ cudaError_t run_dw_pair(const DenseGemmArgs& a, cudaStream_t stream) {
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
@@ -600,6 +604,7 @@ cudaError_t run_dw_pair(const DenseGemmArgs& a, cudaStream_t stream) {
   const int units = pair_tiles * splits;
   const int clusters = units < clusters_max ? units : clusters_max;
   cfg.gridDim = dim3(2 * clusters);
+  add_pdl_attr(cfg, attr);
   cudaError_t e = cudaLaunchKernelEx(&cfg, dw_pair_kernel, tA, tB, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -663,8 +668,15 @@ cudaError_t run(const DenseGemmArgs& a, cudaStream_t stream) {
   p.tiles_m = tiles_m; p.tiles_n = tiles_n;
   p.num_tiles = tiles_m * tiles_n * splits;
   const int grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
-  kernel<<<grid, kThreads, C::SMEM, stream>>>(tA, tB, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  add_pdl_attr(cfg, attr);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tA, tB, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // N tile for the skinny (rank-wide) products.

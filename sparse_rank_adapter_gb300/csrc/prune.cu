@@ -19,6 +19,7 @@
 #include <cstdint>
 
 #include "slope_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace slope {
 namespace {
@@ -67,6 +68,8 @@ __global__ void __launch_bounds__(kPruneThreads) prune24_kernel(const uint4* __r
                                                                 uint2* __restrict__ vals,
                                                                 uint8_t* __restrict__ meta,
                                                                 int64_t nchunks) {
+  grid_dependency_wait();
+  allow_dependents_launch();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
        base < nchunks; base += stride * kPruneUnroll) {
@@ -219,6 +222,8 @@ __global__ void __launch_bounds__(kDpThreads) double_prune24_kernel(
   __shared__ DpTables tab;
   fill_tables(tab);
   __syncthreads();
+  grid_dependency_wait();
+  allow_dependents_launch();
   const uint32_t n_h8 = static_cast<uint32_t>(rows / 8), n_c16 = static_cast<uint32_t>(cols / 16);
   const uint32_t tiles_h = (n_h8 + 31) / 32, tiles_c = (n_c16 + 7) / 8;
   const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -311,6 +316,8 @@ __global__ void __launch_bounds__(32 * CH) double_prune24_staged_kernel(
     if (th >= tiles_h) { th -= tiles_h; ++tc; }
   };
   uint32_t th = blockIdx.x % tiles_h, tc = blockIdx.x / tiles_h;
+  grid_dependency_wait();
+  allow_dependents_launch();
   if (tc < tiles_c) issue(th, tc, 0);
   cp_async_commit();
   int stage = 0;
@@ -353,9 +360,15 @@ cudaError_t launch_prune24(const void* W, int64_t rows, int64_t cols, void* vals
   int64_t blocks = (nchunks + per_block - 1) / per_block;
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
   if (blocks > cap) blocks = cap;
-  prune24_kernel<<<static_cast<unsigned>(blocks), kPruneThreads, 0, stream>>>(
-      static_cast<const uint4*>(W), static_cast<uint2*>(vals), meta, nchunks);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attrs[1];
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kPruneThreads);
+  cfg.stream = stream;
+  add_pdl_attr(cfg, attrs);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, prune24_kernel, static_cast<const uint4*>(W),
+                                     static_cast<uint2*>(vals), meta, nchunks);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 constexpr uint32_t kKeyShift = 1u << 17;  // the k17 argument of the A2 kernels
@@ -381,10 +394,16 @@ static cudaError_t run_staged(const void* vals, const uint8_t* meta, int64_t row
   const int64_t tiles = ((rows + 255) / 256) * (cols / (16 * CH));
   const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm;
   const int64_t blocks = tiles < cap ? tiles : cap;
-  kernel<<<static_cast<unsigned>(blocks), C::kThreads, C::kSmem, stream>>>(
-      static_cast<const uint8_t*>(vals), meta, static_cast<uint2*>(t_vals), t_meta, rows, cols,
-      kKeyShift);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attrs[1];
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = stream;
+  add_pdl_attr(cfg, attrs);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<const uint8_t*>(vals), meta,
+                                     static_cast<uint2*>(t_vals), t_meta, rows, cols, kKeyShift);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_double_prune24(const void* vals, const uint8_t* meta, int64_t rows,
@@ -404,10 +423,16 @@ cudaError_t launch_double_prune24(const void* vals, const uint8_t* meta, int64_t
   int64_t blocks = tiles;
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
   if (blocks > cap) blocks = cap;
-  double_prune24_kernel<<<static_cast<unsigned>(blocks), kDpThreads, 0, stream>>>(
-      static_cast<const uint4*>(vals), reinterpret_cast<const uint16_t*>(meta),
-      static_cast<uint2*>(t_vals), t_meta, rows, cols, kKeyShift);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attrs[1];
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kDpThreads);
+  cfg.stream = stream;
+  add_pdl_attr(cfg, attrs);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, double_prune24_kernel, static_cast<const uint4*>(vals),
+                                     reinterpret_cast<const uint16_t*>(meta),
+                                     static_cast<uint2*>(t_vals), t_meta, rows, cols, kKeyShift);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace slope

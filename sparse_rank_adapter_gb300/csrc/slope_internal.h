@@ -10,6 +10,17 @@
 
 namespace slope {
 
+// Appends the programmatic stream-serialization attribute (the kernel may
+// begin its set-up while the previous kernel on the stream finishes; every
+// kernel of this library waits for that kernel before touching global
+// memory) to a launch configuration whose attrs array has room for it.
+inline void add_pdl_attr(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attrs) {
+  attrs[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  ++cfg.numAttrs;
+}
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

@@ -17,6 +17,20 @@ enum : unsigned int { kStatusTimeout = 1u };
 // kernels never come near it.
 constexpr long long kWaitLimitCycles = 4LL << 30;
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream-serialization attribute may start while the previous kernel on the
+// stream is still running; grid_dependency_wait() blocks until that kernel
+// has completed and its memory is visible, so it must come before the first
+// global-memory access.  allow_dependents_launch() lets the next kernel's
+// CTAs be scheduled (they still wait in grid_dependency_wait() before
+// touching memory).  Both are no-ops in a kernel launched without it.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

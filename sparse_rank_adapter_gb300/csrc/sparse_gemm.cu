@@ -167,6 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  grid_dependency_wait();  // the previous kernel's outputs are visible from here
+  allow_dependents_launch();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -388,7 +390,7 @@ cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
@@ -459,6 +461,7 @@ cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
     grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
   }
   cfg.gridDim = dim3(grid);
+  add_pdl_attr(cfg, attr);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tA, tB, tMeta, tA2, tB2, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
