@@ -21,13 +21,15 @@
 // loads half of the shared B tile (the tokens) and multicasts it to both,
 // and a stage is refilled only after both CTAs' MMAs released it.
 //
-// Roles (448 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues
-// the MMAs (one thread), warps 2..5 drain the accumulator, and two groups of
-// four warps (6..9 for the even stages of the ring, 10..13 for the odd ones)
-// move each stage's 2:4 metadata from shared memory into TMEM, so the short
-// stages of narrow tiles do not wait on it.  The accumulator is
-// double-buffered in TMEM, so the epilogue of one tile overlaps the K-loop
-// of the next.  Every mbarrier wait is bounded.
+// Roles (576 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues
+// the MMAs (one thread), warps 2..5 and 14..17 drain the accumulator (two
+// warps per TMEM lane quadrant, alternate 32-column chunks, so that the
+// epilogue of a tile stays shorter than the K-loop of the next even for
+// short K), and two groups of four warps (6..9 for the even stages of the
+// ring, 10..13 for the odd ones) move each stage's 2:4 metadata from shared
+// memory into TMEM, so the short stages of narrow tiles do not wait on it.
+// The accumulator is double-buffered in TMEM, so the epilogue of one tile
+// overlaps the K-loop of the next.  Every mbarrier wait is bounded.
 //
 // Metadata in TMEM: k-step j (32 logical columns = 8 groups = one 32-bit
 // word per row) of stage s sits in its own column META_COL + 16 s + 4 j, so
@@ -54,7 +56,8 @@ constexpr int kBM = 128;               // weight rows per tile (MMA M)
 constexpr int kBKc = 64;               // compressed A columns per stage (= 128 logical K)
 constexpr int kA_BYTES = kBM * 128;    // 16 KB: 128 rows x 128 B (SW128)
 constexpr int kMETA_BYTES = kBM * 16;  // 2 KB: 128 rows x 16 B (32 groups)
-constexpr int kThreads = 448;
+constexpr int kThreads = 576;
+constexpr int kEpiWarps = 8;
 
 template <int BN>
 struct SpCfg {
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+      mbar_init(&acc_empty[b], kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -281,9 +284,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_commit(mma_done);
     }
-  } else if (warp < 6) {
+  } else if (warp < 6 || warp >= 14) {
     // ------------------------------------------------ epilogue -----------
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int half = warp >= 14 ? 1 : 0;  // which alternate column chunks
     int local = 0;
     for (int u = unit0; u < units; u += ustep, ++local) {
       const int buf = local & 1;
@@ -294,8 +298,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t trow = tmem + buf * C::ACC_COLS + (static_cast<uint32_t>(32 * q) << 16);
       constexpr int CH = BN < 32 ? BN : 32;
+      if (half * CH >= BN) {  // no chunk for this warp: release the buffer at once
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        continue;
+      }
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += CH) {
+      for (int c0 = half * CH; c0 < BN; c0 += 2 * CH) {
         uint32_t v[32];
         if constexpr (CH == 32) {
           tmem_ld_32x32b_x32(trow + c0, v);
@@ -308,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tmem_ld_wait();
-        if (c0 + CH >= BN) {  // last chunk read: hand the buffer back early
+        if (c0 + 2 * CH >= BN) {  // this warp's last chunk read: hand the buffer back early
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[buf]);
