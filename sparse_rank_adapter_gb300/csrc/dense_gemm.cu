@@ -20,6 +20,15 @@
 // Roles (192 threads): warp 0 TMA, warp 1 TMEM owner + MMA issuer, warps
 // 2..5 epilogue.  The accumulator is double-buffered in TMEM so a tile's
 // epilogue overlaps the next tile's K-loop.  Every mbarrier wait is bounded.
+//
+// The hi/lo store needs the whole sum before it rounds, so its split-K goes
+// through a thread-block cluster instead of atomics: the cluster's CTAs take
+// K ranges of the same tile; each peer writes its fp32 partial into its own
+// shared memory and arrives (release, cluster scope) on the leader's
+// barrier; the leader reads the partials over distributed shared memory,
+// adds them to its own, stores, and arrives back on each peer's barrier so
+// the peer may overwrite its partial with the next tile's.  This is what
+// gives a handful of token tiles (small T) more than one SM each.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -41,10 +50,15 @@ template <int BN>
 struct DnCfg {
   static constexpr int B_BYTES = BN * kBK * 2;
   static constexpr int STAGE = kA_BYTES + B_BYTES;
-  static constexpr int STAGES = (192 * 1024) / STAGE > 8 ? 8 : (192 * 1024) / STAGE;
+  // fp32 partial tile that a cluster peer hands to its leader when a narrow
+  // tile's K is split over a cluster (column-major: [BN][128])
+  static constexpr int RED_BYTES = BN <= 64 ? kBM * BN * 4 : 0;
+  static constexpr int STAGES_FIT = (192 * 1024 - RED_BYTES) / STAGE;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int ACC_COLS = BN < 32 ? 32 : BN;  // one accumulator buffer
   static constexpr int TMEM_COLS = 2 * ACC_COLS;       // double-buffered
-  static constexpr int SMEM = STAGES * STAGE + 1024 + 1024;
+  // stages | barriers (1 KB) | partial tile | alignment slack
+  static constexpr int SMEM = STAGES * STAGE + 1024 + RED_BYTES + 1024;
   // MN-major B: swizzle atom width in elements (64 for SW128) and its code.
   static constexpr int B_ATOM = BN >= 64 ? 64 : BN;
   static constexpr uint32_t B_SWZ = BN >= 64 ? kSwizzle128 : BN == 32 ? kSwizzle64 : kSwizzle32;
@@ -61,6 +75,7 @@ struct DnParams {
   const uint8_t* meta;  // masked dW: metadata, N/8 bytes per row
   int dense_dw, accumulate, atomic_out;
   int lo_off, fold;
+  int csplit;  // CTAs of a cluster that split one tile's K (hi/lo store only); 1 = none
   unsigned int* status;
 };
 
@@ -182,18 +197,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = empty + C::STAGES;  // [2]
   uint64_t* acc_empty = acc_full + 2;      // [2]
   uint64_t* mma_done = acc_empty + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* red_full = mma_done + 1;   // leader: every peer's partial is in place
+  uint64_t* red_empty = red_full + 1;  // peer: the leader has read this CTA's partial
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(red_empty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  float* red = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE + 1024);
 
   const int warp = warp_id(), lane = lane_id();
+  const int cs = p.csplit;
+  const uint32_t crank = cs > 1 ? cluster_ctarank() : 0u;
   const int tiles_mn = p.tiles_m * p.tiles_n;
   const int units = p.num_tiles;
-  const int unit0 = static_cast<int>(blockIdx.x);
-  const int ustep = static_cast<int>(gridDim.x);
-  // unit -> (tile m0, n0, split z)
+  const int unit0 = static_cast<int>(cs > 1 ? blockIdx.x / cs : blockIdx.x);
+  const int ustep = static_cast<int>(cs > 1 ? gridDim.x / cs : gridDim.x);
+  // unit -> (tile m0, n0, split z); in a cluster the split is the CTA's rank
   auto decode = [&](int u, int& m0, int& n0, int& z) {
     const int mn = u % tiles_mn;
-    z = u / tiles_mn;
+    z = cs > 1 ? static_cast<int>(crank) : u / tiles_mn;
     m0 = (mn % p.tiles_m) * kBM;
     n0 = (mn / p.tiles_m) * BN;
   };
@@ -208,6 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
     }
     mbar_init(mma_done, 1);
+    mbar_init(red_full, 4 * (cs > 1 ? cs - 1 : 1));  // four epilogue warps per peer
+    mbar_init(red_empty, 4);                         // the leader's four epilogue warps
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -216,7 +238,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if (cs > 1)
+    cluster_sync();  // the peers' barriers exist before anyone arrives on them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   grid_dependency_wait();  // the previous kernel's outputs are visible from here
@@ -312,6 +337,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       if (!mbar_wait(&acc_full[buf], use & 1, abort_flag, p.status)) break;
       tc_fence_after();
+      // cluster split-K: a peer first waits until the leader has read its
+      // previous partial; the leader waits until every peer's is in place
+      const bool peer = cs > 1 && crank != 0, leader = cs > 1 && crank == 0;
+      if (peer && !mbar_wait_cluster(red_empty, (local & 1) ^ 1, abort_flag, p.status)) break;
+      if (leader && !mbar_wait_cluster(red_full, local & 1, abort_flag, p.status)) break;
       const uint32_t trow = tmem + buf * C::ACC_COLS + (static_cast<uint32_t>(32 * q) << 16);
       constexpr int CH = BN < 32 ? BN : 32;
       uint4 mrow[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
@@ -341,8 +371,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[buf]);
         }
+        if constexpr (C::RED_BYTES > 0) {
+          const int row = 32 * q + lane;
+          if (peer) {  // hand the partial over; the leader stores
+#pragma unroll
+            for (int j = 0; j < CH; ++j) red[(c0 + j) * kBM + row] = __uint_as_float(v[j]);
+            continue;
+          }
+          if (leader) {
+            for (int pr = 1; pr < cs; ++pr) {
+              const uint32_t base = mapa_shared(smem_u32(red), static_cast<uint32_t>(pr));
+#pragma unroll
+              for (int j = 0; j < CH; ++j)
+                v[j] = __float_as_uint(__uint_as_float(v[j]) +
+                                       ld_shared_cluster_f32(base + 4u * ((c0 + j) * kBM + row)));
+            }
+          }
+        }
         if (m >= p.M) continue;
         epilogue_chunk<BN, CH, EPI>(p, v, m, n0, c0, mrow);
+      }
+      if (cs > 1) {
+        // peer: the partial is written; leader: the peers' partials are read
+        asm volatile("fence.acq_rel.cluster;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          if (peer) {
+            mbar_arrive_cluster(mapa_shared(smem_u32(red_full), 0u));
+          } else {
+            for (int pr = 1; pr < cs; ++pr)
+              mbar_arrive_cluster(mapa_shared(smem_u32(red_empty), static_cast<uint32_t>(pr)));
+          }
+        }
       }
     }
   }
@@ -355,6 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(mma_done, 0, &no_abort, p.status);
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+  // No CTA leaves while the leader may still read its partial or arrive on
+  // its barrier.
+  if (cs > 1) cluster_sync();
 }
 
 // ---------------------------------------------------------------------------
@@ -582,6 +645,7 @@ cudaError_t run_dw_pair(const DenseGemmArgs& a, cudaStream_t stream) {
   splits = (num_kb + kbs - 1) / kbs;
 
   DnParams p = {};
+  p.csplit = 1;
   p.M = static_cast<int>(M); p.N = static_cast<int>(N); p.K = static_cast<int>(K);
   p.kb_per_split = kbs; p.num_kb = num_kb;
   p.tiles_m = tiles_m; p.tiles_n = tiles_n;
@@ -643,9 +707,22 @@ cudaError_t run(const DenseGemmArgs& a, cudaStream_t stream) {
   const int tiles_n = static_cast<int>((N + BN - 1) / BN);
   int splits = a.splits;
   if (splits <= 0) splits = choose_splits(tiles_m * tiles_n, sm_count(), num_kb);
-  if (EPI == DenseEpi::StoreBf16HiLo) splits = 1;
-  const int kbs = (num_kb + splits - 1) / splits;
-  splits = (num_kb + kbs - 1) / kbs;  // every split owns >= 1 K-block
+  int csplit = 1;
+  if (EPI == DenseEpi::StoreBf16HiLo) {
+    // no atomic split for the rounding store; when the tiles leave SMs
+    // idle, split K over a cluster of up to 8 CTAs (>= 4 K-blocks each)
+    splits = 1;
+    const int tiles = tiles_m * tiles_n;
+    int want = sm_count() / tiles;
+    want = want < 8 ? want : 8;
+    want = want < num_kb / 4 ? want : num_kb / 4;
+    if (C::RED_BYTES > 0 && want >= 2) {
+      const int kbs = (num_kb + want - 1) / want;
+      csplit = (num_kb + kbs - 1) / kbs;  // every CTA of the cluster owns >= 1 K-block
+    }
+  }
+  const int kbs = csplit > 1 ? (num_kb + csplit - 1) / csplit : (num_kb + splits - 1) / splits;
+  splits = csplit > 1 ? 1 : (num_kb + kbs - 1) / kbs;  // every split owns >= 1 K-block
 
   DnParams p;
   p.M = static_cast<int>(M); p.N = static_cast<int>(N); p.K = static_cast<int>(K);
@@ -656,6 +733,7 @@ cudaError_t run(const DenseGemmArgs& a, cudaStream_t stream) {
   p.atomic_out = 0;
   p.lo_off = a.lo_off;
   p.fold = a.fold;
+  p.csplit = csplit;
   if (EPI == DenseEpi::MaskedWeightGrad && splits > 1) {
     p.atomic_out = 1;
     if (!a.accumulate) {
@@ -667,13 +745,23 @@ cudaError_t run(const DenseGemmArgs& a, cudaStream_t stream) {
   if (!p.status) return cudaErrorInvalidDevicePointer;
   p.tiles_m = tiles_m; p.tiles_n = tiles_n;
   p.num_tiles = tiles_m * tiles_n * splits;
-  const int grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
+  // with a cluster split, one cluster per tile (tiles * csplit <= SMs)
+  const int grid = csplit > 1 ? p.num_tiles * csplit
+                              : (p.num_tiles < sm_count() ? p.num_tiles : sm_count());
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
+  if (csplit > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(csplit);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
   add_pdl_attr(cfg, attr);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tA, tB, p);
   return e != cudaSuccess ? e : cudaGetLastError();
