@@ -63,14 +63,17 @@ template <int BN>
 struct SpCfg {
   static constexpr int B_BYTES = BN * 256;  // two 64-column SW128 atoms of BN rows
   static constexpr int STAGE = kA_BYTES + B_BYTES + kMETA_BYTES;
-  static constexpr int STAGES_FIT = (200 * 1024) / STAGE;
+  // fp32 partial tile a cluster peer hands to its leader when a narrow tile's
+  // K is split over a cluster (column-major: [BN][128])
+  static constexpr int RED_BYTES = BN <= 64 ? kBM * BN * 4 : 0;
+  static constexpr int STAGES_FIT = (200 * 1024 - RED_BYTES) / STAGE;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int ACC_COLS = BN < 32 ? 32 : BN;  // one accumulator buffer
   static constexpr int META_COL = 2 * ACC_COLS;        // after the two buffers
   static constexpr int TMEM_NEED = META_COL + 16 * STAGES;
   static constexpr int TMEM_COLS =
       TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
-  static constexpr int SMEM = STAGES * STAGE + 1024 /*barriers*/ + 1024 /*align slack*/;
+  static constexpr int SMEM = STAGES * STAGE + 1024 /*barriers*/ + RED_BYTES + 1024 /*align slack*/;
   static_assert(STAGE % 1024 == 0, "stage must keep 1024-byte alignment");
   static_assert(TMEM_NEED <= 512, "TMEM budget");
   static_assert(STAGES >= 2, "pipeline depth");
@@ -90,6 +93,8 @@ struct SpParams {
   int num_kb;      // sparse K-blocks (K / 128)
   int num_ab;      // adapter blocks per part (ceil(r / 64)); parts: hi, lo
   int out_bf16;
+  int csplit;        // CTAs of a cluster that split one tile's K (not with PAIR); 1 = none
+  int kb_per_split;  // sparse K-blocks per CTA of such a cluster
   void* out;
   unsigned int* status;
 };
@@ -111,16 +116,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = meta_full + C::STAGES;  // [2]
   uint64_t* acc_empty = acc_full + 2;          // [2]
   uint64_t* mma_done = acc_empty + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* red_full = mma_done + 1;   // split leader: every peer's partial is in place
+  uint64_t* red_empty = red_full + 1;  // split peer: the leader has read this CTA's partial
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(red_empty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  float* red = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE + 1024);
 
   const int warp = warp_id(), lane = lane_id();
-  const int per_tile = p.num_kb + 2 * p.num_ab;
+  // Cluster split of K (narrow tiles, never with PAIR): CTA `crank` of the
+  // cluster takes sparse K-blocks [crank * kb_per_split, ...); the last one
+  // also runs the adapter steps.  Its fp32 partial goes to the leader.
+  const int cs = PAIR ? 1 : p.csplit;
+  const uint32_t crank = cs > 1 ? cluster_ctarank() : 0u;
+  const int kb0 = cs > 1 ? static_cast<int>(crank) * p.kb_per_split : 0;
+  const int nsp = cs > 1 ? min(p.num_kb - kb0, p.kb_per_split) : p.num_kb;
+  const int nad = (cs == 1 || static_cast<int>(crank) == cs - 1) ? 2 * p.num_ab : 0;
+  const int per_tile = nsp + nad;
+  // step kk of a tile -> K-block index: sparse blocks kb0.., then the adapter
+  // blocks, numbered from num_kb as in the unsplit tile
+  auto kblock = [&](int kk) { return kk < nsp ? kb0 + kk : p.num_kb + (kk - nsp); };
   // Work units: tiles, or (with PAIR) pairs of M-adjacent tiles per cluster.
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   const int units = PAIR ? p.num_tiles / 2 : p.num_tiles;
-  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int ustep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1)
+                         : static_cast<int>(cs > 1 ? blockIdx.x / cs : blockIdx.x);
+  const int ustep = PAIR ? static_cast<int>(gridDim.x >> 1)
+                         : static_cast<int>(cs > 1 ? gridDim.x / cs : gridDim.x);
   // Raster order: bands of group_m M tiles (pairs with PAIR); within a band
   // the M tiles turn fastest, then the N tiles, so the band's weight tiles
   // stay in L2 while every token tile passes over them once.
@@ -156,6 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acc_empty[b], kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(mma_done, 1);
+    mbar_init(red_full, kEpiWarps * (cs > 1 ? cs - 1 : 1));  // every epilogue warp of each peer
+    mbar_init(red_empty, kEpiWarps);                         // the leader's epilogue warps
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -164,8 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  if (PAIR)
-    cluster_sync();  // the peer's barriers exist before any multicast reaches them
+  if (PAIR || cs > 1)
+    cluster_sync();  // the peer's barriers exist before any multicast or arrival reaches them
   else
     __syncthreads();
   tc_fence_after();
@@ -184,7 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = unit0; u < units && !stop; u += ustep) {
         const int m0 = tile_m0(u);
         const int n0 = tile_n0(u);
-        for (int kb = 0; kb < per_tile; ++kb, ++it) {
+        for (int kk = 0; kk < per_tile; ++kk, ++it) {
+          const int kb = kblock(kk);
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
           if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.status)) { stop = true; break; }
@@ -246,7 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * C::ACC_COLS;
-        for (int kb = 0; kb < per_tile; ++kb, ++it) {
+        for (int kk = 0; kk < per_tile; ++kk, ++it) {
+          const int kb = kblock(kk);
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
           // meta_full[s] completes once per fill of stage s (metadata or not),
@@ -263,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t da = smem_desc(aA + j * 32, 0, 1024, kSwizzle128);
               const uint64_t db = smem_desc(aB + (j >> 1) * (BN * 128) + (j & 1) * 64, 0, 1024,
                                             kSwizzle128);
-              mma_sp_bf16_ss(d, da, db, tmeta + 4 * j, id_sp, (kb > 0 || j > 0) ? 1u : 0u);
+              mma_sp_bf16_ss(d, da, db, tmeta + 4 * j, id_sp, (kk > 0 || j > 0) ? 1u : 0u);
             }
           } else {
             const int c = (kb - p.num_kb) % p.num_ab;
@@ -296,13 +321,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n0 = tile_n0(u);
       if (!mbar_wait(&acc_full[buf], use & 1, abort_flag, p.status)) break;
       tc_fence_after();
+      // cluster split of K: a peer first waits until the leader has read its
+      // previous partial; the leader waits until every peer's is in place
+      const bool peer = cs > 1 && crank != 0, leader = cs > 1 && crank == 0;
+      if (peer && !mbar_wait_cluster(red_empty, (local & 1) ^ 1, abort_flag, p.status)) break;
+      if (leader && !mbar_wait_cluster(red_full, local & 1, abort_flag, p.status)) break;
       const uint32_t trow = tmem + buf * C::ACC_COLS + (static_cast<uint32_t>(32 * q) << 16);
       constexpr int CH = BN < 32 ? BN : 32;
       if (half * CH >= BN) {  // no chunk for this warp: release the buffer at once
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
-        continue;
       }
 #pragma unroll 1
       for (int c0 = half * CH; c0 < BN; c0 += 2 * CH) {
@@ -323,6 +352,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[buf]);
         }
+        if constexpr (C::RED_BYTES > 0) {
+          const int row = 32 * q + lane;
+          if (peer) {  // hand the partial over; the leader stores
+#pragma unroll
+            for (int j = 0; j < CH; ++j) red[(c0 + j) * kBM + row] = __uint_as_float(v[j]);
+            continue;
+          }
+          if (leader) {
+            for (int pr = 1; pr < cs; ++pr) {
+              const uint32_t base = mapa_shared(smem_u32(red), static_cast<uint32_t>(pr));
+#pragma unroll
+              for (int j = 0; j < CH; ++j)
+                v[j] = __float_as_uint(__uint_as_float(v[j]) +
+                                       ld_shared_cluster_f32(base + 4u * ((c0 + j) * kBM + row)));
+            }
+          }
+        }
         const int nlim = p.N - (n0 + c0);
         if (p.out_bf16) {
           __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(n0 + c0) * p.M + m;
@@ -334,6 +380,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < CH; ++j)
             if (j < nlim) o[static_cast<size_t>(j) * p.M] = __uint_as_float(v[j]);
+        }
+      }
+      if (cs > 1) {
+        // peer: the partial is written; leader: the peers' partials are read
+        asm volatile("fence.acq_rel.cluster;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          if (peer) {
+            mbar_arrive_cluster(mapa_shared(smem_u32(red_full), 0u));
+          } else {
+            for (int pr = 1; pr < cs; ++pr)
+              mbar_arrive_cluster(mapa_shared(smem_u32(red_empty), static_cast<uint32_t>(pr)));
+          }
         }
       }
     }
@@ -354,7 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     bool stop = false;
     for (int u = unit0; u < units && !stop; u += ustep) {
-      for (int kb = 0; kb < per_tile; ++kb, ++it) {
+      for (int kk = 0; kk < per_tile; ++kk, ++it) {
+        const int kb = kblock(kk);
         const int s = it % C::STAGES;
         if ((s & 1) != group) continue;
         const uint32_t ph = (it / C::STAGES) & 1;
@@ -385,9 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(mma_done, 0, &no_abort, p.status);
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
-  // No CTA leaves while its peer may still multicast into it or arrive on
-  // its barriers.
-  if (PAIR) cluster_sync();
+  // No CTA leaves while its peer may still multicast into it, read its
+  // partial or arrive on its barriers.
+  if (PAIR || cs > 1) cluster_sync();
 }
 
 template <int BN, bool A2_MN, bool PAIR>
@@ -459,6 +519,19 @@ cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
     p.group_m = g < 1 ? 1 : (g > rows ? rows : g);
   }
   p.out_bf16 = a.out_bf16 ? 1 : 0;
+  // Narrow tiles that leave SMs idle split K over a cluster of up to 8 CTAs
+  // (>= 4 sparse K-blocks each); the partials meet in the leader's registers.
+  p.csplit = 1;
+  p.kb_per_split = p.num_kb;
+  if (!PAIR && C::RED_BYTES > 0) {
+    int want = sm_count() / p.num_tiles;
+    want = want < 8 ? want : 8;
+    want = want < p.num_kb / 4 ? want : p.num_kb / 4;
+    if (want >= 2) {
+      p.kb_per_split = (p.num_kb + want - 1) / want;
+      p.csplit = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;  // each CTA >= 1 block
+    }
+  }
   p.out = a.out;
   p.status = device_status_ptr();
   if (!p.status) return cudaErrorInvalidDevicePointer;
@@ -468,7 +541,16 @@ cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
     const int clusters = units < max_clusters[dev].load() ? units : max_clusters[dev].load();
     grid = 2 * clusters;
   } else {
-    grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
+    grid = p.csplit > 1 ? p.num_tiles * p.csplit  // one cluster per tile
+                        : (p.num_tiles < sm_count() ? p.num_tiles : sm_count());
+    if (p.csplit > 1) {
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(p.csplit);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+    }
   }
   cfg.gridDim = dim3(grid);
   add_pdl_attr(cfg, attr);
