@@ -559,8 +559,10 @@ cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-// N tile by token count: the smallest tile that covers small batches; for
-// large ones 192 (the widest that still double-buffers in TMEM beside the
+// N tile by token count: the smallest tile that covers small batches (up to
+// 128 tokens, 64-wide tiles while the weight has fewer 128-row tiles than
+// there are SMs, so that its stream spreads over more of them); for large
+// batches 192 (the widest that still double-buffers in TMEM beside the
 // metadata) unless 128 gives the grid noticeably more tiles per SM.
 template <bool A2_MN>
 cudaError_t dispatch(const SparseGemmArgs& a, cudaStream_t stream) {
@@ -568,6 +570,7 @@ cudaError_t dispatch(const SparseGemmArgs& a, cudaStream_t stream) {
   if (a.N <= 64) return run<64, A2_MN, false>(a, stream);
   const int64_t tiles_m = a.M / kBM;
   const bool pair = tiles_m % 2 == 0;  // clusters pair M-adjacent tiles
+  if (a.N <= 128 && tiles_m < sm_count()) return run<64, A2_MN, false>(a, stream);
   if (a.N <= 128)
     return pair ? run<128, A2_MN, true>(a, stream) : run<128, A2_MN, false>(a, stream);
   const int64_t t192 = tiles_m * ((a.N + 191) / 192);
