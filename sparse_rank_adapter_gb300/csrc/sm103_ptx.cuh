@@ -176,6 +176,15 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
   return v;
 }
 
+// Arrive, without release semantics, on a barrier of any CTA of the cluster:
+// for a signal that orders no generic-memory writes (e.g. TMEM stores that
+// tcgen05.wait::st has already completed), it skips the cluster-scope
+// release fence.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
 // Arrive on a barrier of any CTA of the cluster (shared::cluster address).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)

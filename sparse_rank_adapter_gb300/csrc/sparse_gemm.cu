@@ -559,6 +559,382 @@ cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Sparse GEMM on CTA pairs: the pair-wide sparse MMA (M = 256 = two 128-row
+// weight tiles, one per CTA; N = BN tokens, of which each CTA holds half)
+// halves the token bytes each SM takes in per flop, which is what bounds the
+// one-CTA kernel at large sizes.  The even CTA issues the MMAs and owns the
+// full barriers that both CTAs' operand loads signal.  Each CTA loads its own
+// rows' metadata on a barrier of its own; its metadata warps copy them into
+// its own TMEM (the pair MMA reads each CTA's metadata at the same column)
+// and then arrive on the even CTA's meta_full.  The even CTA's commits
+// release stages and accumulators in both CTAs; both CTAs' epilogue warps
+// hand accumulator buffers back to the even CTA.
+// ---------------------------------------------------------------------------
+
+template <int BN>
+struct Sp2Cfg {
+  static constexpr int HB = BN / 2;              // token rows each CTA holds
+  static constexpr int B_BYTES = HB * 256;       // two 64-column SW128 atoms of HB rows
+  static constexpr int STAGE = kA_BYTES + B_BYTES + kMETA_BYTES;
+  static constexpr int STAGES_FIT = (212 * 1024) / STAGE;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int ACC_COLS = BN;
+  static constexpr int META_COL = 2 * ACC_COLS;
+  static constexpr int TMEM_NEED = META_COL + 16 * STAGES;
+  static constexpr int TMEM_COLS = TMEM_NEED <= 256 ? 256 : 512;
+  static constexpr int SMEM = STAGES * STAGE + 1024 /*barriers*/ + 1024 /*align slack*/;
+  static_assert(STAGE % 1024 == 0 && (HB * 128) % 1024 == 0, "1024-byte aligned atoms");
+  static_assert(TMEM_NEED <= 512, "TMEM budget");
+  static_assert(STAGES >= 2, "pipeline depth");
+};
+
+// 26 warps: the 18 roles of the one-CTA kernel plus two more groups of four
+// metadata warps (warps 18..25), so that four stages' metadata move into
+// TMEM at once (stage s goes to group s % 4).
+constexpr int kThreadsPair = 832;
+
+template <int BN, bool A2_MN>
+__global__ void __launch_bounds__(kThreadsPair, 1)
+    sparse_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmMeta,
+                       const __grid_constant__ CUtensorMap tmA2,
+                       const __grid_constant__ CUtensorMap tmB2, const SpParams p) {
+  using C = Sp2Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);  // even CTA's
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* meta_ready = empty + C::STAGES;     // this CTA's metadata tile landed
+  uint64_t* meta_full = meta_ready + C::STAGES; // even CTA's: both CTAs' metadata in TMEM
+  uint64_t* acc_full = meta_full + C::STAGES;   // [2]
+  uint64_t* acc_empty = acc_full + 2;           // [2], counted in the even CTA
+  uint64_t* mma_done = acc_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  const uint32_t rank = cluster_ctarank();
+  const int per_tile = p.num_kb + 2 * p.num_ab;
+  const int units = p.num_tiles / 2;  // pairs of M-adjacent tiles x token tiles
+  const int unit0 = static_cast<int>(blockIdx.x >> 1);
+  const int ustep = static_cast<int>(gridDim.x >> 1);
+  // Raster order as in the one-CTA kernel: bands of group_m M pairs, the M
+  // pairs turning fastest within a band.
+  const int rows_m = p.tiles_m / 2;
+  const int tiles_n = units / rows_m;
+  auto decode = [&](int u, int& m0, int& n0) {
+    const int per_band = p.group_m * tiles_n;
+    const int b = u / per_band, w = u % per_band;
+    const int first = b * p.group_m;
+    const int gm = min(p.group_m, rows_m - first);
+    m0 = (2 * (first + w % gm) + static_cast<int>(rank)) * kBM;  // this CTA's 128 weight rows
+    n0 = (w / gm) * BN;                                           // the pair's token tile
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&meta_ready[s], 1);
+      mbar_init(&meta_full[s], 8);  // four metadata warps in each CTA
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 2 * kEpiWarps);  // the epilogue warps of both CTAs
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_holder, C::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  if (warp >= 6 && warp < 10) {
+    // Every metadata column starts with a legal pattern (each group keeps
+    // positions 0 and 1), so no MMA can ever meet an unwritten one.
+    const uint32_t tq = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + C::META_COL;
+    const uint32_t legal[4] = {0x44444444u, 0x44444444u, 0x44444444u, 0x44444444u};
+    for (int c = 0; c < 16 * C::STAGES; c += 4) tmem_st_32x32b_x4(tq + c, legal);
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  cluster_sync();  // every barrier of both CTAs exists before anything reaches it
+  tc_fence_after();
+  grid_dependency_wait();  // the previous kernel's outputs are visible from here
+  allow_dependents_launch();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------- TMA producer -------
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      tma_prefetch_desc(&tmMeta);
+      int it = 0;
+      bool stop = false;
+      for (int u = unit0; u < units && !stop; u += ustep) {
+        int m0, n0;
+        decode(u, m0, n0);
+        const int nb = n0 + static_cast<int>(rank) * C::HB;  // this CTA's half of the tokens
+        for (int kb = 0; kb < per_tile; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.status)) { stop = true; break; }
+          uint8_t* sA = smem + s * C::STAGE;
+          uint8_t* sB = sA + kA_BYTES;
+          uint8_t* sMeta = sB + C::B_BYTES;
+          const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);  // the even CTA's barrier
+          if (kb < p.num_kb) {
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (kA_BYTES + C::B_BYTES));
+            tma_load_2d_pair(sA, &tmA, bar, kb * kBKc, m0);
+            tma_load_2d_pair(sB, &tmB, bar, kb * 128, nb);
+            tma_load_2d_pair(sB + C::HB * 128, &tmB, bar, kb * 128 + 64, nb);
+            mbar_arrive_expect_tx(&meta_ready[s], kMETA_BYTES);
+            tma_load_2d(sMeta, &tmMeta, &meta_ready[s], kb * 16, m0);
+          } else {
+            // adapter block c of part `part` (0 = hi, 1 = lo), as in the
+            // one-CTA kernel; each CTA brings its rows of A2 and its half of B2
+            const int a = kb - p.num_kb;
+            const int part = a / p.num_ab, c = a % p.num_ab;
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (kA_BYTES + C::HB * 128));
+            if (A2_MN) {
+              tma_load_2d_pair(sA, &tmA2, bar, m0, c * 64);
+              tma_load_2d_pair(sA + 8192, &tmA2, bar, m0 + 64, c * 64);
+            } else {
+              tma_load_2d_pair(sA, &tmA2, bar, c * 64, m0);
+            }
+            tma_load_2d_pair(sB, &tmB2, bar, part * p.r + c * 64, nb);
+            mbar_arrive(&meta_ready[s]);  // no metadata in this stage
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------------------------------------- MMA issuer ---------
+      const uint32_t id_sp = idesc_bf16(2 * kBM, BN, false, false, true);
+      const uint32_t id_ad = idesc_bf16(2 * kBM, BN, A2_MN, false, false);
+      const int r16 = (p.r + 15) / 16;
+      int it = 0, local = 0;
+      bool stop = false;
+      for (int u = unit0; u < units && !stop; u += ustep, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * C::ACC_COLS;
+        for (int kb = 0; kb < per_tile; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1;
+          if (!mbar_wait(&full[s], ph, abort_flag, p.status)) { stop = true; break; }
+          // both CTAs' metadata of this fill is in TMEM (the odd CTA's
+          // warps arrive with release at cluster scope)
+          if (!mbar_wait_cluster(&meta_full[s], ph, abort_flag, p.status)) { stop = true; break; }
+          tc_fence_after();
+          const uint32_t aA = smem_u32(smem + s * C::STAGE);
+          const uint32_t aB = aA + kA_BYTES;
+          if (kb < p.num_kb) {
+            const uint32_t tmeta = tmem + C::META_COL + 16 * s;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {  // 4 x (K = 32 logical)
+              const uint64_t da = smem_desc(aA + j * 32, 0, 1024, kSwizzle128);
+              const uint64_t db = smem_desc(aB + (j >> 1) * (C::HB * 128) + (j & 1) * 64, 0, 1024,
+                                            kSwizzle128);
+              mma_sp_bf16_ss_pair(d, da, db, tmeta + 4 * j, id_sp, (kb > 0 || j > 0) ? 1u : 0u);
+            }
+          } else {
+            const int c = (kb - p.num_kb) % p.num_ab;
+            const int steps = min(4, r16 - 4 * c);
+            for (int j = 0; j < steps; ++j) {
+              const uint64_t da = A2_MN ? smem_desc(aA + j * 2048, 8192, 1024, kSwizzle128)
+                                        : smem_desc(aA + j * 32, 0, 1024, kSwizzle128);
+              const uint64_t db = smem_desc(aB + j * 32, 0, 1024, kSwizzle128);
+              mma_bf16_ss_pair(d, da, db, id_ad, 1u);
+            }
+          }
+          mma_commit_pair_mc(&empty[s], 3);  // release the stage in both CTAs
+        }
+        if (!stop) mma_commit_pair_mc(&acc_full[buf], 3);
+      }
+      mma_commit_pair_mc(mma_done, 3);
+    }
+  } else if (warp < 6 || (warp >= 14 && warp < 18)) {
+    // ------------------------------------------------ epilogue -----------
+    const int q = warp & 3;
+    const int half = warp >= 14 ? 1 : 0;
+    const uint32_t acc_empty0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
+    int local = 0;
+    for (int u = unit0; u < units; u += ustep, ++local) {
+      int m0, n0;
+      decode(u, m0, n0);
+      const int buf = local & 1;
+      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      const int m = m0 + 32 * q + lane;
+      if (!mbar_wait(&acc_full[buf], use & 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t trow = tmem + buf * C::ACC_COLS + (static_cast<uint32_t>(32 * q) << 16);
+#pragma unroll 1
+      for (int c0 = 32 * half; c0 < BN; c0 += 64) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(trow + c0, v);
+        tmem_ld_wait();
+        if (c0 + 64 >= BN) {  // this warp's last chunk read: hand the buffer back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8 * buf);
+        }
+        const int nlim = p.N - (n0 + c0);
+        if (p.out_bf16) {
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(n0 + c0) * p.M + m;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nlim) o[static_cast<size_t>(j) * p.M] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        } else {
+          float* o = static_cast<float*>(p.out) + static_cast<size_t>(n0 + c0) * p.M + m;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nlim) o[static_cast<size_t>(j) * p.M] = __uint_as_float(v[j]);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------ metadata -> TMEM ---
+    // As in the one-CTA kernel, on this CTA's own metadata and TMEM, with
+    // four groups taking the stages by s % 4 (each group takes every fill
+    // of its stages in order); the arrival goes to the even CTA's meta_full.
+    const int q = warp & 3;
+    const int group = warp < 14 ? (warp - 6) >> 2 : 2 + ((warp - 18) >> 2);
+    const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::META_COL;
+    const uint32_t meta_full0 = mapa_shared(smem_u32(&meta_full[0]), 0);
+    int it = 0;
+    bool stop = false;
+    for (int u = unit0; u < units && !stop; u += ustep) {
+      for (int kb = 0; kb < per_tile; ++kb, ++it) {
+        const int s = it % C::STAGES;
+        if ((s & 3) != group) continue;
+        const uint32_t ph = (it / C::STAGES) & 1;
+        if (!mbar_wait(&meta_ready[s], ph, abort_flag, p.status)) { stop = true; break; }
+        if (kb < p.num_kb) {
+          const uint4 w = *reinterpret_cast<const uint4*>(smem + s * C::STAGE + kA_BYTES +
+                                                          C::B_BYTES + 16 * (32 * q + lane));
+          const uint32_t col = tq + 16 * s;
+          tmem_st_32x32b_x1(col + 0, pair_rows(w.x, lane));
+          tmem_st_32x32b_x1(col + 4, pair_rows(w.y, lane));
+          tmem_st_32x32b_x1(col + 8, pair_rows(w.z, lane));
+          tmem_st_32x32b_x1(col + 12, pair_rows(w.w, lane));
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          // the stores are complete (tcgen05.wait::st); the signal orders no
+          // generic-memory writes, so the odd CTA arrives without a release
+          if (rank == 0)
+            mbar_arrive(&meta_full[s]);
+          else
+            mbar_arrive_cluster_relaxed(meta_full0 + 8 * s);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    volatile int no_abort = 0;
+    mbar_wait(mma_done, 0, &no_abort, p.status);
+    tmem_dealloc_pair(tmem, C::TMEM_COLS);
+  }
+  cluster_sync();  // no CTA leaves while its peer may still signal it or read its TMEM
+}
+
+template <int BN, bool A2_MN>
+cudaError_t run_pair2(const SparseGemmArgs& a, cudaStream_t stream) {
+  using C = Sp2Cfg<BN>;
+  auto kernel = sparse_pair_kernel<BN, A2_MN>;
+  static std::atomic<int> attr_set[64];
+  static std::atomic<int> max_clusters[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(kThreadsPair);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  if (!attr_set[dev].load()) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    cfg.gridDim = dim3(2 * (sm_count() / 2));
+    e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    max_clusters[dev].store(n > 0 ? n : 1);
+    attr_set[dev].store(1);
+  }
+  CUtensorMap tA, tB, tMeta, tA2, tB2;
+  const uint64_t M = a.M, N = a.N, K = a.K, r = a.r;
+  const uint32_t b_rows = BN / 2;  // rows of B one CTA's TMA box brings
+  bool ok = make_tmap_2d(&tA, a.a_vals, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K / 2, M, K, 64, kBM,
+                         Swz::B128) &&
+            make_tmap_2d(&tB, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, 2 * K, 64, b_rows,
+                         Swz::B128) &&
+            make_tmap_2d(&tMeta, a.a_meta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 8, M, K / 8, 16,
+                         kBM, Swz::None);
+  if (r > 0) {
+    ok = ok && (A2_MN ? make_tmap_2d(&tA2, a.a2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, r, 2 * M,
+                                     64, 64, Swz::B128)
+                      : make_tmap_2d(&tA2, a.a2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, r, M, 2 * r,
+                                     64, kBM, Swz::B128));
+    ok = ok && make_tmap_2d(&tB2, a.b2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2 * r, N, 4 * r, 64,
+                            b_rows, Swz::B128);
+  } else {
+    tA2 = tA;  // unused
+    tB2 = tB;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  SpParams p = {};
+  p.M = static_cast<int>(M); p.N = static_cast<int>(N); p.K = static_cast<int>(K);
+  p.r = static_cast<int>(r);
+  p.tiles_m = static_cast<int>(M / kBM);  // even
+  p.num_tiles = p.tiles_m * static_cast<int>((N + BN - 1) / BN);
+  p.num_kb = static_cast<int>(K / 128);
+  p.num_ab = static_cast<int>((r + 63) / 64);
+  {  // a band of weight-tile pairs (values + metadata, all of K) of about 40 MB
+    const double tile_bytes = 2.0 * kBM * K * 1.125;
+    int g = static_cast<int>(40.0e6 / tile_bytes);
+    const int rows = p.tiles_m / 2;
+    p.group_m = g < 1 ? 1 : (g > rows ? rows : g);
+  }
+  p.out_bf16 = a.out_bf16 ? 1 : 0;
+  p.csplit = 1;
+  p.kb_per_split = p.num_kb;
+  p.out = a.out;
+  p.status = device_status_ptr();
+  if (!p.status) return cudaErrorInvalidDevicePointer;
+  const int units = p.num_tiles / 2;
+  const int clusters = units < max_clusters[dev].load() ? units : max_clusters[dev].load();
+  cfg.gridDim = dim3(2 * clusters);
+  add_pdl_attr(cfg, attr);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tA, tB, tMeta, tA2, tB2, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 // N tile by token count: the smallest tile that covers small batches (up to
 // 128 tokens, 64-wide tiles while the weight has fewer 128-row tiles than
 // there are SMs, so that its stream spreads over more of them); for large
@@ -572,11 +948,11 @@ cudaError_t dispatch(const SparseGemmArgs& a, cudaStream_t stream) {
   const bool pair = tiles_m % 2 == 0;  // clusters pair M-adjacent tiles
   if (a.N <= 128 && tiles_m < sm_count()) return run<64, A2_MN, false>(a, stream);
   if (a.N <= 128)
-    return pair ? run<128, A2_MN, true>(a, stream) : run<128, A2_MN, false>(a, stream);
+    return pair ? run_pair2<128, A2_MN>(a, stream) : run<128, A2_MN, false>(a, stream);
   const int64_t t192 = tiles_m * ((a.N + 191) / 192);
   if (t192 < 2 * sm_count())
-    return pair ? run<128, A2_MN, true>(a, stream) : run<128, A2_MN, false>(a, stream);
-  return pair ? run<192, A2_MN, true>(a, stream) : run<192, A2_MN, false>(a, stream);
+    return pair ? run_pair2<128, A2_MN>(a, stream) : run<128, A2_MN, false>(a, stream);
+  return pair ? run_pair2<192, A2_MN>(a, stream) : run<192, A2_MN, false>(a, stream);
 }
 
 }  // namespace
