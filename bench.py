@@ -180,14 +180,15 @@ class BlockStep:
             for b in self.layers:
                 self.S.slope_prune_nm(b["W"], b["Wv"], b["Wm"], stream=stream)
 
-    def run(self, stream, marks=None):
-        """Issues the step on `stream`; `marks` (optional) records an event
-        pair around every ABI call, keyed by call name.  A training step
-        prunes (the row mask is re-derived from the current weights),
-        double-prunes, runs the forward and both gradients; an inference step
-        runs the forward on the pre-compressed weights."""
+    def run(self, stream, marks=None, only=None):
+        """Issues the step on `stream` (or, with `only`, the calls of that one
+        linear); `marks` (optional) records an event pair around every ABI
+        call, keyed by call name.  A training step prunes (the row mask is
+        re-derived from the current weights), double-prunes, runs the forward
+        and both gradients; an inference step runs the forward on the
+        pre-compressed weights."""
         S = self.S
-        for b in self.layers:
+        for b in (self.layers if only is None else [self.layers[only]]):
             calls = [] if self.wl.forward_only else [
                 ("prune", lambda b=b: S.slope_prune_nm(b["W"], b["Wv"], b["Wm"], stream=stream)),
                 ("double_prune", lambda b=b: S.slope_double_prune(b["Wv"], b["Wm"], b["out"], b["inp"],
@@ -464,26 +465,56 @@ def e2e_measure(args, wl, st, stream, dev):
     h2d = sum(v.numel() * v.element_size() for d in host_in for v in d.values())
     d2h = sum(v.numel() * v.element_size() for d in host_out for v in d.values())
 
+    # Pipelined per linear, as a caller streaming a block would: one copy
+    # stream brings linear i+1's inputs in while linear i computes, another
+    # takes linear i's results out.  Events keep each device buffer from
+    # being overwritten before the work that reads it is done.
+    n_lin = len(st.layers)
+    cin, cout = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(n_lin)]
+    ev_done = [torch.cuda.Event() for _ in range(n_lin)]
+    ev_out = [torch.cuda.Event() for _ in range(n_lin)]
+    started = [False] * n_lin
+
     def one():
-        with torch.cuda.stream(stream):
-            for b, hi in zip(st.layers, host_in):
+        for i, (b, hi, ho) in enumerate(zip(st.layers, host_in, host_out)):
+            if started[i]:
+                cin.wait_event(ev_done[i])  # last step's compute has read these inputs
+            with torch.cuda.stream(cin):
                 for k, v in hi.items():
                     b[k].copy_(v, non_blocking=True)
-            st.run(stream)
-            for b, ho in zip(st.layers, host_out):
+            ev_in[i].record(cin)
+            stream.wait_event(ev_in[i])
+            if started[i]:
+                stream.wait_event(ev_out[i])  # last step's results of this linear are out
+            with torch.cuda.stream(stream):
+                st.run(stream, only=i)
+            ev_done[i].record(stream)
+            cout.wait_event(ev_done[i])
+            with torch.cuda.stream(cout):
                 for k, v in ho.items():
                     v.copy_(b[k], non_blocking=True)
+            ev_out[i].record(cout)
+            started[i] = True
+
+    def join():  # the compute stream waits for the last copies out
+        for i in range(n_lin):
+            stream.wait_event(ev_out[i])
 
     for _ in range(2):
         one()
-    stream.synchronize()
+    join()
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n = max(3, min(args.steps, 20))
     e0.record(stream)
+    cin.wait_event(e0)
+    cout.wait_event(e0)
     for _ in range(n):
         one()
+    join()
     e1.record(stream)
-    stream.synchronize()
+    torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / n
     return {"value": round(flops_per_step(wl) / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}

@@ -381,10 +381,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (leader) {
             for (int pr = 1; pr < cs; ++pr) {
               const uint32_t base = mapa_shared(smem_u32(red), static_cast<uint32_t>(pr));
+              // eight coalesced remote loads in flight (one 128-byte column
+              // segment per warp each), then their adds
 #pragma unroll
-              for (int j = 0; j < CH; ++j)
-                v[j] = __float_as_uint(__uint_as_float(v[j]) +
-                                       ld_shared_cluster_f32(base + 4u * ((c0 + j) * kBM + row)));
+              for (int g = 0; g < CH; g += 8) {
+                float t[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  t[j] = ld_shared_cluster_f32(base + 4u * ((c0 + g + j) * kBM + row));
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[g + j] = __float_as_uint(__uint_as_float(v[g + j]) + t[j]);
+              }
             }
           }
         }
@@ -710,12 +717,14 @@ cudaError_t run(const DenseGemmArgs& a, cudaStream_t stream) {
   int csplit = 1;
   if (EPI == DenseEpi::StoreBf16HiLo) {
     // no atomic split for the rounding store; when the tiles leave SMs
-    // idle, split K over a cluster of up to 8 CTAs (>= 4 K-blocks each)
+    // idle, split K over a cluster of up to 8 CTAs.  The hand-over costs
+    // about 2.5 us (cluster-scope fences and arrivals), so each CTA keeps
+    // at least 16 K-blocks.
     splits = 1;
     const int tiles = tiles_m * tiles_n;
     int want = sm_count() / tiles;
     want = want < 8 ? want : 8;
-    want = want < num_kb / 4 ? want : num_kb / 4;
+    want = want < num_kb / 16 ? want : num_kb / 16;
     if (C::RED_BYTES > 0 && want >= 2) {
       const int kbs = (num_kb + want - 1) / want;
       csplit = (num_kb + kbs - 1) / kbs;  // every CTA of the cluster owns >= 1 K-block

@@ -362,10 +362,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (leader) {
             for (int pr = 1; pr < cs; ++pr) {
               const uint32_t base = mapa_shared(smem_u32(red), static_cast<uint32_t>(pr));
+              // eight coalesced remote loads in flight (one 128-byte column
+              // segment per warp each), then their adds
 #pragma unroll
-              for (int j = 0; j < CH; ++j)
-                v[j] = __float_as_uint(__uint_as_float(v[j]) +
-                                       ld_shared_cluster_f32(base + 4u * ((c0 + j) * kBM + row)));
+              for (int g = 0; g < CH; g += 8) {
+                float t[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  t[j] = ld_shared_cluster_f32(base + 4u * ((c0 + g + j) * kBM + row));
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[g + j] = __float_as_uint(__uint_as_float(v[g + j]) + t[j]);
+              }
             }
           }
         }
@@ -519,14 +526,15 @@ cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
     p.group_m = g < 1 ? 1 : (g > rows ? rows : g);
   }
   p.out_bf16 = a.out_bf16 ? 1 : 0;
-  // Narrow tiles that leave SMs idle split K over a cluster of up to 8 CTAs
-  // (>= 4 sparse K-blocks each); the partials meet in the leader's registers.
+  // Narrow tiles that leave SMs idle split K over a cluster of up to 8 CTAs;
+  // the partials meet in the leader's registers.  The hand-over costs about
+  // 2.5 us, so each CTA keeps at least 16 sparse K-blocks.
   p.csplit = 1;
   p.kb_per_split = p.num_kb;
   if (!PAIR && C::RED_BYTES > 0) {
     int want = sm_count() / p.num_tiles;
     want = want < 8 ? want : 8;
-    want = want < p.num_kb / 4 ? want : p.num_kb / 4;
+    want = want < p.num_kb / 16 ? want : p.num_kb / 16;
     if (want >= 2) {
       p.kb_per_split = (p.num_kb + want - 1) / want;
       p.csplit = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;  // each CTA >= 1 block

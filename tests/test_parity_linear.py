@@ -66,8 +66,8 @@ CASES = [
     (300, 640, 384, 24),    # rank not a multiple of 16
     (130, 256, 128, 72),    # rank above 64: two adapter blocks
     (777, 1152, 896, 64),
-    (16, 2048, 1024, 64),   # few token tiles: K split over clusters (4 and 2 CTAs)
-    (48, 1536, 3072, 32),   # odd cluster sizes (3 and 6 CTAs), ragged T
+    (16, 4096, 2048, 64),   # few token tiles: K split over clusters (4 and 2 CTAs)
+    (48, 6144, 3072, 32),   # odd cluster sizes (6 and 3 CTAs), ragged T
     (4096, 1024, 1024, 16),  # OPT-350M block linears
     (4096, 1024, 4096, 16),
     (4096, 4096, 1024, 16),
