@@ -591,7 +591,10 @@ struct Sp2Cfg {
   static constexpr int META_COL = 2 * ACC_COLS;
   static constexpr int TMEM_NEED = META_COL + 16 * STAGES;
   static constexpr int TMEM_COLS = TMEM_NEED <= 256 ? 256 : 512;
-  static constexpr int SMEM = STAGES * STAGE + 1024 /*barriers*/ + 1024 /*align slack*/;
+  // output staging for the TMA stores: 1 KB per epilogue warp
+  static constexpr int STG_BYTES = 1024;
+  static constexpr int SMEM = STAGES * STAGE + 1024 /*barriers*/ + kEpiWarps * STG_BYTES +
+                              1024 /*align slack*/;
   static_assert(STAGE % 1024 == 0 && (HB * 128) % 1024 == 0, "1024-byte aligned atoms");
   static_assert(TMEM_NEED <= 512, "TMEM budget");
   static_assert(STAGES >= 2, "pipeline depth");
@@ -608,7 +611,8 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmMeta,
                        const __grid_constant__ CUtensorMap tmA2,
-                       const __grid_constant__ CUtensorMap tmB2, const SpParams p) {
+                       const __grid_constant__ CUtensorMap tmB2,
+                       const __grid_constant__ CUtensorMap tmOut, const SpParams p) {
   using C = Sp2Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -778,13 +782,15 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     const int q = warp & 3;
     const int half = warp >= 14 ? 1 : 0;
     const uint32_t acc_empty0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
+    // this warp's 1 KB staging buffer: [token][32 weight rows] of the output,
+    // 16 tokens (bf16) or 8 (fp32) at a time, written out by a TMA store
+    uint8_t* stg = smem + C::STAGES * C::STAGE + 1024 + (q + 4 * half) * C::STG_BYTES;
     int local = 0;
     for (int u = unit0; u < units; u += ustep, ++local) {
       int m0, n0;
       decode(u, m0, n0);
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
-      const int m = m0 + 32 * q + lane;
       if (!mbar_wait(&acc_full[buf], use & 1, abort_flag, p.status)) break;
       tc_fence_after();
       const uint32_t trow = tmem + buf * C::ACC_COLS + (static_cast<uint32_t>(32 * q) << 16);
@@ -798,20 +804,41 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8 * buf);
         }
-        const int nlim = p.N - (n0 + c0);
+        // stage 16 tokens (bf16) or 8 (fp32) at a time and store them
+        auto flush = [&](int t0) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmOut, stg, m0 + 32 * q, n0 + c0 + t0);  // tokens past N are clipped
+            bulk_commit();
+          }
+        };
+        auto reuse = [&]() {  // the warp's previous store has read the buffer
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+        };
         if (p.out_bf16) {
-          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(n0 + c0) * p.M + m;
+          __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stg);
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nlim) o[static_cast<size_t>(j) * p.M] = __float2bfloat16_rn(__uint_as_float(v[j]));
+          for (int g = 0; g < 32; g += 16) {
+            reuse();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) sb[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[g + j]));
+            flush(g);
+          }
         } else {
-          float* o = static_cast<float*>(p.out) + static_cast<size_t>(n0 + c0) * p.M + m;
+          float* sf = reinterpret_cast<float*>(stg);
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nlim) o[static_cast<size_t>(j) * p.M] = __uint_as_float(v[j]);
+          for (int g = 0; g < 32; g += 8) {
+            reuse();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) sf[j * 32 + lane] = __uint_as_float(v[g + j]);
+            flush(g);
+          }
         }
       }
     }
+    if (lane == 0) bulk_wait_all();
   } else {
     // ------------------------------------------------ metadata -> TMEM ---
     // As in the one-CTA kernel, on this CTA's own metadata and TMEM, with
@@ -914,6 +941,13 @@ cudaError_t run_pair2(const SparseGemmArgs& a, cudaStream_t stream) {
     tA2 = tA;  // unused
     tB2 = tB;
   }
+  // output: N x M (tokens x weight rows), boxes of 32 rows x 16 (bf16) or
+  // 8 (fp32) tokens
+  CUtensorMap tOut;
+  ok = ok && (a.out_bf16 ? make_tmap_2d(&tOut, a.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, N,
+                                        2 * M, 32, 16, Swz::None)
+                         : make_tmap_2d(&tOut, a.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, N,
+                                        4 * M, 32, 8, Swz::None));
   if (!ok) return cudaErrorInvalidValue;
   SpParams p = {};
   p.M = static_cast<int>(M); p.N = static_cast<int>(N); p.K = static_cast<int>(K);
@@ -938,7 +972,7 @@ cudaError_t run_pair2(const SparseGemmArgs& a, cudaStream_t stream) {
   const int clusters = units < max_clusters[dev].load() ? units : max_clusters[dev].load();
   cfg.gridDim = dim3(2 * clusters);
   add_pdl_attr(cfg, attr);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tA, tB, tMeta, tA2, tB2, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tA, tB, tMeta, tA2, tB2, tOut, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
