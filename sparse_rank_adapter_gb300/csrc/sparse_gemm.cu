@@ -994,7 +994,7 @@ cudaError_t dispatch(const SparseGemmArgs& a, cudaStream_t stream) {
   const int64_t t192 = tiles_m * ((a.N + 191) / 192);
   if (t192 < 2 * sm_count())
     return pair ? run_pair2<128, A2_MN>(a, stream) : run<128, A2_MN, false>(a, stream);
-  return pair ? run_pair2<192, A2_MN>(a, stream) : run<192, A2_MN, false>(a, stream);
+  return pair ? run_pair2<224, A2_MN>(a, stream) : run<192, A2_MN, false>(a, stream);
 }
 
 }  // namespace
