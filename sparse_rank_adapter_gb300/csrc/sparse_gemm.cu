@@ -980,8 +980,9 @@ cudaError_t run_pair2(const SparseGemmArgs& a, cudaStream_t stream) {
 // N tile by token count: the smallest tile that covers small batches (up to
 // 128 tokens, 64-wide tiles while the weight has fewer 128-row tiles than
 // there are SMs, so that its stream spreads over more of them); for large
-// batches 192 (the widest that still double-buffers in TMEM beside the
-// metadata) unless 128 gives the grid noticeably more tiles per SM.
+// batches CTA pairs with 224- or 128-token tiles (an even number of weight
+// tiles), else one CTA with 192 (the widest that still double-buffers in
+// TMEM beside the metadata) unless 128 gives the grid noticeably more tiles.
 template <bool A2_MN>
 cudaError_t dispatch(const SparseGemmArgs& a, cudaStream_t stream) {
   if (a.N <= 16) return run<16, A2_MN, false>(a, stream);
@@ -991,10 +992,19 @@ cudaError_t dispatch(const SparseGemmArgs& a, cudaStream_t stream) {
   if (a.N <= 128 && tiles_m < sm_count()) return run<64, A2_MN, false>(a, stream);
   if (a.N <= 128)
     return pair ? run_pair2<128, A2_MN>(a, stream) : run<128, A2_MN, false>(a, stream);
+  if (pair) {
+    // CTA pairs: 224 or 128 tokens per tile, whichever needs fewer rounds of
+    // the pairs the GPU holds, counting 32 columns' worth of fixed cost per tile
+    const int64_t clusters = sm_count() / 2;
+    auto cost = [&](int64_t bn) {
+      const int64_t units = (tiles_m / 2) * ((a.N + bn - 1) / bn);
+      return ((units + clusters - 1) / clusters) * (bn + 32);
+    };
+    return cost(224) <= cost(128) ? run_pair2<224, A2_MN>(a, stream) : run_pair2<128, A2_MN>(a, stream);
+  }
   const int64_t t192 = tiles_m * ((a.N + 191) / 192);
-  if (t192 < 2 * sm_count())
-    return pair ? run_pair2<128, A2_MN>(a, stream) : run<128, A2_MN, false>(a, stream);
-  return pair ? run_pair2<224, A2_MN>(a, stream) : run<192, A2_MN, false>(a, stream);
+  if (t192 < 2 * sm_count()) return run<128, A2_MN, false>(a, stream);
+  return run<192, A2_MN, false>(a, stream);
 }
 
 }  // namespace
