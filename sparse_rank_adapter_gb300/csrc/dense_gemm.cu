@@ -442,8 +442,12 @@ constexpr int kPairStage = kA_BYTES + kPairHalfB * kBK * 2;  // 32 KB
 constexpr int kPairStages = 6;
 constexpr int kPairSmem = kPairStages * kPairStage + 1024 + 1024;
 constexpr int kPairTmemCols = 2 * kPairBN;  // double-buffered 256-column accumulator
+// 10 warps: TMA, MMA, and eight epilogue warps (two per TMEM lane quadrant,
+// alternate 32-column chunks), so the last tile's epilogue, which nothing
+// overlaps, is short
+constexpr int kPairThreads = 320;
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kPairThreads, 1)
     dw_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const DnParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -485,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 8);  // four epilogue warps in each CTA
+      mbar_init(&acc_empty[b], 16);  // eight epilogue warps in each CTA
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -567,6 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------ epilogue -----------
     const int q = warp & 3;
+    const int half = warp >= 6 ? 1 : 0;  // which alternate column chunks
     const uint32_t acc_empty0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
     int local = 0;
     for (int u = unit0; u < units; u += ustep, ++local) {
@@ -586,10 +591,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int c0 = 0; c0 < kPairBN; c0 += 32) {
+        if (((c0 >> 5) & 1) != half) continue;  // the other warp of this quadrant's chunk
         uint32_t v[32];
         tmem_ld_32x32b_x32(trow + c0, v);
         tmem_ld_wait();
-        if (c0 + 32 >= kPairBN) {  // last chunk read: hand the buffer back early
+        if (c0 + 64 >= kPairBN) {  // this warp's last chunk read: hand the buffer back early
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8 * buf);
@@ -624,7 +630,7 @@ cudaError_t run_dw_pair(const DenseGemmArgs& a, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kPairThreads);
   cfg.dynamicSmemBytes = kPairSmem;
   cfg.stream = stream;
   if (!attr_set[dev].load()) {
