@@ -23,12 +23,13 @@
 //
 // The hi/lo store needs the whole sum before it rounds, so its split-K goes
 // through a thread-block cluster instead of atomics: the cluster's CTAs take
-// K ranges of the same tile; each peer writes its fp32 partial into its own
-// shared memory and arrives (release, cluster scope) on the leader's
-// barrier; the leader reads the partials over distributed shared memory,
-// adds them to its own, stores, and arrives back on each peer's barrier so
-// the peer may overwrite its partial with the next tile's.  This is what
-// gives a handful of token tiles (small T) more than one SM each.
+// K ranges of the same tile; each writes its fp32 partial into its own
+// shared memory and arrives (release, cluster scope) on every other CTA's
+// barrier; then each adds one slice of the tile's rows over all the
+// partials (distributed shared memory), stores it, and arrives on every
+// other CTA's second barrier, after which partials may be overwritten with
+// the next tile's.  This is what gives a handful of token tiles (small T)
+// more than one SM each.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -197,8 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = empty + C::STAGES;  // [2]
   uint64_t* acc_empty = acc_full + 2;      // [2]
   uint64_t* mma_done = acc_empty + 2;
-  uint64_t* red_full = mma_done + 1;   // leader: every peer's partial is in place
-  uint64_t* red_empty = red_full + 1;  // peer: the leader has read this CTA's partial
+  uint64_t* red_full = mma_done + 1;   // cluster split: every CTA's partial is in place
+  uint64_t* red_empty = red_full + 1;  // cluster split: every CTA has read this CTA's partial
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(red_empty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   float* red = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE + 1024);
@@ -228,8 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
     }
     mbar_init(mma_done, 1);
-    mbar_init(red_full, 4 * (cs > 1 ? cs - 1 : 1));  // four epilogue warps per peer
-    mbar_init(red_empty, 4);                         // the leader's four epilogue warps
+    mbar_init(red_full, 4 * (cs > 1 ? cs - 1 : 1));   // every other CTA's epilogue warps
+    mbar_init(red_empty, 4 * (cs > 1 ? cs - 1 : 1));
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -337,13 +338,90 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       if (!mbar_wait(&acc_full[buf], use & 1, abort_flag, p.status)) break;
       tc_fence_after();
-      // cluster split-K: a peer first waits until the leader has read its
-      // previous partial; the leader waits until every peer's is in place
-      const bool peer = cs > 1 && crank != 0, leader = cs > 1 && crank == 0;
-      if (peer && !mbar_wait_cluster(red_empty, (local & 1) ^ 1, abort_flag, p.status)) break;
-      if (leader && !mbar_wait_cluster(red_full, local & 1, abort_flag, p.status)) break;
       const uint32_t trow = tmem + buf * C::ACC_COLS + (static_cast<uint32_t>(32 * q) << 16);
       constexpr int CH = BN < 32 ? BN : 32;
+      if constexpr (C::RED_BYTES > 0 && EPI == DenseEpi::StoreBf16HiLo) {
+        if (cs > 1) {
+          // Cluster split of K, reduce-scatter: every CTA leaves its fp32
+          // partial in its own shared memory ([column][row]); then each
+          // adds one slice of the rows over all the CTAs' partials and
+          // stores it.  The buffer is overwritten only after every CTA
+          // has read the previous tile's.
+          if (!mbar_wait_cluster(red_empty, (local & 1) ^ 1, abort_flag, p.status)) break;
+          const int row = 32 * q + lane;
+#pragma unroll
+          for (int c0 = 0; c0 < BN; c0 += CH) {
+            uint32_t v[32];
+            if constexpr (CH == 32) {
+              tmem_ld_32x32b_x32(trow + c0, v);
+            } else {
+              uint32_t w[4];
+#pragma unroll
+              for (int u = 0; u < CH / 4; ++u) {
+                tmem_ld_32x32b_x4(trow + c0 + 4 * u, w);
+                v[4 * u] = w[0]; v[4 * u + 1] = w[1]; v[4 * u + 2] = w[2]; v[4 * u + 3] = w[3];
+              }
+            }
+            tmem_ld_wait();
+            if (c0 + CH >= BN) {  // last chunk read: hand the accumulator back
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            }
+#pragma unroll
+            for (int j = 0; j < CH; ++j) red[(c0 + j) * kBM + row] = __uint_as_float(v[j]);
+          }
+          asm volatile("fence.acq_rel.cluster;" ::: "memory");
+          __syncwarp();
+          if (lane == 0)
+            for (int pr = 0; pr < cs; ++pr)
+              if (pr != static_cast<int>(crank))
+                mbar_arrive_cluster(mapa_shared(smem_u32(red_full), static_cast<uint32_t>(pr)));
+          if (!mbar_wait_cluster(red_full, local & 1, abort_flag, p.status)) break;
+          // this CTA's slice: rows [r0, r0 + nrow), 8 columns per work item,
+          // consecutive threads on consecutive rows (coalesced remote loads)
+          const int rows = (kBM + cs - 1) / cs;
+          const int r0 = static_cast<int>(crank) * rows;
+          const int nrow = min(kBM, r0 + rows) - r0;
+          const int items = nrow * (BN / 8);
+          for (int w = static_cast<int>(threadIdx.x) - 64; w < items; w += 128) {
+            const int rr = r0 + w % nrow, cg = w / nrow;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int pr = 0; pr < cs; ++pr) {
+              const uint32_t base = mapa_shared(smem_u32(red), static_cast<uint32_t>(pr));
+              float t[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) t[j] = ld_shared_cluster_f32(base + 4u * ((8 * cg + j) * kBM + rr));
+#pragma unroll
+              for (int j = 0; j < 8; ++j) acc[j] += t[j];
+            }
+            const int mm = m0 + rr, n = n0 + 8 * cg;
+            if (mm < p.M && n < p.N) {  // N % 8 == 0
+              uint4 hi, lo;
+              uint32_t* ph = reinterpret_cast<uint32_t*>(&hi);
+              uint32_t* pl = reinterpret_cast<uint32_t*>(&lo);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * u], acc[2 * u + 1]);
+                const __nv_bfloat162 l = __floats2bfloat162_rn(acc[2 * u] - __bfloat162float(h.x),
+                                                               acc[2 * u + 1] - __bfloat162float(h.y));
+                ph[u] = *reinterpret_cast<const uint32_t*>(&h);
+                pl[u] = *reinterpret_cast<const uint32_t*>(&l);
+              }
+              __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(mm) * p.ldo;
+              *reinterpret_cast<uint4*>(o + n) = hi;
+              *reinterpret_cast<uint4*>(o + p.lo_off + n) = lo;
+            }
+          }
+          asm volatile("fence.acq_rel.cluster;" ::: "memory");
+          __syncwarp();
+          if (lane == 0)
+            for (int pr = 0; pr < cs; ++pr)
+              if (pr != static_cast<int>(crank))
+                mbar_arrive_cluster(mapa_shared(smem_u32(red_empty), static_cast<uint32_t>(pr)));
+          continue;
+        }
+      }
       uint4 mrow[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
       if constexpr (EPI == DenseEpi::MaskedWeightGrad) {
         if (m < p.M) {
@@ -371,45 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[buf]);
         }
-        if constexpr (C::RED_BYTES > 0) {
-          const int row = 32 * q + lane;
-          if (peer) {  // hand the partial over; the leader stores
-#pragma unroll
-            for (int j = 0; j < CH; ++j) red[(c0 + j) * kBM + row] = __uint_as_float(v[j]);
-            continue;
-          }
-          if (leader) {
-            for (int pr = 1; pr < cs; ++pr) {
-              const uint32_t base = mapa_shared(smem_u32(red), static_cast<uint32_t>(pr));
-              // eight coalesced remote loads in flight (one 128-byte column
-              // segment per warp each), then their adds
-#pragma unroll
-              for (int g = 0; g < CH; g += 8) {
-                float t[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                  t[j] = ld_shared_cluster_f32(base + 4u * ((c0 + g + j) * kBM + row));
-#pragma unroll
-                for (int j = 0; j < 8; ++j) v[g + j] = __float_as_uint(__uint_as_float(v[g + j]) + t[j]);
-              }
-            }
-          }
-        }
         if (m >= p.M) continue;
         epilogue_chunk<BN, CH, EPI>(p, v, m, n0, c0, mrow);
-      }
-      if (cs > 1) {
-        // peer: the partial is written; leader: the peers' partials are read
-        asm volatile("fence.acq_rel.cluster;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
-          if (peer) {
-            mbar_arrive_cluster(mapa_shared(smem_u32(red_full), 0u));
-          } else {
-            for (int pr = 1; pr < cs; ++pr)
-              mbar_arrive_cluster(mapa_shared(smem_u32(red_empty), static_cast<uint32_t>(pr)));
-          }
-        }
       }
     }
   }
