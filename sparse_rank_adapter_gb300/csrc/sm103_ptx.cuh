@@ -105,18 +105,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// 2-D tile load into the same shared-memory offset of every CTA of the
-// cluster named in `mask`; each destination CTA's barrier at `bar`'s offset
-// counts the bytes it receives.  Only within this GPU's own memory.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                               int32_t x, int32_t y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask)
-      : "memory");
-}
-
 // ------------------------------------------------------------- cluster ----
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -354,22 +342,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
       : "memory");
-}
-
-// As mma_commit, arriving on the barrier at `bar`'s offset in every CTA of
-// the cluster named in `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
-// Copy a 128-row x 16-byte shared-memory matrix into 128 TMEM lanes x 4 columns.
-__device__ __forceinline__ void tmem_cp_128x128b(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc)
-               : "memory");
 }
 
 // Each thread of the warp reads 32 consecutive 32-bit columns of its lane

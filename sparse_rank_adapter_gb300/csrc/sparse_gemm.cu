@@ -16,10 +16,10 @@
 // the epilogue writes directly (lane = m, so a warp's stores of one column
 // n are 128 contiguous bytes).
 //
-// Persistent kernel, one CTA per SM, tiles taken round-robin.  With PAIR,
-// CTAs run in clusters of two on adjacent M tiles with the same N tile: each
-// loads half of the shared B tile (the tokens) and multicasts it to both,
-// and a stage is refilled only after both CTAs' MMAs released it.
+// Two kernels.  sparse_gemm_kernel: one CTA per tile, persistent, one CTA
+// per SM, tiles taken round-robin; it serves up to 128 tokens and weights
+// with an odd number of 128-row tiles.  sparse_pair_kernel (below): CTA
+// pairs on the pair-wide MMA for the large batches.
 //
 // Roles (576 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues
 // the MMAs (one thread), warps 2..5 and 14..17 drain the accumulator (two
@@ -93,13 +93,13 @@ struct SpParams {
   int num_kb;      // sparse K-blocks (K / 128)
   int num_ab;      // adapter blocks per part (ceil(r / 64)); parts: hi, lo
   int out_bf16;
-  int csplit;        // CTAs of a cluster that split one tile's K (not with PAIR); 1 = none
+  int csplit;        // CTAs of a cluster that split one tile's K (one-CTA kernel); 1 = none
   int kb_per_split;  // sparse K-blocks per CTA of such a cluster
   void* out;
   unsigned int* status;
 };
 
-template <int BN, bool A2_MN, bool PAIR>
+template <int BN, bool A2_MN>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
@@ -123,10 +123,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* red = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE + 1024);
 
   const int warp = warp_id(), lane = lane_id();
-  // Cluster split of K (narrow tiles, never with PAIR): CTA `crank` of the
+  // Cluster split of K (narrow tiles): CTA `crank` of the
   // cluster takes sparse K-blocks [crank * kb_per_split, ...); the last one
   // also runs the adapter steps.  Its fp32 partial goes to the leader.
-  const int cs = PAIR ? 1 : p.csplit;
+  const int cs = p.csplit;
   const uint32_t crank = cs > 1 ? cluster_ctarank() : 0u;
   const int kb0 = cs > 1 ? static_cast<int>(crank) * p.kb_per_split : 0;
   const int nsp = cs > 1 ? min(p.num_kb - kb0, p.kb_per_split) : p.num_kb;
@@ -135,17 +135,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   // step kk of a tile -> K-block index: sparse blocks kb0.., then the adapter
   // blocks, numbered from num_kb as in the unsplit tile
   auto kblock = [&](int kk) { return kk < nsp ? kb0 + kk : p.num_kb + (kk - nsp); };
-  // Work units: tiles, or (with PAIR) pairs of M-adjacent tiles per cluster.
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-  const int units = PAIR ? p.num_tiles / 2 : p.num_tiles;
-  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1)
-                         : static_cast<int>(cs > 1 ? blockIdx.x / cs : blockIdx.x);
-  const int ustep = PAIR ? static_cast<int>(gridDim.x >> 1)
-                         : static_cast<int>(cs > 1 ? gridDim.x / cs : gridDim.x);
-  // Raster order: bands of group_m M tiles (pairs with PAIR); within a band
-  // the M tiles turn fastest, then the N tiles, so the band's weight tiles
-  // stay in L2 while every token tile passes over them once.
-  const int rows_m = PAIR ? p.tiles_m / 2 : p.tiles_m;
+  // Work units: tiles (one per cluster when K is split).
+  const int units = p.num_tiles;
+  const int unit0 = static_cast<int>(cs > 1 ? blockIdx.x / cs : blockIdx.x);
+  const int ustep = static_cast<int>(cs > 1 ? gridDim.x / cs : gridDim.x);
+  // Raster order: bands of group_m M tiles; within a band the M tiles turn
+  // fastest, then the N tiles, so the band's weight tiles stay in L2 while
+  // every token tile passes over them once.
+  const int rows_m = p.tiles_m;
   const int tiles_n = units / rows_m;
   auto band = [&](int u, int& mi, int& ni) {
     const int per_band = p.group_m * tiles_n;
@@ -158,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tile_m0 = [&](int u) {
     int mi, ni;
     band(u, mi, ni);
-    return PAIR ? (2 * mi + static_cast<int>(rank)) * kBM : mi * kBM;
+    return mi * kBM;
   };
   auto tile_n0 = [&](int u) {
     int mi, ni;
@@ -169,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], PAIR ? 2 : 1);  // both CTAs' MMAs release a stage
+      mbar_init(&empty[s], 1);
       mbar_init(&meta_full[s], 4);  // one arrival per metadata warp
     }
     for (int b = 0; b < 2; ++b) {
@@ -187,13 +184,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  if (PAIR || cs > 1)
-    cluster_sync();  // the peer's barriers exist before any multicast or arrival reaches them
+  if (cs > 1)
+    cluster_sync();  // the peers' barriers exist before any arrival reaches them
   else
     __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  grid_dependency_wait();  // the previous kernel's outputs are visible from here
+  // With the adapter (r > 0) the kernel before this one on the stream is
+  // the call's own rank-r GEMM, which produces only the adapter's B operand
+  // (XL or G); its CTAs could start only after everything before it had
+  // completed.  So the weights and tokens may be read at once and only the
+  // TMA producer waits, before its first adapter load: the rank-r GEMM runs
+  // alongside the sparse K-loop.  Without the adapter the predecessor is
+  // unknown, and every thread waits here.
+  if (p.r == 0) grid_dependency_wait();
   allow_dependents_launch();
 
   if (warp == 0) {
@@ -202,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
       tma_prefetch_desc(&tmMeta);
+      bool dep_done = p.r == 0;
       int it = 0;
       bool stop = false;
       for (int u = unit0; u < units && !stop; u += ustep) {
@@ -218,20 +223,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kb < p.num_kb) {
             mbar_arrive_expect_tx(&full[s], kA_BYTES + C::B_BYTES + kMETA_BYTES);
             tma_load_2d(sA, &tmA, &full[s], kb * kBKc, m0);
-            if (PAIR) {  // this CTA's half of the B rows, to both CTAs
-              const int h = static_cast<int>(rank) * (BN / 2);
-              tma_load_2d_mc(sB + h * 128, &tmB, &full[s], kb * 128, n0 + h, 3);
-              tma_load_2d_mc(sB + BN * 128 + h * 128, &tmB, &full[s], kb * 128 + 64, n0 + h, 3);
-            } else {
-              tma_load_2d(sB, &tmB, &full[s], kb * 128, n0);
-              tma_load_2d(sB + BN * 128, &tmB, &full[s], kb * 128 + 64, n0);
-            }
+            tma_load_2d(sB, &tmB, &full[s], kb * 128, n0);
+            tma_load_2d(sB + BN * 128, &tmB, &full[s], kb * 128 + 64, n0);
             tma_load_2d(sMeta, &tmMeta, &full[s], kb * 16, m0);
           } else {
             // adapter block c of part `part` (0 = hi, 1 = lo): rank columns
             // 64c .. 64c+63 of A2, and the same columns of that part of B2.
             // A2 rows/columns past r are zero-filled, so whatever B2 holds
             // past the part's r columns adds nothing.
+            if (!dep_done) {  // the rank-r GEMM's output is visible from here
+              grid_dependency_wait();
+              dep_done = true;
+            }
             const int a = kb - p.num_kb;
             const int part = a / p.num_ab, c = a % p.num_ab;
             mbar_arrive_expect_tx(&full[s], kA_BYTES + BN * 128);
@@ -241,12 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {      // L: M x r, 128 rows of 64 rank columns
               tma_load_2d(sA, &tmA2, &full[s], c * 64, m0);
             }
-            if (PAIR) {
-              const int h = static_cast<int>(rank) * (BN / 2);
-              tma_load_2d_mc(sB + h * 128, &tmB2, &full[s], part * p.r + c * 64, n0 + h, 3);
-            } else {
-              tma_load_2d(sB, &tmB2, &full[s], part * p.r + c * 64, n0);
-            }
+            tma_load_2d(sB, &tmB2, &full[s], part * p.r + c * 64, n0);
           }
         }
       }
@@ -300,10 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_bf16_ss(d, da, db, id_ad, 1u);
             }
           }
-          if (PAIR)
-            mma_commit_mc(&empty[s], 3);  // release the stage in both CTAs
-          else
-            mma_commit(&empty[s]);
+          mma_commit(&empty[s]);
         }
         if (!stop) mma_commit(&acc_full[buf]);
       }
@@ -452,17 +447,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(mma_done, 0, &no_abort, p.status);
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
-  // No CTA leaves while its peer may still multicast into it, read its
-  // partial or arrive on its barriers.
-  if (PAIR || cs > 1) cluster_sync();
+  // No CTA leaves while a peer may still read its partial or arrive on its
+  // barriers.
+  if (cs > 1) cluster_sync();
 }
 
-template <int BN, bool A2_MN, bool PAIR>
+template <int BN, bool A2_MN>
 cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
   using C = SpCfg<BN>;
-  auto kernel = sparse_gemm_kernel<BN, A2_MN, PAIR>;
+  auto kernel = sparse_gemm_kernel<BN, A2_MN>;
   static std::atomic<int> attr_set[64];
-  static std::atomic<int> max_clusters[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -471,29 +465,14 @@ cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
-  if (PAIR) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  }
   if (!attr_set[dev].load()) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    if (PAIR) {
-      int n = 0;
-      cfg.gridDim = dim3(2 * (sm_count() / 2));
-      e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
-      if (e != cudaSuccess) return e;
-      max_clusters[dev].store(n > 0 ? n : 1);
-    }
     attr_set[dev].store(1);
   }
   CUtensorMap tA, tB, tMeta, tA2, tB2;
   const uint64_t M = a.M, N = a.N, K = a.K, r = a.r;
-  const uint32_t b_rows = PAIR ? BN / 2 : BN;  // rows of B one TMA box brings
+  const uint32_t b_rows = BN;  // rows of B one TMA box brings
   bool ok = make_tmap_2d(&tA, a.a_vals, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K / 2, M, K, 64, kBM,
                          Swz::B128) &&
             make_tmap_2d(&tB, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, 2 * K, 64, b_rows,
@@ -520,10 +499,9 @@ cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
   p.num_kb = static_cast<int>(K / 128);
   p.num_ab = static_cast<int>((r + 63) / 64);
   {  // a band of weight tiles (values + metadata, all of K) of about 40 MB
-    const double tile_bytes = static_cast<double>(kBM) * K * 1.125 * (PAIR ? 2 : 1);
+    const double tile_bytes = static_cast<double>(kBM) * K * 1.125;
     int g = static_cast<int>(40.0e6 / tile_bytes);
-    const int rows = PAIR ? p.tiles_m / 2 : p.tiles_m;
-    p.group_m = g < 1 ? 1 : (g > rows ? rows : g);
+    p.group_m = g < 1 ? 1 : (g > p.tiles_m ? p.tiles_m : g);
   }
   p.out_bf16 = a.out_bf16 ? 1 : 0;
   // Narrow tiles that leave SMs idle split K over a cluster of up to 8 CTAs;
@@ -531,7 +509,7 @@ cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
   // 2.5 us, so each CTA keeps at least 16 sparse K-blocks.
   p.csplit = 1;
   p.kb_per_split = p.num_kb;
-  if (!PAIR && C::RED_BYTES > 0) {
+  if (C::RED_BYTES > 0) {
     int want = sm_count() / p.num_tiles;
     want = want < 8 ? want : 8;
     want = want < p.num_kb / 16 ? want : p.num_kb / 16;
@@ -543,22 +521,15 @@ cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
   p.out = a.out;
   p.status = device_status_ptr();
   if (!p.status) return cudaErrorInvalidDevicePointer;
-  int grid;
-  if (PAIR) {
-    const int units = p.num_tiles / 2;
-    const int clusters = units < max_clusters[dev].load() ? units : max_clusters[dev].load();
-    grid = 2 * clusters;
-  } else {
-    grid = p.csplit > 1 ? p.num_tiles * p.csplit  // one cluster per tile
-                        : (p.num_tiles < sm_count() ? p.num_tiles : sm_count());
-    if (p.csplit > 1) {
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = static_cast<unsigned>(p.csplit);
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-    }
+  const int grid = p.csplit > 1 ? p.num_tiles * p.csplit  // one cluster per tile
+                                 : (p.num_tiles < sm_count() ? p.num_tiles : sm_count());
+  if (p.csplit > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.csplit);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
   }
   cfg.gridDim = dim3(grid);
   add_pdl_attr(cfg, attr);
@@ -680,7 +651,14 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   tc_fence_before();
   cluster_sync();  // every barrier of both CTAs exists before anything reaches it
   tc_fence_after();
-  grid_dependency_wait();  // the previous kernel's outputs are visible from here
+  // With the adapter (r > 0) the kernel before this one on the stream is
+  // the call's own rank-r GEMM, which produces only the adapter's B operand
+  // (XL or G); its CTAs could start only after everything before it had
+  // completed.  So the weights and tokens may be read at once and only the
+  // TMA producer waits, before its first adapter load: the rank-r GEMM runs
+  // alongside the sparse K-loop.  Without the adapter the predecessor is
+  // unknown, and every thread waits here.
+  if (p.r == 0) grid_dependency_wait();
   allow_dependents_launch();
 
   if (warp == 0) {
@@ -689,6 +667,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
       tma_prefetch_desc(&tmMeta);
+      bool dep_done = p.r == 0;
       int it = 0;
       bool stop = false;
       for (int u = unit0; u < units && !stop; u += ustep) {
@@ -713,6 +692,10 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           } else {
             // adapter block c of part `part` (0 = hi, 1 = lo), as in the
             // one-CTA kernel; each CTA brings its rows of A2 and its half of B2
+            if (!dep_done) {  // the rank-r GEMM's output is visible from here
+              grid_dependency_wait();
+              dep_done = true;
+            }
             const int a = kb - p.num_kb;
             const int part = a / p.num_ab, c = a % p.num_ab;
             if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (kA_BYTES + C::HB * 128));
@@ -985,13 +968,13 @@ cudaError_t run_pair2(const SparseGemmArgs& a, cudaStream_t stream) {
 // TMEM beside the metadata) unless 128 gives the grid noticeably more tiles.
 template <bool A2_MN>
 cudaError_t dispatch(const SparseGemmArgs& a, cudaStream_t stream) {
-  if (a.N <= 16) return run<16, A2_MN, false>(a, stream);
-  if (a.N <= 64) return run<64, A2_MN, false>(a, stream);
+  if (a.N <= 16) return run<16, A2_MN>(a, stream);
+  if (a.N <= 64) return run<64, A2_MN>(a, stream);
   const int64_t tiles_m = a.M / kBM;
   const bool pair = tiles_m % 2 == 0;  // clusters pair M-adjacent tiles
-  if (a.N <= 128 && tiles_m < sm_count()) return run<64, A2_MN, false>(a, stream);
+  if (a.N <= 128 && tiles_m < sm_count()) return run<64, A2_MN>(a, stream);
   if (a.N <= 128)
-    return pair ? run_pair2<128, A2_MN>(a, stream) : run<128, A2_MN, false>(a, stream);
+    return pair ? run_pair2<128, A2_MN>(a, stream) : run<128, A2_MN>(a, stream);
   if (pair) {
     // CTA pairs: 224 or 128 tokens per tile, whichever needs fewer rounds of
     // the pairs the GPU holds, counting 32 columns' worth of fixed cost per tile
@@ -1003,8 +986,8 @@ cudaError_t dispatch(const SparseGemmArgs& a, cudaStream_t stream) {
     return cost(224) <= cost(128) ? run_pair2<224, A2_MN>(a, stream) : run_pair2<128, A2_MN>(a, stream);
   }
   const int64_t t192 = tiles_m * ((a.N + 191) / 192);
-  if (t192 < 2 * sm_count()) return run<128, A2_MN, false>(a, stream);
-  return run<192, A2_MN, false>(a, stream);
+  if (t192 < 2 * sm_count()) return run<128, A2_MN>(a, stream);
+  return run<192, A2_MN>(a, stream);
 }
 
 }  // namespace
