@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/slope.h"
 #include "slope_internal.h"
@@ -98,12 +99,55 @@ EncodeTiledFn encode_fn() {
 }
 }  // namespace
 
+// Encoded tensor maps, cached by everything that goes into them (address,
+// element type, extents, row stride, box, swizzle): a hit is exactly the map
+// that encoding would produce, so a call on the same buffers skips the
+// driver's encoder.  Direct-mapped, 256 entries, one lock.
+namespace {
+struct TmapKey {
+  const void* base;
+  uint64_t inner, outer, row_bytes;
+  uint32_t box_inner, box_outer;
+  int dtype, swz;
+  bool operator==(const TmapKey& o) const {
+    return base == o.base && inner == o.inner && outer == o.outer && row_bytes == o.row_bytes &&
+           box_inner == o.box_inner && box_outer == o.box_outer && dtype == o.dtype && swz == o.swz;
+  }
+};
+struct TmapSlot {
+  bool used = false;
+  TmapKey key;
+  CUtensorMap map;
+};
+constexpr int kTmapSlots = 256;
+TmapSlot g_tmap_cache[kTmapSlots];
+std::mutex g_tmap_mutex;
+
+size_t tmap_hash(const TmapKey& k) {
+  uint64_t h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
+  for (uint64_t v : {k.inner, k.outer, k.row_bytes, uint64_t(k.box_inner) << 32 | k.box_outer,
+                     uint64_t(k.dtype) << 8 | uint64_t(k.swz)})
+    h = (h ^ v) * 0x100000001B3ull;
+  return static_cast<size_t>(h >> 32) % kTmapSlots;
+}
+}  // namespace
+
 bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes,
                   uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                   uint32_t box_outer, Swz swz) {
+  (void)elem_bytes;
+  const TmapKey key{base, inner, outer, row_bytes, box_inner, box_outer, static_cast<int>(dtype),
+                    static_cast<int>(swz)};
+  const size_t slot = tmap_hash(key);
+  {
+    std::lock_guard<std::mutex> lock(g_tmap_mutex);
+    if (g_tmap_cache[slot].used && g_tmap_cache[slot].key == key) {
+      *map = g_tmap_cache[slot].map;
+      return true;
+    }
+  }
   EncodeTiledFn f = encode_fn();
   if (!f) return false;
-  (void)elem_bytes;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
@@ -117,7 +161,12 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
       f(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
         CU_TENSOR_MAP_INTERLEAVE_NONE, s, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lock(g_tmap_mutex);
+  g_tmap_cache[slot].used = true;
+  g_tmap_cache[slot].key = key;
+  g_tmap_cache[slot].map = *map;
+  return true;
 }
 
 // ----------------------------------------------------- status word --------
