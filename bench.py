@@ -202,16 +202,12 @@ class BlockStep:
                 calls += [
                     ("bwd_input", lambda b=b: S.slope_linear_bwd_input(b["dY"], b["Dv"], b["Dm"], b["L"], b["R"],
                                                                        b["dX"], b["G"], stream=stream)),
-                    # the weight-gradient call in two parts, so that the dW GEMM
-                    # is bracketed alone: dW, then the adapter gradients
-                    ("dw", lambda b=b: S.slope_linear_bwd_weight(b["dY"], b["X"], b["Wm"], b["XL"], b["G"],
-                                                                 b["dW"], b["dL"], b["dR"],
-                                                                 flags=S.SKIP_ADAPTER, stream=stream)),
-                ]
-                if self.wl.rank:
-                    calls.append(("adapter_grads", lambda b=b: S.slope_linear_bwd_weight(
+                    # dW and the adapter gradients dL, dR in one call (one
+                    # launch: the dW GEMM computes the two rank-r products too)
+                    ("bwd_weight", lambda b=b: S.slope_linear_bwd_weight(
                         b["dY"], b["X"], b["Wm"], b["XL"], b["G"], b["dW"], b["dL"], b["dR"],
-                        flags=S.SKIP_DW, stream=stream)))
+                        stream=stream)),
+                ]
             for name, fn in calls:
                 if marks is not None:
                     e0, e1 = marks.new(name, b)
@@ -228,7 +224,7 @@ class BlockStep:
             n += 2 if self.wl.rank else 1  # fwd: (XL) + sparse
             if not self.wl.forward_only:
                 n += 2 if self.wl.rank else 1  # bwd_input: (G) + sparse
-                n += 3 if self.wl.rank else 1  # dW call, then (dL, dR)
+                n += 1  # dW with dL, dR alongside
         return n
 
 
@@ -247,16 +243,12 @@ class Marks:
 
 
 def call_flops(name, T, inp, out, r):
-    """Dense-equivalent flops of one ABI call: the forward and input-gradient
-    calls run the main product 2·T·in·out and two rank-r products
-    2·T·r·(in + out); the dW call the main product; the adapter-gradient
-    call the two rank-r products."""
-    if name in ("fwd", "bwd_input"):
+    """Dense-equivalent flops of one ABI call: every GEMM call runs its main
+    product 2·T·in·out (forward, input gradient, weight gradient) and two
+    rank-r products 2·T·r·(in + out) (XL and the adapter term; G and the
+    adapter term; dL and dR)."""
+    if name in ("fwd", "bwd_input", "bwd_weight"):
         return 2.0 * T * inp * out + 2.0 * T * r * (inp + out)
-    if name == "dw":
-        return 2.0 * T * inp * out
-    if name == "adapter_grads":
-        return 2.0 * T * r * (inp + out)
     return 0.0
 
 
@@ -386,14 +378,9 @@ def gpu_arm(args):
         ach = alg / (calls_ms[dom] * 1e-3) / 1e12
         peak = bf16_sus * (2.0 if dom in ("fwd", "bwd_input") else 1.0)
         roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak}
-        if dom == "adapter_grads":  # the skinny products stream X and dY: memory-bound
-            byts = sum(2.0 * T * (i + o) for i, o, _ in per_call[dom]) / n_obs
-            achb = byts / (calls_ms[dom] * 1e-3) / 1e9
-            roof = {"bound": "hbm", "achieved": achb, "peak": hbm, "unit": "GB/s", "frac": achb / hbm}
     kernel_of = {"prune": "prune24_kernel (slope_prune_nm)", "double_prune": "double_prune24_kernel (slope_double_prune)",
                  "fwd": "slope_linear_fwd (XL GEMM + sparse GEMM)", "bwd_input": "slope_linear_bwd_input (G GEMM + sparse GEMM)",
-                 "dw": "dW GEMM (slope_linear_bwd_weight, SLOPE_SKIP_ADAPTER)",
-                 "adapter_grads": "dL, dR GEMMs (slope_linear_bwd_weight, SLOPE_SKIP_DW)"}
+                 "bwd_weight": "dW GEMM with dL, dR (slope_linear_bwd_weight)"}
     roof.update({"kernel": kernel_of.get(dom, dom), "traffic": None,
                  "peak_source": f"{src} ({'2x ' if dom in ('fwd', 'bwd_input') else ''}bf16 sustained)"
                  if roof['bound'] == 'tensor' else f"{src} hbm",

@@ -355,6 +355,10 @@ extern "C" int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T,
     }
     return SLOPE_OK;
   }
+  // dW and the adapter gradients in one launch when the dW GEMM runs on CTA
+  // pairs (an even number of 128-row weight tiles) and 2r fits one tile:
+  // dRᵀ = dYᵀ·XL shares dW's A operand and dLᵀ = Gᵀ·X its B operand.
+  const bool fuse = do_dw && do_ad && r <= 128 && (out / 128) % 2 == 0;
   if (do_dw) {
     // dW = M ⊙ (dYᵀ·X): M = out, N = in, K = T; A = dY MN-major, B = X MN-major.
     DenseGemmArgs w{};
@@ -362,9 +366,12 @@ extern "C" int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T,
     w.M = out; w.N = in; w.K = T; w.lda = out; w.ldb = in;
     w.epi = DenseEpi::MaskedWeightGrad; w.out = dW; w.ldo = dense ? in : in / 2;
     w.meta = Wm; w.dense_dw = dense; w.accumulate = acc; w.splits = 0;
+    if (fuse) {
+      w.fuse_r = r; w.xl = XL; w.g = G; w.dl = dL; w.dr = dR;
+    }
     if (launch_dense_gemm(w, st) != cudaSuccess) return SLOPE_ERR_CUDA;
   }
-  if (!do_ad) return SLOPE_OK;
+  if (!do_ad || fuse) return SLOPE_OK;
   if (!acc) {
     if (cudaMemsetAsync(dL, 0, sizeof(float) * in * r, st) != cudaSuccess ||
         cudaMemsetAsync(dR, 0, sizeof(float) * out * r, st) != cudaSuccess)

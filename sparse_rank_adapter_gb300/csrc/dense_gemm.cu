@@ -77,6 +77,9 @@ struct DnParams {
   int dense_dw, accumulate, atomic_out;
   int lo_off, fold;
   int csplit;  // CTAs of a cluster that split one tile's K (hi/lo store only); 1 = none
+  int fuse_r;  // pair dW kernel: r of the adapter gradients computed alongside; 0 = none
+  float* dl;   // in x r fp32 (added into)
+  float* dr;   // r x out fp32 (added into)
   unsigned int* status;
 };
 
@@ -490,6 +493,7 @@ constexpr int kPairThreads = 320;
 
 __global__ void __launch_bounds__(kPairThreads, 1)
     dw_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmXL,
                    const DnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -505,22 +509,39 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const int warp = warp_id(), lane = lane_id();
   const uint32_t rank = cluster_ctarank();
   const int pairs_m = p.tiles_m / 2;
-  const int per_split = pairs_m * p.tiles_n;
-  const int units = per_split * (p.num_tiles / (p.tiles_m * p.tiles_n));
+  const int w_tiles = pairs_m * p.tiles_n;  // dW tiles of one split
+  // With the adapter gradients fused, each split also has pairs_m dRᵀ tiles
+  // (dYᵀ·XL: the pair's weight rows against the 2r columns of XL) and
+  // tiles_n dLᵀ tiles (Gᵀ·X: the 2r columns of G, as rows, against X).
+  const int per_split = w_tiles + (p.fuse_r > 0 ? pairs_m + p.tiles_n : 0);
+  const int units = per_split * p.num_tiles;  // num_tiles holds the split count here
   const int unit0 = static_cast<int>(blockIdx.x >> 1);
   const int ustep = static_cast<int>(gridDim.x >> 1);
-  // Raster order within a split: bands of group_n N tiles; within a band the
-  // N tiles turn fastest, then the M pairs, so the band's X tiles stay in L2
-  // while each dY tile is used by the whole band as soon as it is loaded.
-  auto decode = [&](int u, int& m0, int& n0, int& z) {
+  // unit -> (this CTA's rows m0, the pair's columns n0, split z, kind: 0 dW,
+  // 1 dRᵀ, 2 dLᵀ).  dW tiles in raster order within a split: bands of
+  // group_n N tiles; within a band the N tiles turn fastest, then the M
+  // pairs, so the band's X tiles stay in L2 while each dY tile is used by
+  // the whole band as soon as it is loaded.
+  auto decode = [&](int u, int& m0, int& n0, int& z, int& kind) {
     const int mn = u % per_split;
     z = u / per_split;
-    const int per_band = p.group_n * pairs_m;
-    const int b = mn / per_band, w = mn % per_band;
-    const int first = b * p.group_n;
-    const int gn = min(p.group_n, p.tiles_n - first);
-    m0 = (2 * (w / gn) + static_cast<int>(rank)) * kBM;  // this CTA's 128 rows
-    n0 = (first + w % gn) * kPairBN;                       // the pair's 256 columns
+    if (mn < w_tiles) {
+      kind = 0;
+      const int per_band = p.group_n * pairs_m;
+      const int b = mn / per_band, w = mn % per_band;
+      const int first = b * p.group_n;
+      const int gn = min(p.group_n, p.tiles_n - first);
+      m0 = (2 * (w / gn) + static_cast<int>(rank)) * kBM;  // this CTA's 128 rows
+      n0 = (first + w % gn) * kPairBN;                       // the pair's 256 columns
+    } else if (mn < w_tiles + pairs_m) {
+      kind = 1;
+      m0 = (2 * (mn - w_tiles) + static_cast<int>(rank)) * kBM;
+      n0 = 0;
+    } else {
+      kind = 2;
+      m0 = static_cast<int>(rank) * kBM;  // rows = columns of G (2r of them are real)
+      n0 = (mn - w_tiles - pairs_m) * kPairBN;
+    }
   };
 
   if (threadIdx.x == 0) {
@@ -552,11 +573,17 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       // ---------------------------------------------- TMA producer -------
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
+      if (p.fuse_r > 0) {
+        tma_prefetch_desc(&tmG);
+        tma_prefetch_desc(&tmXL);
+      }
       int it = 0;
       bool stop = false;
       for (int u = unit0; u < units && !stop; u += ustep) {
-        int m0, n0, z;
-        decode(u, m0, n0, z);
+        int m0, n0, z, kind;
+        decode(u, m0, n0, z, kind);
+        const CUtensorMap* mA = kind == 2 ? &tmG : &tmA;   // rows: weight rows, or G's columns
+        const CUtensorMap* mB = kind == 1 ? &tmXL : &tmB;  // columns: X's, or XL's
         const int nb = n0 + static_cast<int>(rank) * kPairHalfB;  // this CTA's half of B
         const int kb0 = z * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
@@ -568,10 +595,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);  // the even CTA's barrier
           if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * kPairStage);
           const int k0 = kb * kBK;
-          tma_load_2d_pair(sA, &tmA, bar, m0, k0);
-          tma_load_2d_pair(sA + 8192, &tmA, bar, m0 + 64, k0);
-          tma_load_2d_pair(sB, &tmB, bar, nb, k0);
-          tma_load_2d_pair(sB + 8192, &tmB, bar, nb + 64, k0);
+          // (boxes past G's or XL's 2r columns are zero-filled and still
+          // count their full bytes)
+          tma_load_2d_pair(sA, mA, bar, m0, k0);
+          tma_load_2d_pair(sA + 8192, mA, bar, m0 + 64, k0);
+          tma_load_2d_pair(sB, mB, bar, nb, k0);
+          tma_load_2d_pair(sB + 8192, mB, bar, nb + 64, k0);
         }
       }
     }
@@ -582,8 +611,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       int it = 0, local = 0;
       bool stop = false;
       for (int u = unit0; u < units && !stop; u += ustep, ++local) {
-        int m0, n0, z;
-        decode(u, m0, n0, z);
+        int m0, n0, z, kind;
+        decode(u, m0, n0, z, kind);
         const int kb0 = z * p.kb_per_split, kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         const int buf = local & 1;
         const uint32_t use = static_cast<uint32_t>(local >> 1);
@@ -616,14 +645,59 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const uint32_t acc_empty0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
     int local = 0;
     for (int u = unit0; u < units; u += ustep, ++local) {
-      int m0, n0, z;
-      decode(u, m0, n0, z);
+      int m0, n0, z, kind;
+      decode(u, m0, n0, z, kind);
       const int m = m0 + 32 * q + lane;
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       if (!mbar_wait(&acc_full[buf], use & 1, abort_flag, p.status)) break;
       tc_fence_after();
       const uint32_t trow = tmem + buf * kPairBN + (static_cast<uint32_t>(32 * q) << 16);
+      if (kind != 0) {
+        // Adapter gradients.  Columns (dRᵀ) or rows (dLᵀ) j < 2r are real;
+        // the lo half j >= r folds onto j - r.  fp32 adds into dR (r x out:
+        // lanes = consecutive weight rows) or dL (in x r: lanes = consecutive
+        // j of one input column).
+        const int r = p.fuse_r;
+        const int ncols = kind == 1 ? (2 * r + 31) / 32 * 32 : kPairBN;
+        const int jrow = static_cast<int>(rank) * kBM + 32 * q + lane;  // dLᵀ: j of this lane
+        const bool live = kind == 1 || static_cast<int>(rank) * kBM + 32 * q < 2 * r;
+        bool handed = false;
+        if (live) {
+          for (int c0 = 32 * half; c0 < ncols; c0 += 64) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(trow + c0, v);
+            tmem_ld_wait();
+            if (c0 + 64 >= ncols) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8 * buf);
+              handed = true;
+            }
+            if (kind == 1) {
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj) {
+                const int c = c0 + jj;
+                if (c < 2 * r) red_add_f32(p.dr + static_cast<size_t>(c < r ? c : c - r) * p.M + m,
+                                           __uint_as_float(v[jj]));
+              }
+            } else if (jrow < 2 * r) {
+              const int jf = jrow < r ? jrow : jrow - r;
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj) {
+                const int i = n0 + c0 + jj;
+                if (i < p.N) red_add_f32(p.dl + static_cast<size_t>(i) * r + jf, __uint_as_float(v[jj]));
+              }
+            }
+          }
+        }
+        if (!handed) {  // nothing of this tile for this warp: hand the buffer back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8 * buf);
+        }
+        continue;
+      }
       uint4 mrow[2];
       {
         const uint4* mp = reinterpret_cast<const uint4*>(p.meta + static_cast<size_t>(m) * (p.N / 8) + n0 / 8);
@@ -688,12 +762,22 @@ cudaError_t run_dw_pair(const DenseGemmArgs& a, cudaStream_t stream) {
   CUtensorMap tA, tB;  // dY (K x M) and X (K x N), both MN-major, 64 x 64 boxes
   bool ok = make_tmap_2d(&tA, a.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, 2 * a.lda, 64, kBK, Swz::B128) &&
             make_tmap_2d(&tB, a.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, 2 * a.ldb, 64, kBK, Swz::B128);
+  const int fr = a.fuse_r;
+  CUtensorMap tG, tXL;  // G and XL (K x 2r), MN-major, 64 x 64 boxes (past 2r: zeros)
+  if (fr > 0) {
+    ok = ok &&
+         make_tmap_2d(&tG, a.g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2 * fr, K, 4 * fr, 64, kBK, Swz::B128) &&
+         make_tmap_2d(&tXL, a.xl, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2 * fr, K, 4 * fr, 64, kBK, Swz::B128);
+  } else {
+    tG = tA;  // unused
+    tXL = tB;
+  }
   if (!ok) return cudaErrorInvalidValue;
   const int num_kb = static_cast<int>((K + kBK - 1) / kBK);
   const int tiles_m = static_cast<int>(M / kBM);  // even
   const int tiles_n = static_cast<int>((N + kPairBN - 1) / kPairBN);
   const int clusters_max = max_clusters[dev].load();
-  const int pair_tiles = (tiles_m / 2) * tiles_n;
+  const int pair_tiles = (tiles_m / 2) * tiles_n + (fr > 0 ? tiles_m / 2 + tiles_n : 0);
   int splits = choose_splits(pair_tiles, clusters_max, num_kb);
   const int kbs = (num_kb + splits - 1) / splits;
   splits = (num_kb + kbs - 1) / kbs;
@@ -703,7 +787,10 @@ cudaError_t run_dw_pair(const DenseGemmArgs& a, cudaStream_t stream) {
   p.M = static_cast<int>(M); p.N = static_cast<int>(N); p.K = static_cast<int>(K);
   p.kb_per_split = kbs; p.num_kb = num_kb;
   p.tiles_m = tiles_m; p.tiles_n = tiles_n;
-  p.num_tiles = tiles_m * tiles_n * splits;
+  p.num_tiles = splits;  // the kernel's units: (dW + adapter tiles of one split) x splits
+  p.fuse_r = fr;
+  p.dl = a.dl;
+  p.dr = a.dr;
   {  // a band of X tiles (256 columns over the split's K range) of about 40 MB
     const double tile_bytes = 2.0 * kPairBN * kBK * kbs;
     int g = static_cast<int>(40.0e6 / tile_bytes);
@@ -717,13 +804,19 @@ cudaError_t run_dw_pair(const DenseGemmArgs& a, cudaStream_t stream) {
     if (cudaError_t e = cudaMemsetAsync(a.out, 0, static_cast<size_t>(M) * a.ldo * sizeof(float), stream))
       return e;
   }
+  if (fr > 0 && !a.accumulate) {  // the adapter gradients are always added atomically
+    if (cudaError_t e = cudaMemsetAsync(a.dl, 0, static_cast<size_t>(N) * fr * sizeof(float), stream))
+      return e;
+    if (cudaError_t e = cudaMemsetAsync(a.dr, 0, static_cast<size_t>(fr) * M * sizeof(float), stream))
+      return e;
+  }
   p.status = device_status_ptr();
   if (!p.status) return cudaErrorInvalidDevicePointer;
   const int units = pair_tiles * splits;
   const int clusters = units < clusters_max ? units : clusters_max;
   cfg.gridDim = dim3(2 * clusters);
   add_pdl_attr(cfg, attr);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, dw_pair_kernel, tA, tB, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, dw_pair_kernel, tA, tB, tG, tXL, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -780,7 +873,7 @@ cudaError_t run(const DenseGemmArgs& a, cudaStream_t stream) {
   const int kbs = csplit > 1 ? (num_kb + csplit - 1) / csplit : (num_kb + splits - 1) / splits;
   splits = csplit > 1 ? 1 : (num_kb + kbs - 1) / kbs;  // every split owns >= 1 K-block
 
-  DnParams p;
+  DnParams p = {};
   p.M = static_cast<int>(M); p.N = static_cast<int>(N); p.K = static_cast<int>(K);
   p.kb_per_split = kbs; p.num_kb = num_kb;
   p.ldo = a.ldo; p.out = a.out; p.meta = a.meta;

@@ -93,6 +93,14 @@ struct DenseGemmArgs {
   int splits;        // split-K factor; 0 chooses one from the grid size
   int lo_off;        // StoreBf16HiLo: column offset of the low parts (= r)
   int fold;          // AddF32*: columns n >= fold add into column n - fold (0: none)
+  // MaskedWeightGrad on CTA pairs may also compute the adapter gradients in
+  // the same launch (fuse_r > 0): dR += XLᵀ·dY and dL += Xᵀ·G, with XL and G
+  // T x 2r bf16 (hi | lo), dL in x r and dR r x out fp32, added into.
+  int fuse_r = 0;
+  const void* xl = nullptr;
+  const void* g = nullptr;
+  float* dl = nullptr;
+  float* dr = nullptr;
 };
 cudaError_t launch_dense_gemm(const DenseGemmArgs& a, cudaStream_t stream);
 

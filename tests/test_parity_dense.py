@@ -20,8 +20,12 @@ def S():
     return slope
 
 
+# An even number of 128-row weight tiles (out = 256, 512, 768, 1024) takes the
+# launch that computes dW, dL and dR together (2r up to 256); odd ones the
+# separate adapter-gradient GEMMs.
 @pytest.mark.parametrize("T,inp,out,r", [(64, 256, 256, 8), (200, 384, 512, 16), (1, 128, 128, 8),
-                                         (4096, 1024, 1024, 16), (1000, 640, 896, 64), (333, 256, 384, 24)])
+                                         (4096, 1024, 1024, 16), (1000, 640, 896, 64), (333, 256, 384, 24),
+                                         (777, 640, 1024, 64), (300, 512, 768, 120)])
 @pytest.mark.parametrize("dense", [False, True])
 def test_weight_and_adapter_grads(S, T, inp, out, r, dense):
     import torch
