@@ -166,36 +166,37 @@ __device__ __forceinline__ uint32_t top2_entry(uint32_t w01, uint32_t w23, const
   return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(out) + off);
 }
 
-// Work item: 8 consecutive rows (one "octet" h8) x 16 consecutive columns
-// (chunk c16) of the rows x cols pruned weight, given as each row's 16 B of
-// kept values v[k] and 16 bits of metadata m[k].  It expands each row's four
-// groups with byte permutes (pruned positions become +0) and, for each of
-// the 16 columns, prunes the two row-quadruples along the old row
-// dimension: 4 kept values (8 B) and one metadata byte for row i of the
-// transposed output, at column octet h8.  Lanes of a warp take consecutive
-// octets of the same chunk, so each output row segment a warp writes is
-// 256 B (values) / 32 B (metadata) contiguous.
-__device__ __forceinline__ void transpose_prune_octet(const uint4 (&v)[8], const uint32_t (&m)[8],
+// Work item: 8 consecutive rows (one "octet" h8) x 4·Q consecutive columns
+// (groups q0 .. q0 + Q - 1 of chunk c16) of the rows x cols pruned weight,
+// given as each row's kept-pair words pw[k][q] of those groups and its
+// metadata m[k] shifted so that group q0 is the low nibble.  It expands each
+// row's groups with byte permutes (pruned positions become +0) and, for each
+// column, prunes the two row-quadruples along the old row dimension: 4 kept
+// values (8 B) and one metadata byte for row i of the transposed output, at
+// column octet h8.  Lanes of a warp take consecutive octets of the same
+// chunk, so each output row segment a warp writes is 256 B (values) / 32 B
+// (metadata) contiguous.
+template <int Q>
+__device__ __forceinline__ void transpose_prune_octet(const uint32_t (&pw)[8][Q], const uint32_t (&m)[8],
                                                       const DpTables& tab,
                                                       uint2* __restrict__ t_vals,
                                                       uint8_t* __restrict__ t_meta,
                                                       int64_t out_stride, uint32_t h8,
-                                                      uint32_t c16, uint32_t k17) {
+                                                      uint32_t c16, uint32_t k17, int q0) {
   const uint32_t k1 = k17 >> 16, k8 = k17 >> 14;
-  uint2* tv = t_vals + 16 * static_cast<int64_t>(c16) * out_stride + h8;
-  uint8_t* tm = t_meta + 16 * static_cast<int64_t>(c16) * out_stride + h8;
+  uint2* tv = t_vals + (16 * static_cast<int64_t>(c16) + 4 * q0) * out_stride + h8;
+  uint8_t* tm = t_meta + (16 * static_cast<int64_t>(c16) + 4 * q0) * out_stride + h8;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {  // group of 4 columns within the chunk
+  for (int q = 0; q < Q; ++q) {  // group of 4 columns
     uint32_t e0[8], e1[8];        // row k, columns 0-1 / 2-3 of the group
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const uint32_t pair = (q == 0) ? v[k].x : (q == 1) ? v[k].y : (q == 2) ? v[k].z : v[k].w;
       // byte offset 8·nibble: the shift comes from a multiply-high, whose
       // +1 term only adds below bit 3
       const uint32_t m8 = (q == 0) ? m[k] * k8 : __umulhi(m[k], (1u << (35 - 4 * q)) + 1u);
       const uint2 sel = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(tab.expand) + (m8 & 0x78u));
-      e0[k] = __byte_perm(pair, 0u, sel.x);
-      e1[k] = __byte_perm(pair, 0u, sel.y);
+      e0[k] = __byte_perm(pw[k][q], 0u, sel.x);
+      e1[k] = __byte_perm(pw[k][q], 0u, sel.y);
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -231,15 +232,16 @@ __global__ void __launch_bounds__(kDpThreads) double_prune24_kernel(
     const uint32_t h8 = (tile % tiles_h) * 32 + lane;
     const uint32_t c16 = (tile / tiles_h) * 8 + warp;
     if (h8 >= n_h8 || c16 >= n_c16) continue;
-    uint4 v[8];
+    uint32_t pw[8][4];
     uint32_t m[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int64_t at = (static_cast<int64_t>(8) * h8 + k) * n_c16 + c16;
-      v[k] = __ldg(vals + at);
+      const uint4 v = __ldg(vals + at);
+      pw[k][0] = v.x; pw[k][1] = v.y; pw[k][2] = v.z; pw[k][3] = v.w;
       m[k] = __ldg(meta + at);
     }
-    transpose_prune_octet(v, m, tab, t_vals, t_meta, rows / 8, h8, c16, k17);
+    transpose_prune_octet<4>(pw, m, tab, t_vals, t_meta, rows / 8, h8, c16, k17, 0);
   }
 }
 
@@ -255,9 +257,11 @@ __global__ void __launch_bounds__(kDpThreads) double_prune24_kernel(
 template <int CH>
 __device__ __forceinline__ uint32_t swz(uint32_t o) { return (o / (8 / CH)) % CH; }
 
-template <int CH>
+// QS threads share an octet and chunk, each taking 4 / QS groups of 4
+// columns: for small weights (narrow tiles), shorter per-thread work.
+template <int CH, int QS = 1>
 struct DpStaged {
-  static constexpr int kThreads = 32 * CH;
+  static constexpr int kThreads = 32 * CH * QS;
   static constexpr int kValPitch = 16 * CH;
   static constexpr int kValPlane = 32 * kValPitch;
   static constexpr int kValBytes = 8 * kValPlane;
@@ -272,18 +276,20 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
 
-template <int CH>
-__global__ void __launch_bounds__(32 * CH) double_prune24_staged_kernel(
+template <int CH, int QS>
+__global__ void __launch_bounds__(32 * CH * QS) double_prune24_staged_kernel(
     const uint8_t* __restrict__ vals, const uint8_t* __restrict__ meta, uint2* __restrict__ t_vals,
     uint8_t* __restrict__ t_meta, int64_t rows, int64_t cols, uint32_t k17) {
-  using C = DpStaged<CH>;
+  using C = DpStaged<CH, QS>;
+  constexpr int kQ = 4 / QS;  // groups of 4 columns per thread
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ DpTables tab;
   fill_tables(tab);
   const uint32_t n_h8 = static_cast<uint32_t>(rows / 8);
   const uint32_t tiles_h = (static_cast<uint32_t>(rows) + 255) / 256;
   const uint32_t tiles_c = static_cast<uint32_t>(cols / (16 * CH));
-  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31, warp = (threadIdx.x >> 5) % CH;  // warp: the chunk
+  const int q0 = static_cast<int>(threadIdx.x >> 5) / CH * kQ;               // first column group
   const int64_t val_pitch = cols, meta_pitch = cols / 8;  // bytes per input row
   const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
 
@@ -291,7 +297,7 @@ __global__ void __launch_bounds__(32 * CH) double_prune24_staged_kernel(
     const uint32_t row0 = th * 256, ch0 = tc * CH;
     const uint32_t st = sbase + stage * C::kStage;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {  // 256 rows x CH chunks of 16 B values
+    for (int i = 0; i < 8 / QS; ++i) {  // 256 rows x CH chunks of 16 B values
       const uint32_t u = threadIdx.x + i * C::kThreads;
       const uint32_t r = u / CH, c = u % CH;
       if (row0 + r < rows)
@@ -334,15 +340,22 @@ __global__ void __launch_bounds__(32 * CH) double_prune24_staged_kernel(
       const uint8_t* st = smem + stage * C::kStage;
       // offset of this tile's metadata inside the 16 B piece that was copied
       const uint32_t moff = static_cast<uint32_t>((2 * ch0) & 15);
-      uint4 v[8];
+      uint32_t pw[8][kQ];
       uint32_t m[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        v[k] = *reinterpret_cast<const uint4*>(st + k * C::kValPlane + lane * C::kValPitch +
-                                               16 * (warp ^ swz<CH>(lane)));
-        m[k] = *reinterpret_cast<const uint16_t*>(st + C::kValBytes + k * 512 + lane * 16 + moff + 2 * warp);
+        const uint8_t* row = st + k * C::kValPlane + lane * C::kValPitch + 16 * (warp ^ swz<CH>(lane));
+        if constexpr (kQ == 4) {
+          const uint4 v = *reinterpret_cast<const uint4*>(row);
+          pw[k][0] = v.x; pw[k][1] = v.y; pw[k][2] = v.z; pw[k][3] = v.w;
+        } else {
+#pragma unroll
+          for (int q = 0; q < kQ; ++q) pw[k][q] = *reinterpret_cast<const uint32_t*>(row + 4 * (q0 + q));
+        }
+        m[k] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(st + C::kValBytes + k * 512 +
+                                                                          lane * 16 + moff + 2 * warp)) >> (4 * q0);
       }
-      transpose_prune_octet(v, m, tab, t_vals, t_meta, rows / 8, h8, ch0 + warp, k17);
+      transpose_prune_octet<kQ>(pw, m, tab, t_vals, t_meta, rows / 8, h8, ch0 + warp, k17, q0);
     }
     __syncthreads();
     th = nh;
@@ -356,8 +369,9 @@ cudaError_t launch_prune24(const void* W, int64_t rows, int64_t cols, void* vals
                            cudaStream_t stream) {
   const int64_t nchunks = rows * cols / 8;
   if (nchunks == 0) return cudaSuccess;
-  const int64_t per_block = static_cast<int64_t>(kPruneThreads) * kPruneUnroll;
-  int64_t blocks = (nchunks + per_block - 1) / per_block;
+  // one chunk per thread while the grid stays under 8 blocks per SM (short
+  // latency for small weights); beyond that, up to kPruneUnroll per thread
+  int64_t blocks = (nchunks + kPruneThreads - 1) / kPruneThreads;
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
   if (blocks > cap) blocks = cap;
   cudaLaunchConfig_t cfg = {};
@@ -373,11 +387,11 @@ cudaError_t launch_prune24(const void* W, int64_t rows, int64_t cols, void* vals
 
 constexpr uint32_t kKeyShift = 1u << 17;  // the k17 argument of the A2 kernels
 
-template <int CH>
+template <int CH, int QS>
 static cudaError_t run_staged(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols,
                               void* t_vals, uint8_t* t_meta, cudaStream_t stream) {
-  using C = DpStaged<CH>;
-  auto kernel = double_prune24_staged_kernel<CH>;
+  using C = DpStaged<CH, QS>;
+  auto kernel = double_prune24_staged_kernel<CH, QS>;
   static std::atomic<int> per_sm[64];
   int dev = 0;
   cudaGetDevice(&dev);
@@ -413,11 +427,12 @@ cudaError_t launch_double_prune24(const void* vals, const uint8_t* meta, int64_t
   if (cols % 128 == 0) {
     // the widest tile that still gives every SM a tile
     const int64_t tiles_h = (rows + 255) / 256;
+    // (narrower tiles split each octet's columns over more threads)
     if (tiles_h * (cols / 128) >= sm_count())
-      return run_staged<8>(vals, meta, rows, cols, t_vals, t_meta, stream);
+      return run_staged<8, 1>(vals, meta, rows, cols, t_vals, t_meta, stream);
     if (tiles_h * (cols / 64) >= sm_count())
-      return run_staged<4>(vals, meta, rows, cols, t_vals, t_meta, stream);
-    return run_staged<2>(vals, meta, rows, cols, t_vals, t_meta, stream);
+      return run_staged<4, 2>(vals, meta, rows, cols, t_vals, t_meta, stream);
+    return run_staged<2, 4>(vals, meta, rows, cols, t_vals, t_meta, stream);
   }
   const int64_t tiles = ((rows / 8 + 31) / 32) * ((cols / 16 + 7) / 8);
   int64_t blocks = tiles;
