@@ -562,8 +562,9 @@ struct Sp2Cfg {
   static constexpr int META_COL = 2 * ACC_COLS;
   static constexpr int TMEM_NEED = META_COL + 16 * STAGES;
   static constexpr int TMEM_COLS = TMEM_NEED <= 256 ? 256 : 512;
-  // output staging for the TMA stores: 1 KB per epilogue warp
-  static constexpr int STG_BYTES = 1024;
+  // output staging for the TMA stores: two 1 KB buffers per epilogue warp,
+  // so one store can read its buffer while the next is filled
+  static constexpr int STG_BYTES = 2048;
   static constexpr int SMEM = STAGES * STAGE + 1024 /*barriers*/ + kEpiWarps * STG_BYTES +
                               1024 /*align slack*/;
   static_assert(STAGE % 1024 == 0 && (HB * 128) % 1024 == 0, "1024-byte aligned atoms");
@@ -765,9 +766,11 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     const int q = warp & 3;
     const int half = warp >= 14 ? 1 : 0;
     const uint32_t acc_empty0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
-    // this warp's 1 KB staging buffer: [token][32 weight rows] of the output,
-    // 16 tokens (bf16) or 8 (fp32) at a time, written out by a TMA store
-    uint8_t* stg = smem + C::STAGES * C::STAGE + 1024 + (q + 4 * half) * C::STG_BYTES;
+    // this warp's two 1 KB staging buffers: [token][32 weight rows] of the
+    // output, 16 tokens (bf16) or 8 (fp32) at a time, each written out by a
+    // TMA store; they alternate, so a store overlaps the next buffer's fill
+    uint8_t* stg0 = smem + C::STAGES * C::STAGE + 1024 + (q + 4 * half) * C::STG_BYTES;
+    int nstore = 0;
     int local = 0;
     for (int u = unit0; u < units; u += ustep, ++local) {
       int m0, n0;
@@ -788,35 +791,35 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8 * buf);
         }
         // stage 16 tokens (bf16) or 8 (fp32) at a time and store them
-        auto flush = [&](int t0) {
+        auto buffer = [&]() {  // the next buffer, once the store that last used it has read it
+          if (lane == 0) bulk_wait_read_but_one();
+          __syncwarp();
+          return stg0 + (nstore & 1) * 1024;
+        };
+        auto flush = [&](uint8_t* stg, int t0) {
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
             tma_store_2d(&tmOut, stg, m0 + 32 * q, n0 + c0 + t0);  // tokens past N are clipped
             bulk_commit();
           }
-        };
-        auto reuse = [&]() {  // the warp's previous store has read the buffer
-          if (lane == 0) bulk_wait_read_all();
-          __syncwarp();
+          ++nstore;
         };
         if (p.out_bf16) {
-          __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stg);
 #pragma unroll
           for (int g = 0; g < 32; g += 16) {
-            reuse();
+            __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(buffer());
 #pragma unroll
             for (int j = 0; j < 16; ++j) sb[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[g + j]));
-            flush(g);
+            flush(reinterpret_cast<uint8_t*>(sb), g);
           }
         } else {
-          float* sf = reinterpret_cast<float*>(stg);
 #pragma unroll
           for (int g = 0; g < 32; g += 8) {
-            reuse();
+            float* sf = reinterpret_cast<float*>(buffer());
 #pragma unroll
             for (int j = 0; j < 8; ++j) sf[j * 32 + lane] = __uint_as_float(v[g + j]);
-            flush(g);
+            flush(reinterpret_cast<uint8_t*>(sf), g);
           }
         }
       }
