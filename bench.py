@@ -126,19 +126,101 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
+class NvmlClockSampler:
+    """Polls the SM clock and the clock-event reasons through NVML (the
+    driver's libnvidia-ml, loaded with ctypes) about every millisecond from a
+    background thread, so that even a timed region of a few milliseconds
+    gets samples.  Reads only; changes no setting."""
+
+    # clock-event reason bits of nvmlDeviceGetCurrentClocksEventReasons
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, device):
+        import ctypes
+        import threading
+
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.handle = ctypes.c_void_p()
+        import torch
+
+        props = torch.cuda.get_device_properties(device)
+        ok = False
+        uuid = str(getattr(props, "uuid", ""))
+        for u in (uuid, "GPU-" + uuid):
+            if u and self.lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(self.handle)) == 0:
+                ok = True
+                break
+        if not ok and hasattr(props, "pci_bus_id"):
+            bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+            ok = self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.handle)) == 0
+        if not ok:
+            self.lib.nvmlShutdown()
+            raise RuntimeError("no NVML handle for this device")
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn if fn is not None else self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.max_mhz = (float(mx.value) if self.lib.nvmlDeviceGetMaxClockInfo(
+            self.handle, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0 else None)
+        self.samples = []
+        self.stop = threading.Event()
+        self.thread = threading.Thread(target=self._poll, daemon=True)
+
+    def _poll(self):
+        ct = self.ct
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        while not self.stop.is_set():
+            if (self.lib.nvmlDeviceGetClockInfo(self.handle, self.NVML_CLOCK_SM, ct.byref(clk)) == 0
+                    and self.reasons_fn(self.handle, ct.byref(rs)) == 0):
+                self.samples.append((float(clk.value), int(rs.value)))
+            self.stop.wait(0.001)
+
+    def __enter__(self):
+        self.thread.start()
+        while not self.samples and self.thread.is_alive():  # running before the region starts
+            time.sleep(0.0005)
+        self.samples.clear()
+        return self
+
+    def __exit__(self, *exc):
+        self.stop.set()
+        self.thread.join(timeout=5)
+        self.lib.nvmlShutdown()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"], "samples": 0}
+        reasons = sorted({n for _, r in self.samples for bit, n in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "sm_min_mhz": min(c for c, _ in self.samples), "reasons": reasons,
+                "samples": len(self.samples), "source": "nvml, 1 ms polling"}
+
+
+def clock_sampler(device, index):
+    try:
+        return NvmlClockSampler(device)
+    except Exception:
+        return ClockSampler(index)
+
+
 # ------------------------------------------------------------- GPU arm ----
 
 
 class BlockStep:
     """Device buffers and the ordered ABI calls of one block step."""
 
-    def __init__(self, wl, seed: int, device):
+    def __init__(self, wl, seed: int, device, fused_prune: bool = False):
         import torch
 
         from sparse_rank_adapter_gb300 import slope
 
         self.S = slope
         self.wl = wl
+        self.fused_prune = fused_prune
         T, r = wl.tokens, wl.rank
         self.layers = []
         for li, lin in enumerate(wl.linears):
@@ -189,11 +271,17 @@ class BlockStep:
         pre-compressed weights."""
         S = self.S
         for b in (self.layers if only is None else [self.layers[only]]):
-            calls = [] if self.wl.forward_only else [
-                ("prune", lambda b=b: S.slope_prune_nm(b["W"], b["Wv"], b["Wm"], stream=stream)),
-                ("double_prune", lambda b=b: S.slope_double_prune(b["Wv"], b["Wm"], b["out"], b["inp"],
-                                                                  b["Dv"], b["Dm"], stream=stream)),
-            ]
+            if self.wl.forward_only:
+                calls = []
+            elif self.fused_prune:  # A1 and A2 from one read of W
+                calls = [("prune_double", lambda b=b: S.slope_prune_and_double_prune(
+                    b["W"], b["Wv"], b["Wm"], b["Dv"], b["Dm"], stream=stream))]
+            else:
+                calls = [
+                    ("prune", lambda b=b: S.slope_prune_nm(b["W"], b["Wv"], b["Wm"], stream=stream)),
+                    ("double_prune", lambda b=b: S.slope_double_prune(b["Wv"], b["Wm"], b["out"], b["inp"],
+                                                                      b["Dv"], b["Dm"], stream=stream)),
+                ]
             calls += [
                 ("fwd", lambda b=b: S.slope_linear_fwd(b["X"], b["Wv"], b["Wm"], b["L"], b["R"], b["Y"],
                                                        b["XL"], stream=stream)),
@@ -220,7 +308,7 @@ class BlockStep:
     def launches_per_step(self):
         n = 0
         for _ in self.layers:
-            n += 0 if self.wl.forward_only else 2  # prune, double prune
+            n += 0 if self.wl.forward_only else (1 if self.fused_prune else 2)  # prune, double prune
             n += 2 if self.wl.rank else 1  # fwd: (XL) + sparse
             if not self.wl.forward_only:
                 n += 2 if self.wl.rank else 1  # bwd_input: (G) + sparse
@@ -264,6 +352,8 @@ def call_bytes(name, T, inp, out, r):
         return out * inp * (2 + 1 + 0.125)
     if name == "double_prune":
         return out * inp * (1.125 + 1.125)
+    if name == "prune_double":  # W in once; both compressed formats out
+        return out * inp * (2 + 1.125 + 1.125)
     return 0.0
 
 
@@ -287,7 +377,7 @@ def gpu_arm(args):
     wl = synth.WORKLOADS[args.workload]
     stream = torch.cuda.Stream(device=dev)
     n_sets = max(1, args.sets)
-    sets = [BlockStep(wl, seed=s + 10 * rank, device=dev) for s in range(n_sets)]
+    sets = [BlockStep(wl, seed=s + 10 * rank, device=dev, fused_prune=args.fused_prune) for s in range(n_sets)]
     torch.cuda.synchronize()
 
     with torch.cuda.stream(stream):
@@ -326,7 +416,7 @@ def gpu_arm(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with clock_sampler(dev, local) as clk:  # samples the timed region only
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
@@ -337,14 +427,15 @@ def gpu_arm(args):
                 else:
                     sets[i % n_sets].run(stream)
         t_end.record(stream)
-        # per-call breakdown: one marked pass over every input set
-        with torch.cuda.stream(stream):
-            for i in range(n_sets):
-                if args.graph:
-                    mgraphs[i].replay()
-                else:
-                    sets[i].run(stream, marks[i])
-        stream.synchronize()
+        t_end.synchronize()
+    # per-call breakdown: one marked pass over every input set
+    with torch.cuda.stream(stream):
+        for i in range(n_sets):
+            if args.graph:
+                mgraphs[i].replay()
+            else:
+                sets[i].run(stream, marks[i])
+    stream.synchronize()
     if world > 1:
         dist.barrier()
     for m in marks:
@@ -369,7 +460,7 @@ def gpu_arm(args):
         byts = sum(fwd_bytes(T, i, o, r) for i, o, _ in per_call[dom]) / n_obs
         ach = byts / (calls_ms[dom] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm}
-    elif dom in ("prune", "double_prune"):
+    elif dom in ("prune", "double_prune", "prune_double"):
         alg = sum(call_bytes(dom, T, i, o, r) for i, o, _ in per_call[dom]) / n_obs
         ach = alg / (calls_ms[dom] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm}
@@ -380,7 +471,8 @@ def gpu_arm(args):
         roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak}
     kernel_of = {"prune": "prune24_kernel (slope_prune_nm)", "double_prune": "double_prune24_kernel (slope_double_prune)",
                  "fwd": "slope_linear_fwd (XL GEMM + sparse GEMM)", "bwd_input": "slope_linear_bwd_input (G GEMM + sparse GEMM)",
-                 "bwd_weight": "dW GEMM with dL, dR (slope_linear_bwd_weight)"}
+                 "bwd_weight": "dW GEMM with dL, dR (slope_linear_bwd_weight)",
+                 "prune_double": "prune_double24_kernel (slope_prune_and_double_prune)"}
     roof.update({"kernel": kernel_of.get(dom, dom), "traffic": None,
                  "peak_source": f"{src} ({'2x ' if dom in ('fwd', 'bwd_input') else ''}bf16 sustained)"
                  if roof['bound'] == 'tensor' else f"{src} hbm",
@@ -403,7 +495,8 @@ def gpu_arm(args):
                        "outputs": "Y, dX bf16; dW (compressed), dL, dR fp32",
                        "linears": [f"{x.name}:{x.inp}->{x.out}" for x in wl.linears],
                        "l2": f"{n_sets} rotating input sets of {set_bytes(sets[0]) / 2**20:.0f} MiB (> L2 {L2_BYTES // 2**20} MiB)",
-                       "graph": bool(args.graph), "parallelism": f"replicas x{world}"},
+                       "graph": bool(args.graph), "parallelism": f"replicas x{world}",
+                       "prune": "one call (A1 + A2)" if args.fused_prune else "two calls (A1, A2)"},
             "pct_of_sparse_peak": round(100 * value / (2 * bf16), 2),
             "composite_roofline_frac": composite_frac(wl, ms_step, bf16_sus),
             "calls_ms_per_step": {k: round(v, 4) for k, v in calls_ms.items()},
@@ -594,6 +687,8 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--fused-prune", action="store_true",
+                    help="A1 and A2 through the one-call slope_prune_and_double_prune")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

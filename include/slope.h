@@ -113,6 +113,21 @@ int slope_double_prune(const void* vals, const uint8_t* meta, int64_t rows, int6
                        void* t_vals, uint8_t* t_meta, void* stream);
 
 /*
+ * A1 + A2 in one call (§2.3: both compressed copies are made from the same
+ * weight; one read of W serves both).  Writes exactly what slope_prune_nm
+ * followed by slope_double_prune on its output would write: (vals, meta) of
+ * the pruned rows x cols weight and (t_vals, t_meta) of D = P(Wsᵀ), in the
+ * layouts of those two calls.  The four outputs must not overlap W or each
+ * other.  Requires n == 2 and m == 4 (else SLOPE_ERR_UNSUPPORTED),
+ * rows % 8 == 0 and cols % 16 == 0 with both positive (else SLOPE_ERR_SHAPE).
+ * Widths with cols % 128 == 0 run as one kernel; other widths run the two
+ * kernels of the separate calls.
+ */
+int slope_prune_and_double_prune(const void* W, int64_t rows, int64_t cols, int n, int m,
+                                 void* vals, uint8_t* meta, void* t_vals, uint8_t* t_meta,
+                                 void* stream);
+
+/*
  * A3 — sparse forward with the fused adapter (§2.1, §2.2, §2.4, App. D):
  *     Y  = X·Wsᵀ + (X·L)·R          (bf16 inputs, fp32 accumulation)
  *     XL = X·L                        (kept for the backward)

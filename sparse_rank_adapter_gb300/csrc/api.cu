@@ -255,6 +255,20 @@ extern "C" int slope_double_prune(const void* vals, const uint8_t* meta, int64_t
                                          static_cast<cudaStream_t>(stream)));
 }
 
+extern "C" int slope_prune_and_double_prune(const void* W, int64_t rows, int64_t cols, int n,
+                                            int m, void* vals, uint8_t* meta, void* t_vals,
+                                            uint8_t* t_meta, void* stream) {
+  if (n != 2 || m != 4) return SLOPE_ERR_UNSUPPORTED;
+  if (rows <= 0 || cols <= 0 || rows % 8 != 0 || cols % 16 != 0) return SLOPE_ERR_SHAPE;
+  if (!W || !vals || !meta || !t_vals || !t_meta) return SLOPE_ERR_INVALID_ARG;
+  if (!aligned16(W) || !aligned16(vals) || !aligned16(meta) || !aligned16(t_vals) ||
+      !aligned16(t_meta))
+    return SLOPE_ERR_ALIGNMENT;
+  if (int s = check_device()) return s;
+  return from_cuda(launch_prune_double24(W, rows, cols, vals, meta, t_vals, t_meta,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 // Shared size rules of the three GEMM calls.
 static int check_linear(int64_t T, int64_t in, int64_t out, int r) {
   if (T < 0 || in <= 0 || out <= 0 || in % 128 != 0 || out % 128 != 0) return SLOPE_ERR_SHAPE;

@@ -7,6 +7,7 @@
 //                             kernel (cols % 128 == 0) moves its tiles
 //                             through shared memory, the other reads global
 //                             memory directly and takes any legal shape.
+//   prune_double24_kernel     A1 and A2 from one read of W (cols % 128 == 0).
 //
 // Source: "SLoPe: Double-Pruned Sparse Plus Lazy Low-Rank Adapter Pretraining
 // of LLMs", §1 and §2.1 (N:M pruning of the weight, then of its transpose)
@@ -363,6 +364,120 @@ __global__ void __launch_bounds__(32 * CH * QS) double_prune24_staged_kernel(
   }
 }
 
+// ------------------------------------------------------------ A1 + A2 ------
+// Both compressed formats from one read of W.  Tiles and shared-memory layout
+// are the staged A2 kernel's (256 rows x 16·CH columns).  Phase 1: lanes take
+// consecutive 16 B chunks (8 weights = 2 groups) of the tile's rows straight
+// from global memory, so loads and the A1 stores are coalesced.  A row group
+// of four bf16 is two words with two entries each, the same layout as a
+// transposed group, so top2_entry ranks it too (magnitude key, lower column
+// on ties).  The kept pairs and nibbles go to global memory (A1's output) and
+// into shared memory where the staged kernel's copies would have put them.
+// Phase 2 is the staged kernel's compute step on that tile.  Two buffers:
+// phase 1 of the next tile fills one while no thread can still be reading it
+// (every thread passed the barrier after its phase 2 of the tile before).
+
+template <int CH, int QS>
+__global__ void __launch_bounds__(32 * CH * QS, 3) prune_double24_kernel(
+    const uint4* __restrict__ W, uint2* __restrict__ vals, uint8_t* __restrict__ meta,
+    uint2* __restrict__ t_vals, uint8_t* __restrict__ t_meta, int64_t rows, int64_t cols,
+    uint32_t k17) {
+  using C = DpStaged<CH, QS>;
+  constexpr int kQ = 4 / QS;                     // groups of 4 columns per thread in phase 2
+  constexpr int kRowChunks = 2 * CH;             // 8-column chunks per tile row
+  constexpr int kItems = 256 * kRowChunks / C::kThreads;  // chunks per thread in phase 1
+  static_assert(kItems % 4 == 0, "phase 1 loads in batches of four");
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ DpTables tab;
+  fill_tables(tab);
+  __syncthreads();
+  const uint32_t k1 = k17 >> 16;
+  const uint32_t n_h8 = static_cast<uint32_t>(rows / 8);
+  const uint32_t tiles_h = (static_cast<uint32_t>(rows) + 255) / 256;
+  const uint32_t tiles_c = static_cast<uint32_t>(cols / (16 * CH));
+  const uint32_t lane = threadIdx.x & 31, warp = (threadIdx.x >> 5) % CH;
+  const int q0 = static_cast<int>(threadIdx.x >> 5) / CH * kQ;
+  const int64_t row_chunks = cols / 8;  // 8-column chunks per row of W
+  const uint32_t step_c = gridDim.x / tiles_h, step_h = gridDim.x % tiles_h;
+  uint32_t th = blockIdx.x % tiles_h, tc = blockIdx.x / tiles_h;
+  grid_dependency_wait();
+  allow_dependents_launch();
+  for (int stage = 0; tc < tiles_c; stage ^= 1) {
+    uint8_t* st = smem + stage * C::kStage;
+    const uint32_t row0 = th * 256;
+    const int64_t chunk0 = static_cast<int64_t>(tc) * kRowChunks;
+#pragma unroll
+    for (int b = 0; b < kItems; b += 4) {
+      uint4 w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t i = threadIdx.x + (b + u) * C::kThreads;
+        const uint32_t r = i / kRowChunks, cc = i % kRowChunks;
+        if (row0 + r < rows) w[u] = __ldcs(W + (row0 + r) * row_chunks + chunk0 + cc);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t i = threadIdx.x + (b + u) * C::kThreads;
+        const uint32_t r = i / kRowChunks, cc = i % kRowChunks;
+        if (row0 + r < rows) {
+          const uint32_t ea = top2_entry(w[u].x, w[u].y, tab.out[0], k17, k1);
+          const uint32_t eb = top2_entry(w[u].z, w[u].w, tab.out[1], k17, k1);
+          const uint2 kept = make_uint2(__byte_perm(w[u].x, w[u].y, ea), __byte_perm(w[u].z, w[u].w, eb));
+          const uint8_t nib = static_cast<uint8_t>((ea + eb) >> 16);
+          const int64_t at = (row0 + r) * row_chunks + chunk0 + cc;
+          __stcs(vals + at, kept);
+          meta[at] = nib;
+          const uint32_t o = r >> 3, c = cc >> 1, h = cc & 1;
+          *reinterpret_cast<uint2*>(st + (r & 7) * C::kValPlane + o * C::kValPitch +
+                                    16 * (c ^ swz<CH>(o)) + 8 * h) = kept;
+          st[C::kValBytes + (r & 7) * 512 + o * 16 + 2 * c + h] = nib;
+        }
+      }
+    }
+    __syncthreads();
+    const uint32_t h8 = th * 32 + lane;
+    if (h8 < n_h8) {
+      uint32_t pw[8][kQ];
+      uint32_t m[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint8_t* row = st + k * C::kValPlane + lane * C::kValPitch + 16 * (warp ^ swz<CH>(lane));
+        if constexpr (kQ == 4) {
+          const uint4 v = *reinterpret_cast<const uint4*>(row);
+          pw[k][0] = v.x; pw[k][1] = v.y; pw[k][2] = v.z; pw[k][3] = v.w;
+        } else {
+#pragma unroll
+          for (int q = 0; q < kQ; ++q) pw[k][q] = *reinterpret_cast<const uint32_t*>(row + 4 * (q0 + q));
+        }
+        m[k] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(st + C::kValBytes + k * 512 +
+                                                                          lane * 16 + 2 * warp)) >> (4 * q0);
+      }
+      transpose_prune_octet<kQ>(pw, m, tab, t_vals, t_meta, rows / 8, h8, tc * CH + warp, k17, q0);
+    }
+    th += step_h;
+    tc += step_c;
+    if (th >= tiles_h) { th -= tiles_h; ++tc; }
+  }
+}
+
+// Blocks per SM of a persistent kernel at its launch shape, cached per device.
+template <typename Kernel>
+static cudaError_t blocks_per_sm(Kernel kernel, int threads, int smem, std::atomic<int> (&cache)[64],
+                                 int& out) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  out = cache[dev].load();
+  if (out) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&out, kernel, threads, smem);
+  if (e != cudaSuccess) return e;
+  if (out < 1) out = 1;
+  cache[dev].store(out);
+  return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_prune24(const void* W, int64_t rows, int64_t cols, void* vals, uint8_t* meta,
@@ -393,20 +508,10 @@ static cudaError_t run_staged(const void* vals, const uint8_t* meta, int64_t row
   using C = DpStaged<CH, QS>;
   auto kernel = double_prune24_staged_kernel<CH, QS>;
   static std::atomic<int> per_sm[64];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  int blocks_per_sm = per_sm[dev].load();
-  if (!blocks_per_sm) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kernel, C::kThreads, C::kSmem);
-    if (e != cudaSuccess) return e;
-    if (blocks_per_sm < 1) blocks_per_sm = 1;
-    per_sm[dev].store(blocks_per_sm);
-  }
+  int per = 0;
+  if (cudaError_t e = blocks_per_sm(kernel, C::kThreads, C::kSmem, per_sm, per)) return e;
   const int64_t tiles = ((rows + 255) / 256) * (cols / (16 * CH));
-  const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * per;
   const int64_t blocks = tiles < cap ? tiles : cap;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attrs[1];
@@ -418,6 +523,46 @@ static cudaError_t run_staged(const void* vals, const uint8_t* meta, int64_t row
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<const uint8_t*>(vals), meta,
                                      static_cast<uint2*>(t_vals), t_meta, rows, cols, kKeyShift);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int CH, int QS>
+static cudaError_t run_fused(const void* W, int64_t rows, int64_t cols, void* vals, uint8_t* meta,
+                             void* t_vals, uint8_t* t_meta, cudaStream_t stream) {
+  using C = DpStaged<CH, QS>;
+  auto kernel = prune_double24_kernel<CH, QS>;
+  static std::atomic<int> per_sm[64];
+  int per = 0;
+  if (cudaError_t e = blocks_per_sm(kernel, C::kThreads, C::kSmem, per_sm, per)) return e;
+  const int64_t tiles = ((rows + 255) / 256) * (cols / (16 * CH));
+  const int64_t cap = static_cast<int64_t>(sm_count()) * per;
+  const int64_t blocks = tiles < cap ? tiles : cap;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attrs[1];
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = stream;
+  add_pdl_attr(cfg, attrs);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<const uint4*>(W), static_cast<uint2*>(vals),
+                                     meta, static_cast<uint2*>(t_vals), t_meta, rows, cols, kKeyShift);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_prune_double24(const void* W, int64_t rows, int64_t cols, void* vals,
+                                  uint8_t* meta, void* t_vals, uint8_t* t_meta,
+                                  cudaStream_t stream) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  if (cols % 128 == 0) {  // tile widths as A2's staged kernel
+    const int64_t tiles_h = (rows + 255) / 256;
+    if (tiles_h * (cols / 128) >= sm_count())
+      return run_fused<8, 1>(W, rows, cols, vals, meta, t_vals, t_meta, stream);
+    if (tiles_h * (cols / 64) >= sm_count())
+      return run_fused<4, 2>(W, rows, cols, vals, meta, t_vals, t_meta, stream);
+    return run_fused<2, 4>(W, rows, cols, vals, meta, t_vals, t_meta, stream);
+  }
+  // other widths: the two kernels one after the other
+  if (cudaError_t e = launch_prune24(W, rows, cols, vals, meta, stream)) return e;
+  return launch_double_prune24(vals, meta, rows, cols, t_vals, t_meta, stream);
 }
 
 cudaError_t launch_double_prune24(const void* vals, const uint8_t* meta, int64_t rows,

@@ -41,6 +41,9 @@ cudaError_t launch_prune24(const void* W, int64_t rows, int64_t cols, void* vals
 cudaError_t launch_double_prune24(const void* vals, const uint8_t* meta, int64_t rows,
                                   int64_t cols, void* t_vals, uint8_t* t_meta,
                                   cudaStream_t stream);
+cudaError_t launch_prune_double24(const void* W, int64_t rows, int64_t cols, void* vals,
+                                  uint8_t* meta, void* t_vals, uint8_t* t_meta,
+                                  cudaStream_t stream);
 
 // ---- tensor-map encoding (api.cu): 2-D row-major tensor [outer][inner]
 // with `row_bytes` between rows, box [box_outer][box_inner], given swizzle.

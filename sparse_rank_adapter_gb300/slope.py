@@ -29,6 +29,7 @@ SIGNATURES = (
     ("slope_workspace_size", _sz, (_i64, _i64, _i64, _i)),
     ("slope_prune_nm", _i, (_vp, _i64, _i64, _i, _i, _vp, _vp, _vp)),
     ("slope_double_prune", _i, (_vp, _vp, _i64, _i64, _vp, _vp, _vp)),
+    ("slope_prune_and_double_prune", _i, (_vp, _i64, _i64, _i, _i, _vp, _vp, _vp, _vp, _vp)),
     ("slope_linear_fwd", _i, (_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _vp, _sz, _vp)),
     ("slope_linear_bwd_input", _i, (_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _vp, _sz, _vp)),
     ("slope_linear_bwd_weight", _i, (_vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _i, _vp, _u32, _vp, _vp, _vp, _sz, _vp)),
@@ -129,6 +130,21 @@ def slope_double_prune(vals, meta, rows: int, cols: int, t_vals, t_meta, stream=
         _ptr(t_vals, torch.bfloat16, (cols, rows // 2), "t_vals"),
         _ptr(t_meta, torch.uint8, (cols, rows // 8), "t_meta"), _stream(stream))
     _check(st, "slope_double_prune")
+
+
+def slope_prune_and_double_prune(W, vals, meta, t_vals, t_meta, n: int = 2, m: int = 4, stream=None):
+    """A1 and A2 in one call: (vals, meta) of the pruned W and (t_vals, t_meta)
+    of D = P(Wsᵀ), exactly as the two separate calls write them."""
+    import torch
+
+    rows, cols = W.shape
+    st = lib().slope_prune_and_double_prune(
+        _ptr(W, torch.bfloat16, name="W"), rows, cols, n, m,
+        _ptr(vals, torch.bfloat16, (rows, cols // 2), "vals"),
+        _ptr(meta, torch.uint8, (rows, cols // 8), "meta"),
+        _ptr(t_vals, torch.bfloat16, (cols, rows // 2), "t_vals"),
+        _ptr(t_meta, torch.uint8, (cols, rows // 8), "t_meta"), _stream(stream))
+    _check(st, "slope_prune_and_double_prune")
 
 
 def slope_linear_fwd(X, Wv, Wm, L, R, Y, XL=None, workspace=None, stream=None):

@@ -88,6 +88,17 @@ def test_double_prune_argument_checks(L):
 
 
 @cpu_only
+def test_prune_and_double_prune_argument_checks(L):
+    f = L.lib().slope_prune_and_double_prune
+    assert f(A, 16, 16, 1, 2, A, A, A, A, None) == L.ERR_UNSUPPORTED
+    assert f(A, 12, 16, 2, 4, A, A, A, A, None) == L.ERR_SHAPE  # rows % 8
+    assert f(A, 16, 24, 2, 4, A, A, A, A, None) == L.ERR_SHAPE  # cols % 16
+    assert f(A, 0, 16, 2, 4, A, A, A, A, None) == L.ERR_SHAPE
+    assert f(A, 16, 16, 2, 4, A, A, None, A, None) == L.ERR_INVALID_ARG
+    assert f(A, 16, 16, 2, 4, A, A, A, MIS, None) == L.ERR_ALIGNMENT
+
+
+@cpu_only
 def test_linear_argument_checks(L):
     fwd = L.lib().slope_linear_fwd
     bi = L.lib().slope_linear_bwd_input

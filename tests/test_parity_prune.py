@@ -1,7 +1,8 @@
-"""A1/A2 on the GPU against the CPU oracle: kept values and metadata must be
-bit-exact.  Small and ragged shapes in full; the block shapes of the
-measured workloads in full where the oracle is quick, sampled (rows for A1,
-column slabs for A2) at the largest sizes."""
+"""A1/A2 on the GPU against the CPU oracle, as two calls and as the one-call
+A1 + A2: kept values and metadata must be bit-exact.  Small and ragged
+shapes in full; the block shapes of the measured workloads in full where the
+oracle is quick, sampled (rows for A1, column slabs for A2) at the largest
+sizes."""
 
 import numpy as np
 import pytest
@@ -41,6 +42,28 @@ def gpu_double(S, vals, meta, rows, cols):
     return tv, tm
 
 
+def gpu_fused(S, W_bits):
+    import torch
+
+    rows, cols = W_bits.shape
+    W = to_dev(W_bits)
+    vals = torch.empty(rows, cols // 2, dtype=torch.bfloat16, device="cuda")
+    meta = torch.empty(rows, cols // 8, dtype=torch.uint8, device="cuda")
+    tv = torch.empty(cols, rows // 2, dtype=torch.bfloat16, device="cuda")
+    tm = torch.empty(cols, rows // 8, dtype=torch.uint8, device="cuda")
+    S.slope_prune_and_double_prune(W, vals, meta, tv, tm)
+    return vals, meta, tv, tm
+
+
+def check_fused(S, W, ov, om, otv, otm):
+    """The one-call A1 + A2 writes the oracle's four outputs bit for bit."""
+    vals, meta, tv, tm = gpu_fused(S, W)
+    np.testing.assert_array_equal(bits_of(vals), ov)
+    np.testing.assert_array_equal(meta.cpu().numpy(), om)
+    np.testing.assert_array_equal(bits_of(tv), otv)
+    np.testing.assert_array_equal(tm.cpu().numpy(), otm)
+
+
 # cols % 128 == 0 takes the shared-memory staged A2 kernel (32-, 64- or
 # 128-column tiles by size), other widths the direct one; 520 and 2312 rows
 # leave a ragged 256-row tile.
@@ -60,6 +83,7 @@ def test_prune_and_double_prune_bit_exact(S, rows, cols):
         otv, otm, _ = O.double_prune24(ov, om, rows, cols)
         np.testing.assert_array_equal(bits_of(tv), otv)
         np.testing.assert_array_equal(tm.cpu().numpy(), otm)
+        check_fused(S, W, ov, om, otv, otm)
 
 
 def tie_heavy(rows, cols, seed):
@@ -97,6 +121,7 @@ def test_edge_values_bit_exact(S, case):
         otv, otm, _ = O.double_prune24(ov, om, rows, cols)
         np.testing.assert_array_equal(bits_of(tv), otv)
         np.testing.assert_array_equal(tm.cpu().numpy(), otm)
+        check_fused(S, W, ov, om, otv, otm)
 
 
 def test_double_prune_of_arbitrary_compressed_input(S):
@@ -132,9 +157,14 @@ def test_block_shapes_sampled(S, rows, cols):
     """Full-size weights of the measured blocks, pruned on the GPU exactly as
     the benchmark does; the oracle checks sampled rows (A1) and sampled rows
     of the transposed result (A2)."""
+    import torch
+
     W = synth.normal_bf16(0, 4, "W", (rows, cols))
     vals, meta = gpu_prune(S, W)
     tv, tm = gpu_double(S, vals, meta, rows, cols)
+    # the one-call A1 + A2 writes the same four arrays in full
+    for a, b in zip(gpu_fused(S, W), (vals, meta, tv, tm)):
+        assert torch.equal(a, b)
     rng = np.random.default_rng(rows + cols)
     rs = np.unique(np.concatenate([[0, rows - 1], rng.choice(rows, 62, replace=False)]))
     ov, om, _ = O.prune24(W[rs])
