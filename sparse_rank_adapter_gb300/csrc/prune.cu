@@ -276,6 +276,7 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
 template <int CH, int QS>
 __global__ void __launch_bounds__(32 * CH * QS) double_prune24_staged_kernel(
@@ -365,32 +366,41 @@ __global__ void __launch_bounds__(32 * CH * QS) double_prune24_staged_kernel(
 }
 
 // ------------------------------------------------------------ A1 + A2 ------
-// Both compressed formats from one read of W.  Tiles and shared-memory layout
-// are the staged A2 kernel's (256 rows x 16·CH columns).  Phase 1: lanes take
-// consecutive 16 B chunks (8 weights = 2 groups) of the tile's rows straight
-// from global memory, so loads and the A1 stores are coalesced.  A row group
-// of four bf16 is two words with two entries each, the same layout as a
-// transposed group, so top2_entry ranks it too (magnitude key, lower column
-// on ties).  The kept pairs and nibbles go to global memory (A1's output) and
-// into shared memory where the staged kernel's copies would have put them.
-// Phase 2 is the staged kernel's compute step on that tile.  Two buffers:
-// phase 1 of the next tile fills one while no thread can still be reading it
-// (every thread passed the barrier after its phase 2 of the tile before).
+// Both compressed formats from one read of W.  Tiles and the compressed
+// shared-memory layout are the staged A2 kernel's (256 rows x 16·CH
+// columns).  The tile's rows of W are copied into shared memory with
+// cp.async (row-major, 32·CH bytes a row); the copy of the next tile runs
+// while the current one is double-pruned.  Phase 1: lanes take consecutive
+// 16 B chunks (8 weights = 2 groups) of a row.  A row group of four bf16 is
+// two words with two entries each, the same layout as a transposed group,
+// so top2_entry ranks it too (magnitude key, lower column on ties).  The
+// kept pairs and nibbles go to global memory (A1's output, coalesced) and
+// into the compressed layout in shared memory.  Phase 2 is the staged A2
+// kernel's compute step on that tile.
+template <int CH, int QS>
+struct FusedCfg {
+  using D = DpStaged<CH, QS>;
+  static constexpr int kRawPitch = 32 * CH;          // bytes of one tile row of W
+  static constexpr int kRawBytes = 256 * kRawPitch;
+  static constexpr int kSmem = kRawBytes + D::kStage;
+  static constexpr int kMinBlocks = CH == 8 ? 2 : 3;
+};
 
 template <int CH, int QS>
-__global__ void __launch_bounds__(32 * CH * QS, 3) prune_double24_kernel(
+__global__ void __launch_bounds__(32 * CH * QS, (FusedCfg<CH, QS>::kMinBlocks)) prune_double24_kernel(
     const uint4* __restrict__ W, uint2* __restrict__ vals, uint8_t* __restrict__ meta,
     uint2* __restrict__ t_vals, uint8_t* __restrict__ t_meta, int64_t rows, int64_t cols,
     uint32_t k17) {
   using C = DpStaged<CH, QS>;
+  using F = FusedCfg<CH, QS>;
   constexpr int kQ = 4 / QS;                     // groups of 4 columns per thread in phase 2
   constexpr int kRowChunks = 2 * CH;             // 8-column chunks per tile row
   constexpr int kItems = 256 * kRowChunks / C::kThreads;  // chunks per thread in phase 1
-  static_assert(kItems % 4 == 0, "phase 1 loads in batches of four");
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ DpTables tab;
+  uint8_t* raw = smem;                // the tile's rows of W
+  uint8_t* st = smem + F::kRawBytes;  // its compressed form, A2's staged layout
   fill_tables(tab);
-  __syncthreads();
   const uint32_t k1 = k17 >> 16;
   const uint32_t n_h8 = static_cast<uint32_t>(rows / 8);
   const uint32_t tiles_h = (static_cast<uint32_t>(rows) + 255) / 256;
@@ -398,43 +408,53 @@ __global__ void __launch_bounds__(32 * CH * QS, 3) prune_double24_kernel(
   const uint32_t lane = threadIdx.x & 31, warp = (threadIdx.x >> 5) % CH;
   const int q0 = static_cast<int>(threadIdx.x >> 5) / CH * kQ;
   const int64_t row_chunks = cols / 8;  // 8-column chunks per row of W
+  const uint32_t raw_s = static_cast<uint32_t>(__cvta_generic_to_shared(raw));
+
+  auto issue = [&](uint32_t th, uint32_t tc) {
+    const uint32_t row0 = th * 256;
+    const int64_t chunk0 = static_cast<int64_t>(tc) * kRowChunks;
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+      const uint32_t i = threadIdx.x + it * C::kThreads;
+      const uint32_t r = i / kRowChunks, cc = i % kRowChunks;
+      if (row0 + r < rows) cp_async16(raw_s + r * F::kRawPitch + 16 * cc, W + (row0 + r) * row_chunks + chunk0 + cc);
+    }
+    cp_async_commit();
+  };
+
   const uint32_t step_c = gridDim.x / tiles_h, step_h = gridDim.x % tiles_h;
   uint32_t th = blockIdx.x % tiles_h, tc = blockIdx.x / tiles_h;
   grid_dependency_wait();
   allow_dependents_launch();
-  for (int stage = 0; tc < tiles_c; stage ^= 1) {
-    uint8_t* st = smem + stage * C::kStage;
+  if (tc < tiles_c) issue(th, tc);
+  while (tc < tiles_c) {
+    cp_async_wait_all();
+    __syncthreads();  // the tile's W is in; every thread is done with the last tile
     const uint32_t row0 = th * 256;
     const int64_t chunk0 = static_cast<int64_t>(tc) * kRowChunks;
-#pragma unroll
-    for (int b = 0; b < kItems; b += 4) {
-      uint4 w[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint32_t i = threadIdx.x + (b + u) * C::kThreads;
-        const uint32_t r = i / kRowChunks, cc = i % kRowChunks;
-        if (row0 + r < rows) w[u] = __ldcs(W + (row0 + r) * row_chunks + chunk0 + cc);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint32_t i = threadIdx.x + (b + u) * C::kThreads;
-        const uint32_t r = i / kRowChunks, cc = i % kRowChunks;
-        if (row0 + r < rows) {
-          const uint32_t ea = top2_entry(w[u].x, w[u].y, tab.out[0], k17, k1);
-          const uint32_t eb = top2_entry(w[u].z, w[u].w, tab.out[1], k17, k1);
-          const uint2 kept = make_uint2(__byte_perm(w[u].x, w[u].y, ea), __byte_perm(w[u].z, w[u].w, eb));
-          const uint8_t nib = static_cast<uint8_t>((ea + eb) >> 16);
-          const int64_t at = (row0 + r) * row_chunks + chunk0 + cc;
-          __stcs(vals + at, kept);
-          meta[at] = nib;
-          const uint32_t o = r >> 3, c = cc >> 1, h = cc & 1;
-          *reinterpret_cast<uint2*>(st + (r & 7) * C::kValPlane + o * C::kValPitch +
-                                    16 * (c ^ swz<CH>(o)) + 8 * h) = kept;
-          st[C::kValBytes + (r & 7) * 512 + o * 16 + 2 * c + h] = nib;
-        }
+#pragma unroll 4
+    for (int it = 0; it < kItems; ++it) {
+      const uint32_t i = threadIdx.x + it * C::kThreads;
+      const uint32_t r = i / kRowChunks, cc = i % kRowChunks;
+      if (row0 + r < rows) {
+        const uint4 w = *reinterpret_cast<const uint4*>(raw + r * F::kRawPitch + 16 * cc);
+        const uint32_t ea = top2_entry(w.x, w.y, tab.out[0], k17, k1);
+        const uint32_t eb = top2_entry(w.z, w.w, tab.out[1], k17, k1);
+        const uint2 kept = make_uint2(__byte_perm(w.x, w.y, ea), __byte_perm(w.z, w.w, eb));
+        const uint8_t nib = static_cast<uint8_t>((ea + eb) >> 16);
+        const int64_t at = (row0 + r) * row_chunks + chunk0 + cc;
+        __stcs(vals + at, kept);
+        meta[at] = nib;
+        const uint32_t o = r >> 3, c = cc >> 1, h = cc & 1;
+        *reinterpret_cast<uint2*>(st + (r & 7) * C::kValPlane + o * C::kValPitch +
+                                  16 * (c ^ swz<CH>(o)) + 8 * h) = kept;
+        st[C::kValBytes + (r & 7) * 512 + o * 16 + 2 * c + h] = nib;
       }
     }
-    __syncthreads();
+    __syncthreads();  // compressed tile complete; W's buffer is free
+    uint32_t nh = th + step_h, nc = tc + step_c;
+    if (nh >= tiles_h) { nh -= tiles_h; ++nc; }
+    if (nc < tiles_c) issue(nh, nc);
     const uint32_t h8 = th * 32 + lane;
     if (h8 < n_h8) {
       uint32_t pw[8][kQ];
@@ -454,9 +474,8 @@ __global__ void __launch_bounds__(32 * CH * QS, 3) prune_double24_kernel(
       }
       transpose_prune_octet<kQ>(pw, m, tab, t_vals, t_meta, rows / 8, h8, tc * CH + warp, k17, q0);
     }
-    th += step_h;
-    tc += step_c;
-    if (th >= tiles_h) { th -= tiles_h; ++tc; }
+    th = nh;
+    tc = nc;
   }
 }
 
@@ -529,10 +548,11 @@ template <int CH, int QS>
 static cudaError_t run_fused(const void* W, int64_t rows, int64_t cols, void* vals, uint8_t* meta,
                              void* t_vals, uint8_t* t_meta, cudaStream_t stream) {
   using C = DpStaged<CH, QS>;
+  using F = FusedCfg<CH, QS>;
   auto kernel = prune_double24_kernel<CH, QS>;
   static std::atomic<int> per_sm[64];
   int per = 0;
-  if (cudaError_t e = blocks_per_sm(kernel, C::kThreads, C::kSmem, per_sm, per)) return e;
+  if (cudaError_t e = blocks_per_sm(kernel, C::kThreads, F::kSmem, per_sm, per)) return e;
   const int64_t tiles = ((rows + 255) / 256) * (cols / (16 * CH));
   const int64_t cap = static_cast<int64_t>(sm_count()) * per;
   const int64_t blocks = tiles < cap ? tiles : cap;
@@ -540,7 +560,7 @@ static cudaError_t run_fused(const void* W, int64_t rows, int64_t cols, void* va
   cudaLaunchAttribute attrs[1];
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
   cfg.blockDim = dim3(C::kThreads);
-  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.dynamicSmemBytes = F::kSmem;
   cfg.stream = stream;
   add_pdl_attr(cfg, attrs);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<const uint4*>(W), static_cast<uint2*>(vals),
