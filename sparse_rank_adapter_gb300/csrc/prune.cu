@@ -25,77 +25,6 @@
 namespace slope {
 namespace {
 
-// Packs a 16-bit bf16 pattern and its in-group index into one integer whose
-// order is the ranking: larger magnitude first, then lower index.  The sign
-// sits below the index so the pattern can be rebuilt from the winner.
-__device__ __forceinline__ uint32_t rank_key(uint32_t bits16, uint32_t j) {
-  return ((bits16 & 0x7FFFu) << 3) | ((3u - j) << 1) | (bits16 >> 15);
-}
-
-__device__ __forceinline__ uint32_t pattern_of(uint32_t key) {
-  return (key >> 3) | ((key & 1u) << 15);
-}
-
-// Top two of a group of four bf16 patterns.  Returns the kept pair packed
-// (lower column in the low half) and writes the nibble i0 | i1 << 2.
-__device__ __forceinline__ uint32_t top2of4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3,
-                                            uint32_t& nibble) {
-  const uint32_t k0 = rank_key(b0, 0), k1 = rank_key(b1, 1);
-  const uint32_t k2 = rank_key(b2, 2), k3 = rank_key(b3, 3);
-  const uint32_t a = max(k0, k1), b = min(k0, k1);
-  const uint32_t c = max(k2, k3), d = min(k2, k3);
-  const uint32_t first = max(a, c);
-  const uint32_t second = max(min(a, c), max(b, d));
-  const uint32_t j1 = 3u - ((first >> 1) & 3u);
-  const uint32_t j2 = 3u - ((second >> 1) & 3u);
-  const bool ordered = j1 < j2;
-  const uint32_t lo = ordered ? j1 : j2, hi = ordered ? j2 : j1;
-  const uint32_t vlo = pattern_of(ordered ? first : second);
-  const uint32_t vhi = pattern_of(ordered ? second : first);
-  nibble = lo | (hi << 2);
-  return vlo | (vhi << 16);
-}
-
-// ---------------------------------------------------------------- A1 ------
-// One 16-byte chunk = 8 consecutive weights of a row = 2 groups -> 8 bytes of
-// kept values and one metadata byte.  Row-major contiguity makes chunk c of
-// the flattened matrix map to vals[c] (uint2) and meta[c]; every warp access
-// is fully coalesced.
-
-constexpr int kPruneThreads = 256;
-constexpr int kPruneUnroll = 4;
-
-__global__ void __launch_bounds__(kPruneThreads) prune24_kernel(const uint4* __restrict__ W,
-                                                                uint2* __restrict__ vals,
-                                                                uint8_t* __restrict__ meta,
-                                                                int64_t nchunks) {
-  grid_dependency_wait();
-  allow_dependents_launch();
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-       base < nchunks; base += stride * kPruneUnroll) {
-    uint4 w[kPruneUnroll];
-#pragma unroll
-    for (int u = 0; u < kPruneUnroll; ++u) {
-      const int64_t c = base + u * stride;
-      if (c < nchunks) w[u] = __ldcs(W + c);
-    }
-#pragma unroll
-    for (int u = 0; u < kPruneUnroll; ++u) {
-      const int64_t c = base + u * stride;
-      if (c < nchunks) {
-        uint32_t n0, n1;
-        const uint32_t p0 = top2of4(w[u].x & 0xFFFFu, w[u].x >> 16, w[u].y & 0xFFFFu,
-                                    w[u].y >> 16, n0);
-        const uint32_t p1 = top2of4(w[u].z & 0xFFFFu, w[u].z >> 16, w[u].w & 0xFFFFu,
-                                    w[u].w >> 16, n1);
-        __stcs(vals + c, make_uint2(p0, p1));
-        meta[c] = static_cast<uint8_t>(n0 | (n1 << 4));
-      }
-    }
-  }
-}
-
 // ---------------------------------------------------------------- A2 ------
 
 constexpr int kDpThreads = 256;  // direct kernel: 8 warps = 8 column chunks per tile
@@ -165,6 +94,51 @@ __device__ __forceinline__ uint32_t top2_entry(uint32_t w01, uint32_t w23, const
   // zero, so the +1 in each multiplier never reaches the bits kept
   const uint32_t off = (__umulhi(first, 0x200001u) & 0x30u) | (__umulhi(second, 0x80001u) & 0x0Cu);
   return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(out) + off);
+}
+
+// ---------------------------------------------------------------- A1 ------
+// One 16-byte chunk = 8 consecutive weights of a row = 2 groups -> 8 bytes of
+// kept values and one metadata byte.  Row-major contiguity makes chunk c of
+// the flattened matrix map to vals[c] (uint2) and meta[c]; every warp access
+// is fully coalesced.  A row group of four bf16 is two words with two
+// entries each, the layout top2_entry takes (it was written for a group of
+// the transpose, four rows packed two per word), so A1 ranks with the same
+// multiply-add keys and table: magnitude first, the lower column on ties.
+
+constexpr int kPruneThreads = 256;
+constexpr int kPruneUnroll = 4;
+
+__global__ void __launch_bounds__(kPruneThreads) prune24_kernel(const uint4* __restrict__ W,
+                                                                uint2* __restrict__ vals,
+                                                                uint8_t* __restrict__ meta,
+                                                                int64_t nchunks, uint32_t k17) {
+  __shared__ DpTables tab;
+  fill_tables(tab);
+  __syncthreads();
+  grid_dependency_wait();
+  allow_dependents_launch();
+  const uint32_t k1 = k17 >> 16;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       base < nchunks; base += stride * kPruneUnroll) {
+    uint4 w[kPruneUnroll];
+#pragma unroll
+    for (int u = 0; u < kPruneUnroll; ++u) {
+      const int64_t c = base + u * stride;
+      if (c < nchunks) w[u] = __ldcs(W + c);
+    }
+#pragma unroll
+    for (int u = 0; u < kPruneUnroll; ++u) {
+      const int64_t c = base + u * stride;
+      if (c < nchunks) {
+        const uint32_t ea = top2_entry(w[u].x, w[u].y, tab.out[0], k17, k1);
+        const uint32_t eb = top2_entry(w[u].z, w[u].w, tab.out[1], k17, k1);
+        __stcs(vals + c, make_uint2(__byte_perm(w[u].x, w[u].y, ea), __byte_perm(w[u].z, w[u].w, eb)));
+        // the selectors stay below 0x8000: the sum carries nothing into the nibbles
+        meta[c] = static_cast<uint8_t>((ea + eb) >> 16);
+      }
+    }
+  }
 }
 
 // Work item: 8 consecutive rows (one "octet" h8) x 4·Q consecutive columns
@@ -499,6 +473,8 @@ static cudaError_t blocks_per_sm(Kernel kernel, int threads, int smem, std::atom
 
 }  // namespace
 
+constexpr uint32_t kKeyShift = 1u << 17;  // the k17 argument of the prune kernels
+
 cudaError_t launch_prune24(const void* W, int64_t rows, int64_t cols, void* vals, uint8_t* meta,
                            cudaStream_t stream) {
   const int64_t nchunks = rows * cols / 8;
@@ -515,11 +491,10 @@ cudaError_t launch_prune24(const void* W, int64_t rows, int64_t cols, void* vals
   cfg.stream = stream;
   add_pdl_attr(cfg, attrs);
   cudaError_t e = cudaLaunchKernelEx(&cfg, prune24_kernel, static_cast<const uint4*>(W),
-                                     static_cast<uint2*>(vals), meta, nchunks);
+                                     static_cast<uint2*>(vals), meta, nchunks, kKeyShift);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-constexpr uint32_t kKeyShift = 1u << 17;  // the k17 argument of the A2 kernels
 
 template <int CH, int QS>
 static cudaError_t run_staged(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols,
