@@ -347,6 +347,21 @@ def fwd_bytes(T, inp, out, r):
     return out * inp * 1.125 + 2.0 * T * (inp + out) + 2.0 * r * (inp + out) + 2 * 4.0 * T * r
 
 
+def dw_bytes(T, inp, out, r):
+    """Bytes a weight-gradient call must move at least: dY and X in (bf16),
+    the metadata, the compressed fp32 dW out, XL and G in (hi/lo bf16), and
+    dL, dR out (fp32)."""
+    return 2.0 * T * (inp + out) + out * inp / 8 + out * inp / 2 * 4 + 2 * 4.0 * T * r + 4.0 * r * (inp + out)
+
+
+# DRAM bytes (read + write) per launch of the dominant kernel, averaged over
+# its launches in one step, from an ncu capture of the same workload
+# (dram__bytes_read.sum + dram__bytes_write.sum; outputs a short kernel
+# leaves dirty in L2 are not yet written).  Only kernels unchanged since their
+# capture are listed.
+NCU_TRAFFIC = {("opt-350m-block", "bwd_weight"): 30.44e6}
+
+
 def call_bytes(name, T, inp, out, r):
     if name == "prune":
         return out * inp * (2 + 1 + 0.125)
@@ -473,7 +488,12 @@ def gpu_arm(args):
                  "fwd": "slope_linear_fwd (XL GEMM + sparse GEMM)", "bwd_input": "slope_linear_bwd_input (G GEMM + sparse GEMM)",
                  "bwd_weight": "dW GEMM with dL, dR (slope_linear_bwd_weight)",
                  "prune_double": "prune_double24_kernel (slope_prune_and_double_prune)"}
-    roof.update({"kernel": kernel_of.get(dom, dom), "traffic": None,
+    traffic = NCU_TRAFFIC.get((wl.name, dom))
+    if traffic is not None:
+        roof["traffic_unit"] = "bytes per launch"
+        if dom == "bwd_weight":
+            roof["algorithmic_bytes"] = sum(dw_bytes(T, i, o, r) for i, o, _ in per_call[dom]) / len(per_call[dom])
+    roof.update({"kernel": kernel_of.get(dom, dom), "traffic": traffic,
                  "peak_source": f"{src} ({'2x ' if dom in ('fwd', 'bwd_input') else ''}bf16 sustained)"
                  if roof['bound'] == 'tensor' else f"{src} hbm",
                  "launches_per_step": n_launch})
