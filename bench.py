@@ -372,6 +372,35 @@ def call_bytes(name, T, inp, out, r):
     return 0.0
 
 
+def mma_rates(stream, iters: int = 2048, reps: int = 3):
+    """Tensor-core rate self test of the library (resident shared-memory
+    operands, N = 256): dense and 2:4-sparse kind::f16 (random legal
+    metadata, as pruned weights have; and one fixed pattern) on one SM and
+    on SM pairs, dense-equivalent TFLOP/s, best of `reps` launches timed with
+    events on `stream`."""
+    import torch
+
+    from sparse_rank_adapter_gb300 import slope as S
+
+    out = {}
+    with torch.cuda.stream(stream):
+        for kind, name in ((0, "dense"), (1, "sparse_fixed_meta"), (2, "sparse")):
+            for pair in (False, True):
+                S.slope_selftest_mma_rate(kind, pair, 64, stream=stream)  # warm-up
+                best = 0.0
+                for _ in range(reps):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    fl = S.slope_selftest_mma_rate(kind, pair, iters, stream=stream)
+                    e1.record(stream)
+                    e1.synchronize()
+                    best = max(best, fl / (e0.elapsed_time(e1) * 1e-3) / 1e12)
+                out[f"{name}_{'pair' if pair else 'one_sm'}"] = round(best, 1)
+    S.slope_device_status(stream)
+    out["unit"] = "TFLOP/s dense-equivalent, kind::f16 bf16, N = 256, operands resident in shared memory"
+    return out
+
+
 def gpu_arm(args):
     import torch
     import torch.distributed as dist
@@ -498,6 +527,10 @@ def gpu_arm(args):
                  if roof['bound'] == 'tensor' else f"{src} hbm",
                  "launches_per_step": n_launch})
 
+    rates = mma_rates(stream) if args.mma_rate else None
+    if rates and roof["bound"] == "tensor":
+        key = "sparse_pair" if dom in ("fwd", "bwd_input") else "dense_pair"
+        roof["frac_of_mma_selftest"] = roof["achieved"] / rates[key]
     e2e = e2e_measure(args, wl, sets[0], stream, dev) if args.e2e else None
     cpu = None
     if rank == 0 and args.cpu_baseline:
@@ -521,7 +554,7 @@ def gpu_arm(args):
             "composite_roofline_frac": composite_frac(wl, ms_step, bf16_sus),
             "calls_ms_per_step": {k: round(v, 4) for k, v in calls_ms.items()},
             "roofline": roof, "clocks": clocks, "gpu_launches": sets[0].launches_per_step() * args.steps,
-            "e2e": e2e, "cpu_baseline": cpu,
+            "e2e": e2e, "cpu_baseline": cpu, "mma_rate_selftest": rates,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -707,6 +740,8 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-mma-rate", dest="mma_rate", action="store_false",
+                    help="skip the tensor-core rate self test")
     ap.add_argument("--fused-prune", action="store_true",
                     help="A1 and A2 through the one-call slope_prune_and_double_prune")
     args = ap.parse_args()

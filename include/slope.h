@@ -199,6 +199,24 @@ int slope_device_status(void* stream);
  */
 int slope_selftest_wait_timeout(int64_t limit_cycles, void* stream);
 
+/*
+ * Tensor-core rate self test (no counterpart in the method: it measures the
+ * rate the GEMM calls above are judged against).  Every SM (pair = 0) or SM
+ * pair (pair = 1, tcgen05 cta_group::2) issues `iters` rounds of four
+ * back-to-back tcgen05.mma instructions of kind::f16 (bf16 operands, fp32
+ * accumulation, N = 256; M = 128 per SM, 256 per pair) on operands that stay
+ * in shared memory: dense (kind = 0, K = 16 per instruction) or 2:4 sparse
+ * (the .sp form, K = 32 dense-equivalent, metadata in TMEM), with every
+ * group keeping positions 0 and 1 (kind = 1) or each group a random one of
+ * the six legal position pairs, as pruned weights have (kind = 2).
+ * Writes the dense-equivalent flops the launch executes to *flops and
+ * returns once it is enqueued on `stream`; time it with events there.
+ * kind must be 0, 1 or 2, pair 0 or 1 and 1 <= iters <= 2^20, else
+ * SLOPE_ERR_INVALID_ARG.  A bounded wait that ran out is reported by
+ * slope_device_status().
+ */
+int slope_selftest_mma_rate(int kind, int pair, int64_t iters, double* flops, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -407,6 +407,15 @@ extern "C" int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T,
   return from_cuda(launch_dense_gemm(q, st));
 }
 
+extern "C" int slope_selftest_mma_rate(int kind, int pair, int64_t iters, double* flops,
+                                       void* stream) {
+  if (kind < 0 || kind > 2 || (pair != 0 && pair != 1)) return SLOPE_ERR_INVALID_ARG;
+  if (iters < 1 || iters > (int64_t(1) << 20) || !flops) return SLOPE_ERR_INVALID_ARG;
+  if (int s = check_device()) return s;
+  return from_cuda(launch_mma_rate(kind, pair != 0, iters, flops,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
 extern "C" int slope_selftest_wait_timeout(int64_t limit_cycles, void* stream) {
   if (limit_cycles <= 0 || limit_cycles > (int64_t(1) << 34)) return SLOPE_ERR_INVALID_ARG;
   if (int s = check_device()) return s;

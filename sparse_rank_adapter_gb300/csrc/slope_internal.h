@@ -45,6 +45,13 @@ cudaError_t launch_prune_double24(const void* W, int64_t rows, int64_t cols, voi
                                   uint8_t* meta, void* t_vals, uint8_t* t_meta,
                                   cudaStream_t stream);
 
+// ---- tensor-core rate self test (mma_rate.cu): enqueues the launch and
+// writes the dense-equivalent flops it executes to *flops.
+// kind: 0 dense, 1 sparse with one fixed metadata pattern, 2 sparse with
+// random legal metadata.
+cudaError_t launch_mma_rate(int kind, bool pair, int64_t iters, double* flops,
+                            cudaStream_t stream);
+
 // ---- tensor-map encoding (api.cu): 2-D row-major tensor [outer][inner]
 // with `row_bytes` between rows, box [box_outer][box_inner], given swizzle.
 enum class Swz { None, B32, B64, B128 };

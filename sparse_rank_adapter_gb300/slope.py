@@ -35,6 +35,7 @@ SIGNATURES = (
     ("slope_linear_bwd_weight", _i, (_vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _i, _vp, _u32, _vp, _vp, _vp, _sz, _vp)),
     ("slope_device_status", _i, (_vp,)),
     ("slope_selftest_wait_timeout", _i, (_i64, _vp)),
+    ("slope_selftest_mma_rate", _i, (_i, _i, _i64, ctypes.POINTER(ctypes.c_double), _vp)),
 )
 
 _lib = None
@@ -207,6 +208,21 @@ def slope_linear_bwd_weight(dY, X, Wm, XL, G, dW, dL=None, dR=None, flags: int =
 
 def slope_device_status(stream=None):
     _check(lib().slope_device_status(_stream(stream)), "slope_device_status")
+
+
+MMA_DENSE, MMA_SPARSE_FIXED_META, MMA_SPARSE_RANDOM_META = 0, 1, 2
+
+
+def slope_selftest_mma_rate(kind: int, pair: bool, iters: int, stream=None) -> float:
+    """Enqueue the tensor-core rate self test (kind::f16 MMAs from resident
+    shared-memory operands, on every SM or SM pair): dense, 2:4 sparse with
+    one fixed metadata pattern, or 2:4 sparse with random legal metadata.
+    Returns the dense-equivalent flops the launch executes; time it with
+    events on `stream`."""
+    flops = ctypes.c_double(0.0)
+    _check(lib().slope_selftest_mma_rate(int(kind), int(bool(pair)), iters, ctypes.byref(flops),
+                                         _stream(stream)), "slope_selftest_mma_rate")
+    return flops.value
 
 
 def slope_selftest_wait_timeout(limit_cycles: int, stream=None):

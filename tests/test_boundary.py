@@ -124,6 +124,20 @@ def test_linear_argument_checks(L):
 
 
 @cpu_only
+def test_mma_rate_argument_checks(L):
+    import ctypes
+
+    f = L.lib().slope_selftest_mma_rate
+    out = ctypes.c_double(0.0)
+    assert f(3, 0, 16, ctypes.byref(out), None) == L.ERR_INVALID_ARG
+    assert f(-1, 0, 16, ctypes.byref(out), None) == L.ERR_INVALID_ARG
+    assert f(1, -1, 16, ctypes.byref(out), None) == L.ERR_INVALID_ARG
+    assert f(1, 1, 0, ctypes.byref(out), None) == L.ERR_INVALID_ARG
+    assert f(0, 1, (1 << 20) + 1, ctypes.byref(out), None) == L.ERR_INVALID_ARG
+    assert f(0, 0, 16, None, None) == L.ERR_INVALID_ARG
+
+
+@cpu_only
 def test_selftest_argument_checks(L):
     f = L.lib().slope_selftest_wait_timeout
     assert f(0, None) == L.ERR_INVALID_ARG
