@@ -59,10 +59,8 @@ def run_gpu(S, d, T, inp, out, r, forward_only=False):
         dR = torch.empty(r, out, dtype=torch.float32, device=dev) if r else None
         S.slope_double_prune(Wv, Wm, out, inp, Dv, Dm)
         S.slope_linear_bwd_input(dY, Dv, Dm, L, R, dX, G)
-        # the benchmark's two-part weight-gradient call
-        S.slope_linear_bwd_weight(dY, X, Wm, XL, G, dW, dL, dR, flags=S.SKIP_ADAPTER)
-        if r:
-            S.slope_linear_bwd_weight(dY, X, Wm, XL, G, dW, dL, dR, flags=S.SKIP_DW)
+        # the benchmark's weight-gradient call: dW, dL and dR together
+        S.slope_linear_bwd_weight(dY, X, Wm, XL, G, dW, dL, dR)
         res.update(dX=dX, dW=dW, dL=dL, dR=dR)
     torch.cuda.synchronize()
     S.slope_device_status()
@@ -116,9 +114,9 @@ def check_layer(S, layer, T, inp, out, r, forward_only=False, n_t=48, n_o=256, n
     assert_close_rel("dL", np64(g["dL"])[cols], dLr)
 
 
-@pytest.mark.parametrize("name,inp,out", [("fc1", 2560, 10240), ("fc2", 10240, 2560)])
+@pytest.mark.parametrize("name,inp,out", [("q", 2560, 2560), ("fc1", 2560, 10240), ("fc2", 10240, 2560)])
 def test_opt27b_block_linears(S, name, inp, out):
-    check_layer(S, 4 if name == "fc1" else 5, 8192, inp, out, 32)
+    check_layer(S, {"q": 0, "fc1": 4, "fc2": 5}[name], 8192, inp, out, 32)
 
 
 @pytest.mark.parametrize("r", [0, 64])
