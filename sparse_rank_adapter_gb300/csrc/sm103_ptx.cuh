@@ -1,7 +1,9 @@
 // sm103_ptx.cuh — hand-written inline-PTX wrappers for the sm_103a features
-// the kernels use: mbarriers (every wait bounded), TMA tile loads, and the
+// the kernels use: mbarriers (every wait bounded), TMA tile loads and stores,
+// thread-block clusters (distributed shared memory, remote arrivals), and the
 // fifth-generation tensor core (tcgen05: TMEM allocation, dense and 2:4-sparse
-// MMA, shared->TMEM copy, TMEM loads).  No cluster multicast anywhere.
+// MMA on one SM or an SM pair, TMEM loads and stores, commits).  No TMA load
+// multicasts; the only multicast is a pair MMA's commit to both CTAs.
 #pragma once
 
 #include <cuda.h>
