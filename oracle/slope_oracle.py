@@ -18,6 +18,9 @@ cited below by its section labels:
     sparse formats for the weight and its transpose; the weight gradient is
     masked with the weight's own mask and stored without its zeros.
   * §T.1 "Lemma 2.1": the expected zeros added by the second pruning.
+  * App. K again, for the optimizer side: updated weights copied into the
+    compressed format (with the initialised mask kept, as §2.1's training
+    policy does) and linear combinations of matrices sharing a pattern.
 
 Where the page is silent the plainest reading is taken:
 
@@ -188,6 +191,60 @@ def double_prune24(vals: np.ndarray, meta: np.ndarray, rows: int, cols: int):
         raise ValueError("double pruning needs rows % 8 == 0")
     ws = decompress24(vals, meta, cols)
     return prune24(np.ascontiguousarray(ws.T))
+
+
+# ---------------------------------------------------------------------------
+# Optimizer side (App. K: updated weights copied into the compressed format,
+# and sparse linear combinations of matrices that share a pattern; §2.1: the
+# initialised row mask is kept while the transposed one may change; §2.3:
+# both sparse representations are updated during optimisation)
+# ---------------------------------------------------------------------------
+
+
+def recompress24(bits: np.ndarray, meta: np.ndarray) -> np.ndarray:
+    """Compressed values of a rows x cols bf16 matrix at the positions a given
+    2:4 metadata names: the mask is kept, not selected again.  Group g of a
+    row keeps columns 4g + i0 and 4g + i1 of ``bits``, (i0, i1) being the
+    nibble's two fields, in that order."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    rows, cols = bits.shape
+    if cols % 8:
+        raise ValueError("2:4 compression needs cols % 8 == 0")
+    sel = unpack_meta24(meta)
+    grouped = bits.reshape(rows, cols // 4, 4)
+    return np.take_along_axis(grouped, sel, axis=-1).reshape(rows, cols // 2).astype(np.uint16)
+
+
+def recompress_double_prune24(bits: np.ndarray, meta: np.ndarray):
+    """The updated weight compressed with its kept mask (recompress24), and
+    the second pruning of the result (double_prune24).  Returns (vals, t_vals,
+    t_meta)."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    rows, cols = bits.shape
+    vals = recompress24(bits, meta)
+    t_vals, t_meta, _ = double_prune24(vals, meta, rows, cols)
+    return vals, t_vals, t_meta
+
+
+def sparse_axpby24(beta: float, a_vals: np.ndarray, gamma: float, b_vals: np.ndarray,
+                   meta: np.ndarray) -> np.ndarray:
+    """beta·A + gamma·B of two rows x cols matrices that share the 2:4
+    pattern ``meta``, given as real-valued compressed values (rows x cols/2):
+    both are expanded to their dense masked matrices, combined in fp64 and
+    compressed again with the same pattern."""
+    a_vals = np.asarray(a_vals, dtype=np.float64)
+    b_vals = np.asarray(b_vals, dtype=np.float64)
+    rows, half = a_vals.shape
+    cols = 2 * half
+    sel = unpack_meta24(meta)
+
+    def dense(v):
+        out = np.zeros((rows, cols // 4, 4))
+        np.put_along_axis(out, sel, v.reshape(rows, cols // 4, 2), axis=-1)
+        return out.reshape(rows, cols)
+
+    c = beta * dense(a_vals) + gamma * dense(b_vals)
+    return np.take_along_axis(c.reshape(rows, cols // 4, 4), sel, axis=-1).reshape(rows, half)
 
 
 # ---------------------------------------------------------------------------

@@ -360,3 +360,78 @@ def test_products_agree_with_a_second_library():
     dWc, dWd, dL, dR = O.linear_bwd_weight(d["dY"], d["X"], meta, d["L"], d["R"])
     torch.testing.assert_close(torch.from_numpy(dL), X.T @ (dY @ R.T), rtol=1e-12, atol=1e-12)
     torch.testing.assert_close(torch.from_numpy(dR), (X @ L).T @ dY, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- optimizer side
+
+
+def test_recompress_at_own_mask_is_prune():
+    """Gathering a weight at the mask selected from it returns the values the
+    selection kept: the gather and the selection agree on layout and order."""
+    W = synth.normal_bf16(0, 31, "W", (64, 96))
+    v, m, _ = O.prune24(W)
+    np.testing.assert_array_equal(O.recompress24(W, m), v)
+
+
+def test_recompress_worked_example():
+    """One row of eight weights 1..8 and metadata byte 0xD8: the low nibble 0x8
+    names positions 0 and 2 of group 0, the high nibble 0xD positions 1 and 3
+    of group 1, so the values are 1, 3, 6, 8."""
+    W = synth.to_bf16_bits(np.arange(1, 9, dtype=np.float32)).reshape(1, 8)
+    vals = O.recompress24(W, np.array([[0xD8]], dtype=np.uint8))
+    np.testing.assert_array_equal(O.bf16_to_f64(vals), [[1.0, 3.0, 6.0, 8.0]])
+
+
+def test_recompress_is_masked_weight():
+    """Expanding the gathered values gives W where the (kept) mask is set and
+    zero elsewhere; the mask is rebuilt here from the nibbles one by one."""
+    rng = np.random.default_rng(5)
+    W = synth.normal_bf16(0, 32, "W", (16, 32))
+    codes = np.array(sorted(O.LEGAL_NIBBLES), dtype=np.uint8)
+    nib = rng.choice(codes, size=(16, 8))
+    meta = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+    mask = np.zeros((16, 32), dtype=bool)
+    for r in range(16):
+        for g in range(8):
+            mask[r, 4 * g + (nib[r, g] & 3)] = True
+            mask[r, 4 * g + (nib[r, g] >> 2)] = True
+    dense = O.decompress24(O.recompress24(W, meta), meta, 32)
+    np.testing.assert_array_equal(dense, np.where(mask, W, 0).astype(np.uint16))
+
+
+def test_recompress_double_prune_matches_the_two_steps():
+    """With the weight unchanged, re-compressing at its own mask and double
+    pruning gives what prune24 and double_prune24 give; with an updated
+    weight the transposed result still keeps 2 of 4 along its rows and only
+    positions the kept row mask allows."""
+    W = synth.normal_bf16(0, 33, "W", (64, 48))
+    v, m, mask = O.prune24(W)
+    tv, tm, _ = O.double_prune24(v, m, 64, 48)
+    v2, tv2, tm2 = O.recompress_double_prune24(W, m)
+    np.testing.assert_array_equal(v2, v)
+    np.testing.assert_array_equal(tv2, tv)
+    np.testing.assert_array_equal(tm2, tm)
+    W2 = synth.normal_bf16(0, 34, "W", (64, 48))  # the optimizer's new values
+    v3, tv3, tm3 = O.recompress_double_prune24(W2, m)
+    t_mask = O.decompress24(np.full_like(tv3, 0x3F80), tm3, 64) != 0  # positions D keeps
+    assert (t_mask.reshape(48, 16, 4).sum(-1) == 2).all()
+    nz = O.decompress24(tv3, tm3, 64) != 0
+    assert not (nz & ~mask.T).any()  # D's non-zeros lie inside the kept row mask
+
+
+def test_sparse_axpby_cases():
+    """beta·A + gamma·B on a shared pattern: (1, 0) gives A, (0, 1) gives B,
+    A = B gives (beta + gamma)·A, and it is linear in (beta, gamma); the
+    result equals the element-wise combination of the compressed values
+    because both matrices keep the same positions."""
+    rng = np.random.default_rng(7)
+    _, meta, _ = O.prune24(synth.normal_bf16(0, 35, "W", (32, 64)))
+    A = rng.standard_normal((32, 32))
+    B = rng.standard_normal((32, 32))
+    np.testing.assert_array_equal(O.sparse_axpby24(1.0, A, 0.0, B, meta), A)
+    np.testing.assert_array_equal(O.sparse_axpby24(0.0, A, 1.0, B, meta), B)
+    np.testing.assert_allclose(O.sparse_axpby24(0.3, A, 0.5, A, meta), 0.8 * A, rtol=1e-15)
+    c1 = O.sparse_axpby24(0.9, A, -0.01, B, meta)
+    c2 = O.sparse_axpby24(0.9, A, 0.0, B, meta) + O.sparse_axpby24(0.0, A, -0.01, B, meta)
+    np.testing.assert_allclose(c1, c2, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(c1, 0.9 * A - 0.01 * B, rtol=1e-14, atol=1e-15)
