@@ -128,6 +128,39 @@ int slope_prune_and_double_prune(const void* W, int64_t rows, int64_t cols, int 
                                  void* stream);
 
 /*
+ * Optimizer side, weight re-compression (App. K: the kernel that copies
+ * optimizer-updated weights into the compressed format; §2.1: the training
+ * policy keeps the initialised row mask while the transposed, column-wise
+ * mask may change; §2.3: both sparse representations are updated during
+ * optimisation).  W is the updated rows x cols bf16 weight and `meta` its
+ * kept metadata (rows x cols/8, from slope_prune_nm at initialisation).
+ * Writes `vals` (rows x cols/2 bf16): group g of a row takes W's columns
+ * 4g + i0 and 4g + i1, (i0, i1) the fields of its nibble, in that order;
+ * and (t_vals, t_meta), exactly what slope_double_prune(vals, meta, rows,
+ * cols, ...) would write.  One pass over W for cols % 128 == 0, a gather
+ * then the second pruning otherwise.  `meta` is read only; the outputs must
+ * not overlap the inputs or each other.  Requires rows % 8 == 0 and
+ * cols % 16 == 0, both positive (else SLOPE_ERR_SHAPE).
+ */
+int slope_recompress_double_prune(const void* W, const uint8_t* meta, int64_t rows, int64_t cols,
+                                  void* vals, void* t_vals, uint8_t* t_meta, void* stream);
+
+/*
+ * Optimizer side, sparse linear combination (App. K: beta·A + gamma·B for
+ * matrices that share a sparsity pattern, for weight decay).  A, B and out
+ * are the compressed value arrays (n values each, e.g. rows x cols/2) of
+ * matrices with the same metadata, so the combination is element-wise:
+ * out[i] = beta·A[i] + gamma·B[i], computed in fp32 as one fused
+ * multiply-add on gamma·B[i], each array SLOPE_F32 or SLOPE_BF16 by its
+ * dtype argument (a bf16 output is rounded to nearest even).  `out` may be
+ * A or B (an in-place update) but must not partly overlap either.  Requires
+ * n % 8 == 0 (else SLOPE_ERR_SHAPE; n == 0 is a no-op) and known dtypes
+ * (else SLOPE_ERR_INVALID_ARG).
+ */
+int slope_sparse_axpby(float beta, const void* A, int a_dtype, float gamma, const void* B,
+                       int b_dtype, void* out, int out_dtype, int64_t n, void* stream);
+
+/*
  * A3 — sparse forward with the fused adapter (§2.1, §2.2, §2.4, App. D):
  *     Y  = X·Wsᵀ + (X·L)·R          (bf16 inputs, fp32 accumulation)
  *     XL = X·L                        (kept for the backward)

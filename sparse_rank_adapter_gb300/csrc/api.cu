@@ -269,6 +269,33 @@ extern "C" int slope_prune_and_double_prune(const void* W, int64_t rows, int64_t
                                          static_cast<cudaStream_t>(stream)));
 }
 
+extern "C" int slope_recompress_double_prune(const void* W, const uint8_t* meta, int64_t rows,
+                                             int64_t cols, void* vals, void* t_vals,
+                                             uint8_t* t_meta, void* stream) {
+  if (rows <= 0 || cols <= 0 || rows % 8 != 0 || cols % 16 != 0) return SLOPE_ERR_SHAPE;
+  if (!W || !meta || !vals || !t_vals || !t_meta) return SLOPE_ERR_INVALID_ARG;
+  if (!aligned16(W) || !aligned16(meta) || !aligned16(vals) || !aligned16(t_vals) ||
+      !aligned16(t_meta))
+    return SLOPE_ERR_ALIGNMENT;
+  if (int s = check_device()) return s;
+  return from_cuda(launch_recompress_double24(W, meta, rows, cols, vals, t_vals, t_meta,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int slope_sparse_axpby(float beta, const void* A, int a_dtype, float gamma,
+                                  const void* B, int b_dtype, void* out, int out_dtype, int64_t n,
+                                  void* stream) {
+  auto ok_dt = [](int d) { return d == SLOPE_F32 || d == SLOPE_BF16; };
+  if (!ok_dt(a_dtype) || !ok_dt(b_dtype) || !ok_dt(out_dtype)) return SLOPE_ERR_INVALID_ARG;
+  if (n < 0 || n % 8 != 0) return SLOPE_ERR_SHAPE;
+  if (n == 0) return SLOPE_OK;
+  if (!A || !B || !out) return SLOPE_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(out)) return SLOPE_ERR_ALIGNMENT;
+  if (int s = check_device()) return s;
+  return from_cuda(launch_axpby(beta, A, a_dtype, gamma, B, b_dtype, out, out_dtype, n,
+                                static_cast<cudaStream_t>(stream)));
+}
+
 // Shared size rules of the three GEMM calls.
 static int check_linear(int64_t T, int64_t in, int64_t out, int r) {
   if (T < 0 || in <= 0 || out <= 0 || in % 128 != 0 || out % 128 != 0) return SLOPE_ERR_SHAPE;

@@ -14,6 +14,7 @@
 // and §2.3 / App. K (compressed formats for both).  Ranking uses the exact
 // magnitude key (bits & 0x7FFF) with ties to the lower index; the
 // compressed format is the one slope.h documents.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -57,9 +58,18 @@ __device__ __forceinline__ uint32_t output_entry(uint32_t code_first, uint32_t c
   return sel | ((lo | (hi << 2)) << (16 + nib_shift));
 }
 
+// Byte-permute selector that picks a group's two entries at the positions a
+// metadata nibble names (i0 | i1 << 2) out of its four (two words, two
+// entries each), in the order of the nibble's fields.
+__device__ __forceinline__ uint32_t gather_selector(uint32_t nib) {
+  const uint32_t i0 = nib & 3u, i1 = nib >> 2;
+  return (2 * i0) | ((2 * i0 + 1) << 4) | ((2 * i1) << 8) | ((2 * i1 + 1) << 12);
+}
+
 struct DpTables {
   uint2 expand[16];     // by metadata nibble
   uint32_t out[2][16];  // [upper / lower quadruple of the octet][code_first * 4 + code_second]
+  uint32_t gather[16];  // by metadata nibble
 };
 
 __device__ __forceinline__ void fill_tables(DpTables& t) {
@@ -68,6 +78,7 @@ __device__ __forceinline__ void fill_tables(DpTables& t) {
     const uint32_t g = threadIdx.x >> 4, idx = threadIdx.x & 15;
     t.out[g][idx] = output_entry(idx >> 2, idx & 3, 4 * g);
   }
+  if (threadIdx.x >= 32 && threadIdx.x < 48) t.gather[threadIdx.x - 32] = gather_selector(threadIdx.x - 32);
 }
 
 // Top two of the four candidates of a transposed group, packed as two rows
@@ -351,29 +362,35 @@ __global__ void __launch_bounds__(32 * CH * QS) double_prune24_staged_kernel(
 // kept pairs and nibbles go to global memory (A1's output, coalesced) and
 // into the compressed layout in shared memory.  Phase 2 is the staged A2
 // kernel's compute step on that tile.
-template <int CH, int QS>
+// GIVEN: the row mask is an input (the weight is re-compressed at the
+// positions its metadata names instead of selecting them): the tile's
+// metadata bytes are staged beside W, phase 1 gathers with the byte-permute
+// selector of each nibble and writes no metadata.
+template <int CH, int QS, bool GIVEN = false>
 struct FusedCfg {
   using D = DpStaged<CH, QS>;
   static constexpr int kRawPitch = 32 * CH;          // bytes of one tile row of W
   static constexpr int kRawBytes = 256 * kRawPitch;
-  static constexpr int kSmem = kRawBytes + D::kStage;
+  static constexpr int kRawMeta = GIVEN ? 256 * 16 : 0;  // a 16 B piece of each row's metadata
+  static constexpr int kSmem = kRawBytes + kRawMeta + D::kStage;
   static constexpr int kMinBlocks = CH == 8 ? 2 : 3;
 };
 
-template <int CH, int QS>
-__global__ void __launch_bounds__(32 * CH * QS, (FusedCfg<CH, QS>::kMinBlocks)) prune_double24_kernel(
-    const uint4* __restrict__ W, uint2* __restrict__ vals, uint8_t* __restrict__ meta,
-    uint2* __restrict__ t_vals, uint8_t* __restrict__ t_meta, int64_t rows, int64_t cols,
-    uint32_t k17) {
+template <int CH, int QS, bool GIVEN>
+__global__ void __launch_bounds__(32 * CH * QS, (FusedCfg<CH, QS, GIVEN>::kMinBlocks)) prune_double24_kernel(
+    const uint4* __restrict__ W, const uint8_t* __restrict__ meta_in, uint2* __restrict__ vals,
+    uint8_t* __restrict__ meta, uint2* __restrict__ t_vals, uint8_t* __restrict__ t_meta, int64_t rows,
+    int64_t cols, uint32_t k17) {
   using C = DpStaged<CH, QS>;
-  using F = FusedCfg<CH, QS>;
+  using F = FusedCfg<CH, QS, GIVEN>;
   constexpr int kQ = 4 / QS;                     // groups of 4 columns per thread in phase 2
   constexpr int kRowChunks = 2 * CH;             // 8-column chunks per tile row
   constexpr int kItems = 256 * kRowChunks / C::kThreads;  // chunks per thread in phase 1
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ DpTables tab;
   uint8_t* raw = smem;                // the tile's rows of W
-  uint8_t* st = smem + F::kRawBytes;  // its compressed form, A2's staged layout
+  uint8_t* rawm = smem + F::kRawBytes;  // GIVEN: their metadata, 16 B per row
+  uint8_t* st = smem + F::kRawBytes + F::kRawMeta;  // the compressed tile, A2's staged layout
   fill_tables(tab);
   const uint32_t k1 = k17 >> 16;
   const uint32_t n_h8 = static_cast<uint32_t>(rows / 8);
@@ -383,6 +400,7 @@ __global__ void __launch_bounds__(32 * CH * QS, (FusedCfg<CH, QS>::kMinBlocks)) 
   const int q0 = static_cast<int>(threadIdx.x >> 5) / CH * kQ;
   const int64_t row_chunks = cols / 8;  // 8-column chunks per row of W
   const uint32_t raw_s = static_cast<uint32_t>(__cvta_generic_to_shared(raw));
+  const uint32_t rawm_s = static_cast<uint32_t>(__cvta_generic_to_shared(rawm));
 
   auto issue = [&](uint32_t th, uint32_t tc) {
     const uint32_t row0 = th * 256;
@@ -392,6 +410,11 @@ __global__ void __launch_bounds__(32 * CH * QS, (FusedCfg<CH, QS>::kMinBlocks)) 
       const uint32_t i = threadIdx.x + it * C::kThreads;
       const uint32_t r = i / kRowChunks, cc = i % kRowChunks;
       if (row0 + r < rows) cp_async16(raw_s + r * F::kRawPitch + 16 * cc, W + (row0 + r) * row_chunks + chunk0 + cc);
+    }
+    if constexpr (GIVEN) {
+      for (uint32_t r = threadIdx.x; r < 256; r += C::kThreads)
+        if (row0 + r < rows)
+          cp_async16(rawm_s + r * 16, meta_in + (((row0 + r) * row_chunks + chunk0) & ~int64_t(15)));
     }
     cp_async_commit();
   };
@@ -412,13 +435,22 @@ __global__ void __launch_bounds__(32 * CH * QS, (FusedCfg<CH, QS>::kMinBlocks)) 
       const uint32_t r = i / kRowChunks, cc = i % kRowChunks;
       if (row0 + r < rows) {
         const uint4 w = *reinterpret_cast<const uint4*>(raw + r * F::kRawPitch + 16 * cc);
-        const uint32_t ea = top2_entry(w.x, w.y, tab.out[0], k17, k1);
-        const uint32_t eb = top2_entry(w.z, w.w, tab.out[1], k17, k1);
-        const uint2 kept = make_uint2(__byte_perm(w.x, w.y, ea), __byte_perm(w.z, w.w, eb));
-        const uint8_t nib = static_cast<uint8_t>((ea + eb) >> 16);
+        uint2 kept;
+        uint8_t nib;
+        if constexpr (GIVEN) {
+          // the chunk's metadata byte: rows hold cols / 8 bytes, a multiple
+          // of 16, so the tile's bytes sit at chunk0 % 16 in each row's piece
+          nib = rawm[r * 16 + (static_cast<uint32_t>(chunk0) & 15u) + cc];
+          kept = make_uint2(__byte_perm(w.x, w.y, tab.gather[nib & 15u]), __byte_perm(w.z, w.w, tab.gather[nib >> 4]));
+        } else {
+          const uint32_t ea = top2_entry(w.x, w.y, tab.out[0], k17, k1);
+          const uint32_t eb = top2_entry(w.z, w.w, tab.out[1], k17, k1);
+          kept = make_uint2(__byte_perm(w.x, w.y, ea), __byte_perm(w.z, w.w, eb));
+          nib = static_cast<uint8_t>((ea + eb) >> 16);
+        }
         const int64_t at = (row0 + r) * row_chunks + chunk0 + cc;
         __stcs(vals + at, kept);
-        meta[at] = nib;
+        if constexpr (!GIVEN) meta[at] = nib;
         const uint32_t o = r >> 3, c = cc >> 1, h = cc & 1;
         *reinterpret_cast<uint2*>(st + (r & 7) * C::kValPlane + o * C::kValPitch +
                                   16 * (c ^ swz<CH>(o)) + 8 * h) = kept;
@@ -450,6 +482,74 @@ __global__ void __launch_bounds__(32 * CH * QS, (FusedCfg<CH, QS>::kMinBlocks)) 
     }
     th = nh;
     tc = nc;
+  }
+}
+
+// ------------------------------------------------ optimizer side ---------
+// Re-compression of an updated weight at a kept mask (any width with
+// cols % 8 == 0): one 16-byte chunk = 8 weights = 2 groups and its metadata
+// byte in, the two kept pairs out; coalesced like the prune kernel.
+__global__ void __launch_bounds__(kPruneThreads) gather24_kernel(const uint4* __restrict__ W,
+                                                                 const uint8_t* __restrict__ meta,
+                                                                 uint2* __restrict__ vals,
+                                                                 int64_t nchunks) {
+  grid_dependency_wait();
+  allow_dependents_launch();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < nchunks; c += stride) {
+    const uint4 w = __ldcs(W + c);
+    const uint32_t nib = meta[c];
+    __stcs(vals + c, make_uint2(__byte_perm(w.x, w.y, gather_selector(nib & 15u)),
+                                __byte_perm(w.z, w.w, gather_selector(nib >> 4))));
+  }
+}
+
+// beta·A + gamma·B on the compressed values of two matrices that share a 2:4
+// pattern: the metadata is common, so the combination is element-wise on the
+// value arrays.  fp32 arithmetic (one fused multiply-add on gamma·b), inputs
+// and output each fp32 or bf16 (the output rounded to nearest even).  Eight
+// values per thread and step.
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+  const float4 x = __ldcs(reinterpret_cast<const float4*>(p));
+  const float4 y = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+  v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 x = __ldcs(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
+  __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
+  __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(v[4], v[5], v[6], v[7]));
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  __stcs(reinterpret_cast<uint4*>(p), make_uint4(w[0], w[1], w[2], w[3]));
+}
+
+template <typename TA, typename TB, typename TO>
+__global__ void __launch_bounds__(256) axpby_kernel(float beta, const TA* a, float gamma, const TB* b,
+                                                    TO* out, int64_t n8) {  // out may be a or b
+  grid_dependency_wait();
+  allow_dependents_launch();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    float va[8], vb[8], vo[8];
+    load8(a + 8 * i, va);
+    load8(b + 8 * i, vb);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) vo[k] = fmaf(beta, va[k], gamma * vb[k]);
+    store8(out + 8 * i, vo);
   }
 }
 
@@ -519,12 +619,13 @@ static cudaError_t run_staged(const void* vals, const uint8_t* meta, int64_t row
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int CH, int QS>
-static cudaError_t run_fused(const void* W, int64_t rows, int64_t cols, void* vals, uint8_t* meta,
-                             void* t_vals, uint8_t* t_meta, cudaStream_t stream) {
+template <int CH, int QS, bool GIVEN = false>
+static cudaError_t run_fused(const void* W, const uint8_t* meta_in, int64_t rows, int64_t cols,
+                             void* vals, uint8_t* meta, void* t_vals, uint8_t* t_meta,
+                             cudaStream_t stream) {
   using C = DpStaged<CH, QS>;
-  using F = FusedCfg<CH, QS>;
-  auto kernel = prune_double24_kernel<CH, QS>;
+  using F = FusedCfg<CH, QS, GIVEN>;
+  auto kernel = prune_double24_kernel<CH, QS, GIVEN>;
   static std::atomic<int> per_sm[64];
   int per = 0;
   if (cudaError_t e = blocks_per_sm(kernel, C::kThreads, F::kSmem, per_sm, per)) return e;
@@ -538,8 +639,9 @@ static cudaError_t run_fused(const void* W, int64_t rows, int64_t cols, void* va
   cfg.dynamicSmemBytes = F::kSmem;
   cfg.stream = stream;
   add_pdl_attr(cfg, attrs);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<const uint4*>(W), static_cast<uint2*>(vals),
-                                     meta, static_cast<uint2*>(t_vals), t_meta, rows, cols, kKeyShift);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<const uint4*>(W), meta_in,
+                                     static_cast<uint2*>(vals), meta, static_cast<uint2*>(t_vals), t_meta,
+                                     rows, cols, kKeyShift);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -550,14 +652,84 @@ cudaError_t launch_prune_double24(const void* W, int64_t rows, int64_t cols, voi
   if (cols % 128 == 0) {  // tile widths as A2's staged kernel
     const int64_t tiles_h = (rows + 255) / 256;
     if (tiles_h * (cols / 128) >= sm_count())
-      return run_fused<8, 1>(W, rows, cols, vals, meta, t_vals, t_meta, stream);
+      return run_fused<8, 1>(W, nullptr, rows, cols, vals, meta, t_vals, t_meta, stream);
     if (tiles_h * (cols / 64) >= sm_count())
-      return run_fused<4, 2>(W, rows, cols, vals, meta, t_vals, t_meta, stream);
-    return run_fused<2, 4>(W, rows, cols, vals, meta, t_vals, t_meta, stream);
+      return run_fused<4, 2>(W, nullptr, rows, cols, vals, meta, t_vals, t_meta, stream);
+    return run_fused<2, 4>(W, nullptr, rows, cols, vals, meta, t_vals, t_meta, stream);
   }
   // other widths: the two kernels one after the other
   if (cudaError_t e = launch_prune24(W, rows, cols, vals, meta, stream)) return e;
   return launch_double_prune24(vals, meta, rows, cols, t_vals, t_meta, stream);
+}
+
+cudaError_t launch_gather24(const void* W, const uint8_t* meta, int64_t rows, int64_t cols, void* vals,
+                            cudaStream_t stream) {
+  const int64_t nchunks = rows * cols / 8;
+  if (nchunks == 0) return cudaSuccess;
+  int64_t blocks = (nchunks + kPruneThreads - 1) / kPruneThreads;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attrs[1];
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kPruneThreads);
+  cfg.stream = stream;
+  add_pdl_attr(cfg, attrs);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gather24_kernel, static_cast<const uint4*>(W), meta,
+                                     static_cast<uint2*>(vals), nchunks);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_recompress_double24(const void* W, const uint8_t* meta, int64_t rows, int64_t cols,
+                                       void* vals, void* t_vals, uint8_t* t_meta, cudaStream_t stream) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  if (cols % 128 == 0) {
+    const int64_t tiles_h = (rows + 255) / 256;
+    if (tiles_h * (cols / 128) >= sm_count())
+      return run_fused<8, 1, true>(W, meta, rows, cols, vals, nullptr, t_vals, t_meta, stream);
+    if (tiles_h * (cols / 64) >= sm_count())
+      return run_fused<4, 2, true>(W, meta, rows, cols, vals, nullptr, t_vals, t_meta, stream);
+    return run_fused<2, 4, true>(W, meta, rows, cols, vals, nullptr, t_vals, t_meta, stream);
+  }
+  // other widths: the gather, then the second pruning of its output
+  if (cudaError_t e = launch_gather24(W, meta, rows, cols, vals, stream)) return e;
+  return launch_double_prune24(vals, meta, rows, cols, t_vals, t_meta, stream);
+}
+
+template <typename TA, typename TB, typename TO>
+static cudaError_t run_axpby(float beta, const void* a, float gamma, const void* b, void* out, int64_t n,
+                             cudaStream_t stream) {
+  const int64_t n8 = n / 8;
+  int64_t blocks = (n8 + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attrs[1];
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  add_pdl_attr(cfg, attrs);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, axpby_kernel<TA, TB, TO>, beta, static_cast<const TA*>(a), gamma,
+                                     static_cast<const TB*>(b), static_cast<TO*>(out), n8);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_axpby(float beta, const void* a, int a_dt, float gamma, const void* b, int b_dt,
+                         void* out, int out_dt, int64_t n, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  using F = float;
+  using H = __nv_bfloat16;
+  const int key = a_dt * 4 + b_dt * 2 + out_dt;  // 0 = f32, 1 = bf16 each
+  switch (key) {
+    case 0: return run_axpby<F, F, F>(beta, a, gamma, b, out, n, stream);
+    case 1: return run_axpby<F, F, H>(beta, a, gamma, b, out, n, stream);
+    case 2: return run_axpby<F, H, F>(beta, a, gamma, b, out, n, stream);
+    case 3: return run_axpby<F, H, H>(beta, a, gamma, b, out, n, stream);
+    case 4: return run_axpby<H, F, F>(beta, a, gamma, b, out, n, stream);
+    case 5: return run_axpby<H, F, H>(beta, a, gamma, b, out, n, stream);
+    case 6: return run_axpby<H, H, F>(beta, a, gamma, b, out, n, stream);
+    default: return run_axpby<H, H, H>(beta, a, gamma, b, out, n, stream);
+  }
 }
 
 cudaError_t launch_double_prune24(const void* vals, const uint8_t* meta, int64_t rows,

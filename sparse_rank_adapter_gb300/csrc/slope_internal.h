@@ -44,6 +44,13 @@ cudaError_t launch_double_prune24(const void* vals, const uint8_t* meta, int64_t
 cudaError_t launch_prune_double24(const void* W, int64_t rows, int64_t cols, void* vals,
                                   uint8_t* meta, void* t_vals, uint8_t* t_meta,
                                   cudaStream_t stream);
+cudaError_t launch_gather24(const void* W, const uint8_t* meta, int64_t rows, int64_t cols, void* vals,
+                            cudaStream_t stream);
+cudaError_t launch_recompress_double24(const void* W, const uint8_t* meta, int64_t rows, int64_t cols,
+                                       void* vals, void* t_vals, uint8_t* t_meta, cudaStream_t stream);
+// dtype codes: 0 f32, 1 bf16
+cudaError_t launch_axpby(float beta, const void* a, int a_dt, float gamma, const void* b, int b_dt,
+                         void* out, int out_dt, int64_t n, cudaStream_t stream);
 
 // ---- tensor-core rate self test (mma_rate.cu): enqueues the launch and
 // writes the dense-equivalent flops it executes to *flops.

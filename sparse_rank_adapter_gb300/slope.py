@@ -30,6 +30,8 @@ SIGNATURES = (
     ("slope_prune_nm", _i, (_vp, _i64, _i64, _i, _i, _vp, _vp, _vp)),
     ("slope_double_prune", _i, (_vp, _vp, _i64, _i64, _vp, _vp, _vp)),
     ("slope_prune_and_double_prune", _i, (_vp, _i64, _i64, _i, _i, _vp, _vp, _vp, _vp, _vp)),
+    ("slope_recompress_double_prune", _i, (_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp)),
+    ("slope_sparse_axpby", _i, (ctypes.c_float, _vp, _i, ctypes.c_float, _vp, _i, _vp, _i, _i64, _vp)),
     ("slope_linear_fwd", _i, (_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _vp, _sz, _vp)),
     ("slope_linear_bwd_input", _i, (_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _vp, _sz, _vp)),
     ("slope_linear_bwd_weight", _i, (_vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _i, _vp, _u32, _vp, _vp, _vp, _sz, _vp)),
@@ -146,6 +148,37 @@ def slope_prune_and_double_prune(W, vals, meta, t_vals, t_meta, n: int = 2, m: i
         _ptr(t_vals, torch.bfloat16, (cols, rows // 2), "t_vals"),
         _ptr(t_meta, torch.uint8, (cols, rows // 8), "t_meta"), _stream(stream))
     _check(st, "slope_prune_and_double_prune")
+
+
+def slope_recompress_double_prune(W, meta, vals, t_vals, t_meta, stream=None):
+    """Re-compress the updated weight W at its kept mask `meta` into `vals`,
+    and write the second pruning of the result into (t_vals, t_meta)."""
+    import torch
+
+    rows, cols = W.shape
+    st = lib().slope_recompress_double_prune(
+        _ptr(W, torch.bfloat16, name="W"), _ptr(meta, torch.uint8, (rows, cols // 8), "meta"), rows, cols,
+        _ptr(vals, torch.bfloat16, (rows, cols // 2), "vals"),
+        _ptr(t_vals, torch.bfloat16, (cols, rows // 2), "t_vals"),
+        _ptr(t_meta, torch.uint8, (cols, rows // 8), "t_meta"), _stream(stream))
+    _check(st, "slope_recompress_double_prune")
+
+
+def slope_sparse_axpby(beta: float, A, gamma: float, B, out, stream=None):
+    """out = beta·A + gamma·B on the compressed values of matrices sharing a
+    2:4 pattern (fp32 or bf16 tensors of the same number of values)."""
+    import torch
+
+    n = out.numel()
+    if A.numel() != n or B.numel() != n:
+        raise ValueError("A, B and out must hold the same number of values")
+    for t, name in ((A, "A"), (B, "B"), (out, "out")):
+        if t.dtype not in (torch.float32, torch.bfloat16):
+            raise ValueError(f"{name} must be float32 or bfloat16, got {t.dtype}")
+    st = lib().slope_sparse_axpby(
+        float(beta), _ptr(A, None, name="A"), _dtype_code(A), float(gamma), _ptr(B, None, name="B"),
+        _dtype_code(B), _ptr(out, None, name="out"), _dtype_code(out), n, _stream(stream))
+    _check(st, "slope_sparse_axpby")
 
 
 def slope_linear_fwd(X, Wv, Wm, L, R, Y, XL=None, workspace=None, stream=None):

@@ -99,6 +99,22 @@ def test_prune_and_double_prune_argument_checks(L):
 
 
 @cpu_only
+def test_optimizer_side_argument_checks(L):
+    f = L.lib().slope_recompress_double_prune
+    assert f(A, A, 12, 16, A, A, A, None) == L.ERR_SHAPE
+    assert f(A, A, 16, 24, A, A, A, None) == L.ERR_SHAPE
+    assert f(A, None, 16, 16, A, A, A, None) == L.ERR_INVALID_ARG
+    assert f(A, A, 16, 16, A, A, MIS, None) == L.ERR_ALIGNMENT
+    g = L.lib().slope_sparse_axpby
+    assert g(1.0, A, 0, 1.0, A, 2, A, 0, 16, None) == L.ERR_INVALID_ARG  # unknown dtype
+    assert g(1.0, A, 0, 1.0, A, 0, A, 0, 12, None) == L.ERR_SHAPE        # n % 8
+    assert g(1.0, A, 0, 1.0, A, 0, A, 0, -8, None) == L.ERR_SHAPE
+    assert g(1.0, A, 0, 1.0, None, 0, A, 0, 16, None) == L.ERR_INVALID_ARG
+    assert g(1.0, A, 1, 1.0, A, 1, MIS, 1, 16, None) == L.ERR_ALIGNMENT
+    assert g(1.0, None, 0, 1.0, None, 0, None, 0, 0, None) == L.OK      # n == 0
+
+
+@cpu_only
 def test_linear_argument_checks(L):
     fwd = L.lib().slope_linear_fwd
     bi = L.lib().slope_linear_bwd_input
