@@ -213,7 +213,7 @@ def clock_sampler(device, index):
 class BlockStep:
     """Device buffers and the ordered ABI calls of one block step."""
 
-    def __init__(self, wl, seed: int, device, fused_prune: bool = False):
+    def __init__(self, wl, seed: int, device, fused_prune: bool = False, optimizer: bool = False):
         import torch
 
         from sparse_rank_adapter_gb300 import slope
@@ -221,6 +221,7 @@ class BlockStep:
         self.S = slope
         self.wl = wl
         self.fused_prune = fused_prune
+        self.optimizer = optimizer  # kept row mask: re-compression + A2, then beta·A + gamma·B
         T, r = wl.tokens, wl.rank
         self.layers = []
         for li, lin in enumerate(wl.linears):
@@ -245,6 +246,8 @@ class BlockStep:
                 dW=torch.empty(out, inp // 2, dtype=torch.float32, device=device),
                 dL=torch.empty(inp, r, dtype=torch.float32, device=device) if r else None,
                 dR=torch.empty(r, out, dtype=torch.float32, device=device) if r else None,
+                # the optimizer's fp32 master copy of the kept values
+                Wmaster=torch.empty(out, inp // 2, dtype=torch.float32, device=device) if optimizer else None,
                 inp=inp, out=out)
             self.layers.append(b)
 
@@ -257,10 +260,14 @@ class BlockStep:
         return ["Y", "dX", "dW", "dL", "dR"] if not self.wl.forward_only else ["Y"]
 
     def prepare(self, stream):
-        """Inference workloads take their weights pre-compressed: prune once here."""
-        if self.wl.forward_only:
+        """Inference workloads take their weights pre-compressed, and the
+        optimizer step keeps the mask chosen at initialisation: prune once
+        here (and fill the master copy from the kept values)."""
+        if self.wl.forward_only or self.optimizer:
             for b in self.layers:
                 self.S.slope_prune_nm(b["W"], b["Wv"], b["Wm"], stream=stream)
+                if self.optimizer:
+                    b["Wmaster"].copy_(b["Wv"].float())
 
     def run(self, stream, marks=None, only=None):
         """Issues the step on `stream` (or, with `only`, the calls of that one
@@ -273,6 +280,9 @@ class BlockStep:
         for b in (self.layers if only is None else [self.layers[only]]):
             if self.wl.forward_only:
                 calls = []
+            elif self.optimizer:  # the updated W at the kept mask, and the second pruning
+                calls = [("recompress_double", lambda b=b: S.slope_recompress_double_prune(
+                    b["W"], b["Wm"], b["Wv"], b["Dv"], b["Dm"], stream=stream))]
             elif self.fused_prune:  # A1 and A2 from one read of W
                 calls = [("prune_double", lambda b=b: S.slope_prune_and_double_prune(
                     b["W"], b["Wv"], b["Wm"], b["Dv"], b["Dm"], stream=stream))]
@@ -296,6 +306,9 @@ class BlockStep:
                         b["dY"], b["X"], b["Wm"], b["XL"], b["G"], b["dW"], b["dL"], b["dR"],
                         stream=stream)),
                 ]
+                if self.optimizer:  # decayed master values plus the scaled gradient, in place
+                    calls += [("axpby", lambda b=b: S.slope_sparse_axpby(
+                        0.9999, b["Wmaster"], -1e-3, b["dW"], b["Wmaster"], stream=stream))]
             for name, fn in calls:
                 if marks is not None:
                     e0, e1 = marks.new(name, b)
@@ -308,7 +321,8 @@ class BlockStep:
     def launches_per_step(self):
         n = 0
         for _ in self.layers:
-            n += 0 if self.wl.forward_only else (1 if self.fused_prune else 2)  # prune, double prune
+            n += 0 if self.wl.forward_only else (1 if self.fused_prune or self.optimizer else 2)  # prune(s)
+            n += 1 if self.optimizer else 0  # beta·A + gamma·B
             n += 2 if self.wl.rank else 1  # fwd: (XL) + sparse
             if not self.wl.forward_only:
                 n += 2 if self.wl.rank else 1  # bwd_input: (G) + sparse
@@ -369,6 +383,10 @@ def call_bytes(name, T, inp, out, r):
         return out * inp * (1.125 + 1.125)
     if name == "prune_double":  # W in once; both compressed formats out
         return out * inp * (2 + 1.125 + 1.125)
+    if name == "recompress_double":  # W and the kept metadata in; values, D values and metadata out
+        return out * inp * (2 + 0.125 + 1 + 1.125)
+    if name == "axpby":  # fp32 master and fp32 compressed dW in, master out
+        return out * inp / 2 * (4 + 4 + 4)
     return 0.0
 
 
@@ -421,7 +439,8 @@ def gpu_arm(args):
     wl = synth.WORKLOADS[args.workload]
     stream = torch.cuda.Stream(device=dev)
     n_sets = max(1, args.sets)
-    sets = [BlockStep(wl, seed=s + 10 * rank, device=dev, fused_prune=args.fused_prune) for s in range(n_sets)]
+    sets = [BlockStep(wl, seed=s + 10 * rank, device=dev, fused_prune=args.fused_prune, optimizer=args.optimizer)
+            for s in range(n_sets)]
     torch.cuda.synchronize()
 
     with torch.cuda.stream(stream):
@@ -504,7 +523,7 @@ def gpu_arm(args):
         byts = sum(fwd_bytes(T, i, o, r) for i, o, _ in per_call[dom]) / n_obs
         ach = byts / (calls_ms[dom] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm}
-    elif dom in ("prune", "double_prune", "prune_double"):
+    elif dom in ("prune", "double_prune", "prune_double", "recompress_double", "axpby"):
         alg = sum(call_bytes(dom, T, i, o, r) for i, o, _ in per_call[dom]) / n_obs
         ach = alg / (calls_ms[dom] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm}
@@ -516,7 +535,16 @@ def gpu_arm(args):
     kernel_of = {"prune": "prune24_kernel (slope_prune_nm)", "double_prune": "double_prune24_kernel (slope_double_prune)",
                  "fwd": "slope_linear_fwd (XL GEMM + sparse GEMM)", "bwd_input": "slope_linear_bwd_input (G GEMM + sparse GEMM)",
                  "bwd_weight": "dW GEMM with dL, dR (slope_linear_bwd_weight)",
-                 "prune_double": "prune_double24_kernel (slope_prune_and_double_prune)"}
+                 "prune_double": "prune_double24_kernel (slope_prune_and_double_prune)",
+                 "recompress_double": "prune_double24_kernel, kept mask (slope_recompress_double_prune)",
+                 "axpby": "axpby_kernel (slope_sparse_axpby)"}
+    # achieved bandwidth of every memory-bound call (algorithmic bytes over its time)
+    hbm_calls = {}
+    for name, obs in per_call.items():
+        byts = sum(call_bytes(name, T, i, o, r) for i, o, _ in obs) / n_obs
+        if byts > 0 and calls_ms.get(name):
+            gbs = byts / (calls_ms[name] * 1e-3) / 1e9
+            hbm_calls[name] = {"GB/s": round(gbs, 1), "frac": round(gbs / hbm, 3)}
     traffic = NCU_TRAFFIC.get((wl.name, dom))
     if traffic is not None:
         roof["traffic_unit"] = "bytes per launch"
@@ -549,10 +577,12 @@ def gpu_arm(args):
                        "linears": [f"{x.name}:{x.inp}->{x.out}" for x in wl.linears],
                        "l2": f"{n_sets} rotating input sets of {set_bytes(sets[0]) / 2**20:.0f} MiB (> L2 {L2_BYTES // 2**20} MiB)",
                        "graph": bool(args.graph), "parallelism": f"replicas x{world}",
-                       "prune": "one call (A1 + A2)" if args.fused_prune else "two calls (A1, A2)"},
+                       "prune": ("kept mask: re-compression + A2, then beta*A + gamma*B" if args.optimizer
+                                 else "one call (A1 + A2)" if args.fused_prune else "two calls (A1, A2)")},
             "pct_of_sparse_peak": round(100 * value / (2 * bf16), 2),
             "composite_roofline_frac": composite_frac(wl, ms_step, bf16_sus),
             "calls_ms_per_step": {k: round(v, 4) for k, v in calls_ms.items()},
+            "hbm_calls": hbm_calls,
             "roofline": roof, "clocks": clocks, "gpu_launches": sets[0].launches_per_step() * args.steps,
             "e2e": e2e, "cpu_baseline": cpu, "mma_rate_selftest": rates,
         }
@@ -742,6 +772,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-mma-rate", dest="mma_rate", action="store_false",
                     help="skip the tensor-core rate self test")
+    ap.add_argument("--optimizer", action="store_true",
+                    help="training step with the mask kept from initialisation: re-compression + A2 "
+                         "(slope_recompress_double_prune) in place of A1, A2, and beta*A + gamma*B "
+                         "(slope_sparse_axpby) on an fp32 master copy")
     ap.add_argument("--fused-prune", action="store_true",
                     help="A1 and A2 through the one-call slope_prune_and_double_prune")
     args = ap.parse_args()
