@@ -226,6 +226,26 @@ def recompress_double_prune24(bits: np.ndarray, meta: np.ndarray):
     return vals, t_vals, t_meta
 
 
+def double_prune24_frozen(vals: np.ndarray, meta: np.ndarray, rows: int, cols: int,
+                          t_meta: np.ndarray) -> np.ndarray:
+    """The second pruning with its column-wise mask frozen: the transpose of
+    the single-pruned matrix (pruned entries +0) re-compressed at the
+    positions a given transposed metadata ``t_meta`` (cols x rows/8) names,
+    with no new selection.  Returns t_vals (cols x rows/2)."""
+    ws = decompress24(vals, meta, cols)
+    return recompress24(np.ascontiguousarray(ws.T), t_meta)
+
+
+def recompress_frozen24(bits: np.ndarray, meta: np.ndarray, t_meta: np.ndarray):
+    """Both masks kept: the updated weight gathered at the row mask
+    (recompress24), and its transpose gathered at the frozen column mask
+    (double_prune24_frozen).  Returns (vals, t_vals)."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    rows, cols = bits.shape
+    vals = recompress24(bits, meta)
+    return vals, double_prune24_frozen(vals, meta, rows, cols, t_meta)
+
+
 def sparse_axpby24(beta: float, a_vals: np.ndarray, gamma: float, b_vals: np.ndarray,
                    meta: np.ndarray) -> np.ndarray:
     """beta·A + gamma·B of two rows x cols matrices that share the 2:4

@@ -435,3 +435,28 @@ def test_sparse_axpby_cases():
     c2 = O.sparse_axpby24(0.9, A, 0.0, B, meta) + O.sparse_axpby24(0.0, A, -0.01, B, meta)
     np.testing.assert_allclose(c1, c2, rtol=1e-14, atol=1e-15)
     np.testing.assert_allclose(c1, 0.9 * A - 0.01 * B, rtol=1e-14, atol=1e-15)
+
+
+def test_frozen_double_prune_fixed_point_and_gather():
+    """With the column mask frozen at what the second pruning selected, the
+    frozen variant returns the same values; with any other frozen mask each
+    value is the transposed single-pruned entry at the named position (zero
+    where the first pruning removed it)."""
+    W = synth.normal_bf16(0, 36, "W", (64, 48))
+    v, m, mask = O.prune24(W)
+    tv, tm, _ = O.double_prune24(v, m, 64, 48)
+    np.testing.assert_array_equal(O.double_prune24_frozen(v, m, 64, 48, tm), tv)
+    rng = np.random.default_rng(8)
+    codes = np.array(sorted(O.LEGAL_NIBBLES), dtype=np.uint8)
+    nib = rng.choice(codes, size=(48, 16))
+    tmf = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+    got = O.double_prune24_frozen(v, m, 64, 48, tmf)
+    ws = np.where(mask, W, 0).astype(np.uint16)
+    for i in range(48):
+        for g in range(16):
+            i0, i1 = nib[i, g] & 3, nib[i, g] >> 2
+            assert got[i, 2 * g] == ws[4 * g + i0, i]
+            assert got[i, 2 * g + 1] == ws[4 * g + i1, i]
+    vals, tvals = O.recompress_frozen24(W, m, tmf)
+    np.testing.assert_array_equal(vals, v)
+    np.testing.assert_array_equal(tvals, got)
