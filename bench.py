@@ -213,7 +213,8 @@ def clock_sampler(device, index):
 class BlockStep:
     """Device buffers and the ordered ABI calls of one block step."""
 
-    def __init__(self, wl, seed: int, device, fused_prune: bool = False, optimizer: bool = False):
+    def __init__(self, wl, seed: int, device, fused_prune: bool = False, optimizer: bool = False,
+                 frozen_columns: bool = False):
         import torch
 
         from sparse_rank_adapter_gb300 import slope
@@ -222,6 +223,7 @@ class BlockStep:
         self.wl = wl
         self.fused_prune = fused_prune
         self.optimizer = optimizer  # kept row mask: re-compression + A2, then beta·A + gamma·B
+        self.frozen_columns = frozen_columns  # the column mask kept too: no second selection
         T, r = wl.tokens, wl.rank
         self.layers = []
         for li, lin in enumerate(wl.linears):
@@ -265,7 +267,10 @@ class BlockStep:
         here (and fill the master copy from the kept values)."""
         if self.wl.forward_only or self.optimizer:
             for b in self.layers:
-                self.S.slope_prune_nm(b["W"], b["Wv"], b["Wm"], stream=stream)
+                if self.frozen_columns:  # both masks from initialisation
+                    self.S.slope_prune_and_double_prune(b["W"], b["Wv"], b["Wm"], b["Dv"], b["Dm"], stream=stream)
+                else:
+                    self.S.slope_prune_nm(b["W"], b["Wv"], b["Wm"], stream=stream)
                 if self.optimizer:
                     b["Wmaster"].copy_(b["Wv"].float())
 
@@ -280,6 +285,9 @@ class BlockStep:
         for b in (self.layers if only is None else [self.layers[only]]):
             if self.wl.forward_only:
                 calls = []
+            elif self.optimizer and self.frozen_columns:  # the updated W at both kept masks
+                calls = [("recompress_frozen", lambda b=b: S.slope_recompress_frozen(
+                    b["W"], b["Wm"], b["Dm"], b["Wv"], b["Dv"], stream=stream))]
             elif self.optimizer:  # the updated W at the kept mask, and the second pruning
                 calls = [("recompress_double", lambda b=b: S.slope_recompress_double_prune(
                     b["W"], b["Wm"], b["Wv"], b["Dv"], b["Dm"], stream=stream))]
@@ -385,6 +393,8 @@ def call_bytes(name, T, inp, out, r):
         return out * inp * (2 + 1.125 + 1.125)
     if name == "recompress_double":  # W and the kept metadata in; values, D values and metadata out
         return out * inp * (2 + 0.125 + 1 + 1.125)
+    if name == "recompress_frozen":  # W and both metadata in; values and D values out
+        return out * inp * (2 + 0.125 + 0.125 + 1 + 1)
     if name == "axpby":  # fp32 master and fp32 compressed dW in, master out
         return out * inp / 2 * (4 + 4 + 4)
     return 0.0
@@ -439,8 +449,8 @@ def gpu_arm(args):
     wl = synth.WORKLOADS[args.workload]
     stream = torch.cuda.Stream(device=dev)
     n_sets = max(1, args.sets)
-    sets = [BlockStep(wl, seed=s + 10 * rank, device=dev, fused_prune=args.fused_prune, optimizer=args.optimizer)
-            for s in range(n_sets)]
+    sets = [BlockStep(wl, seed=s + 10 * rank, device=dev, fused_prune=args.fused_prune, optimizer=args.optimizer,
+                      frozen_columns=args.frozen_columns) for s in range(n_sets)]
     torch.cuda.synchronize()
 
     with torch.cuda.stream(stream):
@@ -523,7 +533,7 @@ def gpu_arm(args):
         byts = sum(fwd_bytes(T, i, o, r) for i, o, _ in per_call[dom]) / n_obs
         ach = byts / (calls_ms[dom] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm}
-    elif dom in ("prune", "double_prune", "prune_double", "recompress_double", "axpby"):
+    elif dom in ("prune", "double_prune", "prune_double", "recompress_double", "recompress_frozen", "axpby"):
         alg = sum(call_bytes(dom, T, i, o, r) for i, o, _ in per_call[dom]) / n_obs
         ach = alg / (calls_ms[dom] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm}
@@ -537,6 +547,7 @@ def gpu_arm(args):
                  "bwd_weight": "dW GEMM with dL, dR (slope_linear_bwd_weight)",
                  "prune_double": "prune_double24_kernel (slope_prune_and_double_prune)",
                  "recompress_double": "prune_double24_kernel, kept mask (slope_recompress_double_prune)",
+                 "recompress_frozen": "prune_double24_kernel, both masks kept (slope_recompress_frozen)",
                  "axpby": "axpby_kernel (slope_sparse_axpby)"}
     # achieved bandwidth of every memory-bound call (algorithmic bytes over its time)
     hbm_calls = {}
@@ -577,7 +588,9 @@ def gpu_arm(args):
                        "linears": [f"{x.name}:{x.inp}->{x.out}" for x in wl.linears],
                        "l2": f"{n_sets} rotating input sets of {set_bytes(sets[0]) / 2**20:.0f} MiB (> L2 {L2_BYTES // 2**20} MiB)",
                        "graph": bool(args.graph), "parallelism": f"replicas x{world}",
-                       "prune": ("kept mask: re-compression + A2, then beta*A + gamma*B" if args.optimizer
+                       "prune": ("both masks kept: re-compression, then beta*A + gamma*B"
+                                 if args.optimizer and args.frozen_columns
+                                 else "kept mask: re-compression + A2, then beta*A + gamma*B" if args.optimizer
                                  else "one call (A1 + A2)" if args.fused_prune else "two calls (A1, A2)")},
             "pct_of_sparse_peak": round(100 * value / (2 * bf16), 2),
             "composite_roofline_frac": composite_frac(wl, ms_step, bf16_sus),
@@ -776,6 +789,9 @@ def main():
                     help="training step with the mask kept from initialisation: re-compression + A2 "
                          "(slope_recompress_double_prune) in place of A1, A2, and beta*A + gamma*B "
                          "(slope_sparse_axpby) on an fp32 master copy")
+    ap.add_argument("--frozen-columns", action="store_true",
+                    help="with --optimizer: the column mask kept from initialisation too "
+                         "(slope_recompress_frozen in place of the re-compression + A2)")
     ap.add_argument("--fused-prune", action="store_true",
                     help="A1 and A2 through the one-call slope_prune_and_double_prune")
     args = ap.parse_args()

@@ -146,6 +146,29 @@ int slope_recompress_double_prune(const void* W, const uint8_t* meta, int64_t ro
                                   void* vals, void* t_vals, uint8_t* t_meta, void* stream);
 
 /*
+ * A2 with its column-wise mask frozen (§2.1: the transposed mask may be
+ * re-derived or kept; this is the kept form): `t_vals` (cols x rows/2 bf16)
+ * receives the transpose of the single-pruned matrix (vals, meta) gathered
+ * at the positions the given `t_meta` (cols x rows/8, e.g. an earlier
+ * slope_double_prune output) names, with no new selection; a position the
+ * first pruning removed gives +0.  `t_meta` is read only.  Size rules as
+ * slope_double_prune.
+ */
+int slope_double_prune_frozen(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols,
+                              const uint8_t* t_meta, void* t_vals, void* stream);
+
+/*
+ * Optimizer side with both masks kept: the updated weight W gathered at the
+ * row mask `meta` into `vals` (as slope_recompress_double_prune does), and
+ * its transpose gathered at the column mask `t_meta` into `t_vals` (as
+ * slope_double_prune_frozen does), in one pass over W for cols % 128 == 0.
+ * `meta` and `t_meta` are read only.  Size rules as
+ * slope_recompress_double_prune.
+ */
+int slope_recompress_frozen(const void* W, const uint8_t* meta, const uint8_t* t_meta, int64_t rows,
+                            int64_t cols, void* vals, void* t_vals, void* stream);
+
+/*
  * Optimizer side, sparse linear combination (App. K: beta·A + gamma·B for
  * matrices that share a sparsity pattern, for weight decay).  A, B and out
  * are the compressed value arrays (n values each, e.g. rows x cols/2) of

@@ -282,6 +282,31 @@ extern "C" int slope_recompress_double_prune(const void* W, const uint8_t* meta,
                                               static_cast<cudaStream_t>(stream)));
 }
 
+extern "C" int slope_double_prune_frozen(const void* vals, const uint8_t* meta, int64_t rows,
+                                         int64_t cols, const uint8_t* t_meta, void* t_vals,
+                                         void* stream) {
+  if (rows <= 0 || cols <= 0 || rows % 8 != 0 || cols % 16 != 0) return SLOPE_ERR_SHAPE;
+  if (!vals || !meta || !t_meta || !t_vals) return SLOPE_ERR_INVALID_ARG;
+  if (!aligned16(vals) || !aligned16(meta) || !aligned16(t_meta) || !aligned16(t_vals))
+    return SLOPE_ERR_ALIGNMENT;
+  if (int s = check_device()) return s;
+  return from_cuda(launch_double_prune24_frozen(vals, meta, rows, cols, t_meta, t_vals,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int slope_recompress_frozen(const void* W, const uint8_t* meta, const uint8_t* t_meta,
+                                       int64_t rows, int64_t cols, void* vals, void* t_vals,
+                                       void* stream) {
+  if (rows <= 0 || cols <= 0 || rows % 8 != 0 || cols % 16 != 0) return SLOPE_ERR_SHAPE;
+  if (!W || !meta || !t_meta || !vals || !t_vals) return SLOPE_ERR_INVALID_ARG;
+  if (!aligned16(W) || !aligned16(meta) || !aligned16(t_meta) || !aligned16(vals) ||
+      !aligned16(t_vals))
+    return SLOPE_ERR_ALIGNMENT;
+  if (int s = check_device()) return s;
+  return from_cuda(launch_recompress_frozen24(W, meta, t_meta, rows, cols, vals, t_vals,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 extern "C" int slope_sparse_axpby(float beta, const void* A, int a_dtype, float gamma,
                                   const void* B, int b_dtype, void* out, int out_dtype, int64_t n,
                                   void* stream) {

@@ -162,16 +162,32 @@ __global__ void __launch_bounds__(kPruneThreads) prune24_kernel(const uint4* __r
 // column octet h8.  Lanes of a warp take consecutive octets of the same
 // chunk, so each output row segment a warp writes is 256 B (values) / 32 B
 // (metadata) contiguous.
-template <int Q>
+// FROZEN: the transposed metadata is an input (the column-wise mask is
+// kept): each transposed group takes the two positions its byte of
+// `t_meta_in` names, through the byte-permute selector of the nibble, and
+// no metadata is written.
+template <int Q, bool FROZEN = false>
 __device__ __forceinline__ void transpose_prune_octet(const uint32_t (&pw)[8][Q], const uint32_t (&m)[8],
                                                       const DpTables& tab,
                                                       uint2* __restrict__ t_vals,
                                                       uint8_t* __restrict__ t_meta,
                                                       int64_t out_stride, uint32_t h8,
-                                                      uint32_t c16, uint32_t k17, int q0) {
+                                                      uint32_t c16, uint32_t k17, int q0,
+                                                      const uint8_t* __restrict__ t_meta_in = nullptr) {
   const uint32_t k1 = k17 >> 16, k8 = k17 >> 14;
-  uint2* tv = t_vals + (16 * static_cast<int64_t>(c16) + 4 * q0) * out_stride + h8;
-  uint8_t* tm = t_meta + (16 * static_cast<int64_t>(c16) + 4 * q0) * out_stride + h8;
+  const int64_t first = (16 * static_cast<int64_t>(c16) + 4 * q0) * out_stride + h8;
+  uint2* tv = t_vals + first;
+  uint8_t* tm = FROZEN ? nullptr : t_meta + first;
+  // FROZEN: the given bytes of all this thread's output rows, loaded up
+  // front so that their latency overlaps the expansion below
+  uint32_t dmv[Q][4];
+  if constexpr (FROZEN) {
+    const uint8_t* tmi = t_meta_in + first;
+#pragma unroll
+    for (int q = 0; q < Q; ++q)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) dmv[q][j] = tmi[(4 * q + j) * out_stride];
+  }
 #pragma unroll
   for (int q = 0; q < Q; ++q) {  // group of 4 columns
     uint32_t e0[8], e1[8];        // row k, columns 0-1 / 2-3 of the group
@@ -190,12 +206,19 @@ __device__ __forceinline__ void transpose_prune_octet(const uint32_t (&pw)[8][Q]
       const uint32_t pick = (j & 1) ? 0x7632u : 0x5410u;  // high or low halves of two words
       const uint32_t a01 = __byte_perm(e[0], e[1], pick), a23 = __byte_perm(e[2], e[3], pick);
       const uint32_t b01 = __byte_perm(e[4], e[5], pick), b23 = __byte_perm(e[6], e[7], pick);
-      const uint32_t ea = top2_entry(a01, a23, tab.out[0], k17, k1);
-      const uint32_t eb = top2_entry(b01, b23, tab.out[1], k17, k1);
       const int64_t i = 4 * q + j;
+      uint32_t ea, eb;
+      if constexpr (FROZEN) {
+        const uint32_t dm = dmv[q][j];  // low nibble: rows 0-3 of the octet
+        ea = tab.gather[dm & 15u];
+        eb = tab.gather[dm >> 4];
+      } else {
+        ea = top2_entry(a01, a23, tab.out[0], k17, k1);
+        eb = top2_entry(b01, b23, tab.out[1], k17, k1);
+      }
       __stcs(tv + i * out_stride, make_uint2(__byte_perm(a01, a23, ea), __byte_perm(b01, b23, eb)));
       // the selectors stay below 0x8000, so the sum carries nothing into the nibbles
-      tm[i * out_stride] = static_cast<uint8_t>((ea + eb) >> 16);
+      if constexpr (!FROZEN) tm[i * out_stride] = static_cast<uint8_t>((ea + eb) >> 16);
     }
   }
 }
@@ -203,9 +226,11 @@ __device__ __forceinline__ void transpose_prune_octet(const uint32_t (&pw)[8][Q]
 // Any shape (rows % 8 == 0, cols % 16 == 0): each thread loads its octet's
 // rows straight from global memory; the eight warps of a block take
 // adjacent chunks, whose loads share sectors in L1.
+template <bool FROZEN>
 __global__ void __launch_bounds__(kDpThreads) double_prune24_kernel(
     const uint4* __restrict__ vals, const uint16_t* __restrict__ meta, uint2* __restrict__ t_vals,
-    uint8_t* __restrict__ t_meta, int64_t rows, int64_t cols, uint32_t k17) {
+    uint8_t* __restrict__ t_meta, int64_t rows, int64_t cols, uint32_t k17,
+    const uint8_t* __restrict__ t_meta_in) {
   __shared__ DpTables tab;
   fill_tables(tab);
   __syncthreads();
@@ -227,7 +252,7 @@ __global__ void __launch_bounds__(kDpThreads) double_prune24_kernel(
       pw[k][0] = v.x; pw[k][1] = v.y; pw[k][2] = v.z; pw[k][3] = v.w;
       m[k] = __ldg(meta + at);
     }
-    transpose_prune_octet<4>(pw, m, tab, t_vals, t_meta, rows / 8, h8, c16, k17, 0);
+    transpose_prune_octet<4, FROZEN>(pw, m, tab, t_vals, t_meta, rows / 8, h8, c16, k17, 0, t_meta_in);
   }
 }
 
@@ -263,10 +288,11 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
-template <int CH, int QS>
+template <int CH, int QS, bool FROZEN>
 __global__ void __launch_bounds__(32 * CH * QS) double_prune24_staged_kernel(
     const uint8_t* __restrict__ vals, const uint8_t* __restrict__ meta, uint2* __restrict__ t_vals,
-    uint8_t* __restrict__ t_meta, int64_t rows, int64_t cols, uint32_t k17) {
+    uint8_t* __restrict__ t_meta, int64_t rows, int64_t cols, uint32_t k17,
+    const uint8_t* __restrict__ t_meta_in) {
   using C = DpStaged<CH, QS>;
   constexpr int kQ = 4 / QS;  // groups of 4 columns per thread
   extern __shared__ __align__(128) uint8_t smem[];
@@ -342,7 +368,8 @@ __global__ void __launch_bounds__(32 * CH * QS) double_prune24_staged_kernel(
         m[k] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(st + C::kValBytes + k * 512 +
                                                                           lane * 16 + moff + 2 * warp)) >> (4 * q0);
       }
-      transpose_prune_octet<kQ>(pw, m, tab, t_vals, t_meta, rows / 8, h8, ch0 + warp, k17, q0);
+      transpose_prune_octet<kQ, FROZEN>(pw, m, tab, t_vals, t_meta, rows / 8, h8, ch0 + warp, k17, q0,
+                                        t_meta_in);
     }
     __syncthreads();
     th = nh;
@@ -376,11 +403,11 @@ struct FusedCfg {
   static constexpr int kMinBlocks = CH == 8 ? 2 : 3;
 };
 
-template <int CH, int QS, bool GIVEN>
+template <int CH, int QS, bool GIVEN, bool FROZEN>
 __global__ void __launch_bounds__(32 * CH * QS, (FusedCfg<CH, QS, GIVEN>::kMinBlocks)) prune_double24_kernel(
     const uint4* __restrict__ W, const uint8_t* __restrict__ meta_in, uint2* __restrict__ vals,
     uint8_t* __restrict__ meta, uint2* __restrict__ t_vals, uint8_t* __restrict__ t_meta, int64_t rows,
-    int64_t cols, uint32_t k17) {
+    int64_t cols, uint32_t k17, const uint8_t* __restrict__ t_meta_in) {
   using C = DpStaged<CH, QS>;
   using F = FusedCfg<CH, QS, GIVEN>;
   constexpr int kQ = 4 / QS;                     // groups of 4 columns per thread in phase 2
@@ -478,7 +505,8 @@ __global__ void __launch_bounds__(32 * CH * QS, (FusedCfg<CH, QS, GIVEN>::kMinBl
         m[k] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(st + C::kValBytes + k * 512 +
                                                                           lane * 16 + 2 * warp)) >> (4 * q0);
       }
-      transpose_prune_octet<kQ>(pw, m, tab, t_vals, t_meta, rows / 8, h8, tc * CH + warp, k17, q0);
+      transpose_prune_octet<kQ, FROZEN>(pw, m, tab, t_vals, t_meta, rows / 8, h8, tc * CH + warp, k17, q0,
+                                        t_meta_in);
     }
     th = nh;
     tc = nc;
@@ -596,11 +624,12 @@ cudaError_t launch_prune24(const void* W, int64_t rows, int64_t cols, void* vals
 }
 
 
-template <int CH, int QS>
+template <int CH, int QS, bool FROZEN = false>
 static cudaError_t run_staged(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols,
-                              void* t_vals, uint8_t* t_meta, cudaStream_t stream) {
+                              void* t_vals, uint8_t* t_meta, const uint8_t* t_meta_in,
+                              cudaStream_t stream) {
   using C = DpStaged<CH, QS>;
-  auto kernel = double_prune24_staged_kernel<CH, QS>;
+  auto kernel = double_prune24_staged_kernel<CH, QS, FROZEN>;
   static std::atomic<int> per_sm[64];
   int per = 0;
   if (cudaError_t e = blocks_per_sm(kernel, C::kThreads, C::kSmem, per_sm, per)) return e;
@@ -615,17 +644,17 @@ static cudaError_t run_staged(const void* vals, const uint8_t* meta, int64_t row
   cfg.stream = stream;
   add_pdl_attr(cfg, attrs);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<const uint8_t*>(vals), meta,
-                                     static_cast<uint2*>(t_vals), t_meta, rows, cols, kKeyShift);
+                                     static_cast<uint2*>(t_vals), t_meta, rows, cols, kKeyShift, t_meta_in);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int CH, int QS, bool GIVEN = false>
+template <int CH, int QS, bool GIVEN = false, bool FROZEN = false>
 static cudaError_t run_fused(const void* W, const uint8_t* meta_in, int64_t rows, int64_t cols,
                              void* vals, uint8_t* meta, void* t_vals, uint8_t* t_meta,
-                             cudaStream_t stream) {
+                             const uint8_t* t_meta_in, cudaStream_t stream) {
   using C = DpStaged<CH, QS>;
   using F = FusedCfg<CH, QS, GIVEN>;
-  auto kernel = prune_double24_kernel<CH, QS, GIVEN>;
+  auto kernel = prune_double24_kernel<CH, QS, GIVEN, FROZEN>;
   static std::atomic<int> per_sm[64];
   int per = 0;
   if (cudaError_t e = blocks_per_sm(kernel, C::kThreads, F::kSmem, per_sm, per)) return e;
@@ -641,7 +670,7 @@ static cudaError_t run_fused(const void* W, const uint8_t* meta_in, int64_t rows
   add_pdl_attr(cfg, attrs);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<const uint4*>(W), meta_in,
                                      static_cast<uint2*>(vals), meta, static_cast<uint2*>(t_vals), t_meta,
-                                     rows, cols, kKeyShift);
+                                     rows, cols, kKeyShift, t_meta_in);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -652,10 +681,10 @@ cudaError_t launch_prune_double24(const void* W, int64_t rows, int64_t cols, voi
   if (cols % 128 == 0) {  // tile widths as A2's staged kernel
     const int64_t tiles_h = (rows + 255) / 256;
     if (tiles_h * (cols / 128) >= sm_count())
-      return run_fused<8, 1>(W, nullptr, rows, cols, vals, meta, t_vals, t_meta, stream);
+      return run_fused<8, 1>(W, nullptr, rows, cols, vals, meta, t_vals, t_meta, nullptr, stream);
     if (tiles_h * (cols / 64) >= sm_count())
-      return run_fused<4, 2>(W, nullptr, rows, cols, vals, meta, t_vals, t_meta, stream);
-    return run_fused<2, 4>(W, nullptr, rows, cols, vals, meta, t_vals, t_meta, stream);
+      return run_fused<4, 2>(W, nullptr, rows, cols, vals, meta, t_vals, t_meta, nullptr, stream);
+    return run_fused<2, 4>(W, nullptr, rows, cols, vals, meta, t_vals, t_meta, nullptr, stream);
   }
   // other widths: the two kernels one after the other
   if (cudaError_t e = launch_prune24(W, rows, cols, vals, meta, stream)) return e;
@@ -686,10 +715,10 @@ cudaError_t launch_recompress_double24(const void* W, const uint8_t* meta, int64
   if (cols % 128 == 0) {
     const int64_t tiles_h = (rows + 255) / 256;
     if (tiles_h * (cols / 128) >= sm_count())
-      return run_fused<8, 1, true>(W, meta, rows, cols, vals, nullptr, t_vals, t_meta, stream);
+      return run_fused<8, 1, true>(W, meta, rows, cols, vals, nullptr, t_vals, t_meta, nullptr, stream);
     if (tiles_h * (cols / 64) >= sm_count())
-      return run_fused<4, 2, true>(W, meta, rows, cols, vals, nullptr, t_vals, t_meta, stream);
-    return run_fused<2, 4, true>(W, meta, rows, cols, vals, nullptr, t_vals, t_meta, stream);
+      return run_fused<4, 2, true>(W, meta, rows, cols, vals, nullptr, t_vals, t_meta, nullptr, stream);
+    return run_fused<2, 4, true>(W, meta, rows, cols, vals, nullptr, t_vals, t_meta, nullptr, stream);
   }
   // other widths: the gather, then the second pruning of its output
   if (cudaError_t e = launch_gather24(W, meta, rows, cols, vals, stream)) return e;
@@ -732,19 +761,20 @@ cudaError_t launch_axpby(float beta, const void* a, int a_dt, float gamma, const
   }
 }
 
-cudaError_t launch_double_prune24(const void* vals, const uint8_t* meta, int64_t rows,
-                                  int64_t cols, void* t_vals, uint8_t* t_meta,
-                                  cudaStream_t stream) {
+template <bool FROZEN>
+static cudaError_t double_prune24_any(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols,
+                                      void* t_vals, uint8_t* t_meta, const uint8_t* t_meta_in,
+                                      cudaStream_t stream) {
   if (rows == 0 || cols == 0) return cudaSuccess;
   if (cols % 128 == 0) {
     // the widest tile that still gives every SM a tile
     const int64_t tiles_h = (rows + 255) / 256;
     // (narrower tiles split each octet's columns over more threads)
     if (tiles_h * (cols / 128) >= sm_count())
-      return run_staged<8, 1>(vals, meta, rows, cols, t_vals, t_meta, stream);
+      return run_staged<8, 1, FROZEN>(vals, meta, rows, cols, t_vals, t_meta, t_meta_in, stream);
     if (tiles_h * (cols / 64) >= sm_count())
-      return run_staged<4, 2>(vals, meta, rows, cols, t_vals, t_meta, stream);
-    return run_staged<2, 4>(vals, meta, rows, cols, t_vals, t_meta, stream);
+      return run_staged<4, 2, FROZEN>(vals, meta, rows, cols, t_vals, t_meta, t_meta_in, stream);
+    return run_staged<2, 4, FROZEN>(vals, meta, rows, cols, t_vals, t_meta, t_meta_in, stream);
   }
   const int64_t tiles = ((rows / 8 + 31) / 32) * ((cols / 16 + 7) / 8);
   int64_t blocks = tiles;
@@ -756,10 +786,38 @@ cudaError_t launch_double_prune24(const void* vals, const uint8_t* meta, int64_t
   cfg.blockDim = dim3(kDpThreads);
   cfg.stream = stream;
   add_pdl_attr(cfg, attrs);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, double_prune24_kernel, static_cast<const uint4*>(vals),
+  cudaError_t e = cudaLaunchKernelEx(&cfg, double_prune24_kernel<FROZEN>, static_cast<const uint4*>(vals),
                                      reinterpret_cast<const uint16_t*>(meta),
-                                     static_cast<uint2*>(t_vals), t_meta, rows, cols, kKeyShift);
+                                     static_cast<uint2*>(t_vals), t_meta, rows, cols, kKeyShift, t_meta_in);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_double_prune24(const void* vals, const uint8_t* meta, int64_t rows,
+                                  int64_t cols, void* t_vals, uint8_t* t_meta,
+                                  cudaStream_t stream) {
+  return double_prune24_any<false>(vals, meta, rows, cols, t_vals, t_meta, nullptr, stream);
+}
+
+cudaError_t launch_double_prune24_frozen(const void* vals, const uint8_t* meta, int64_t rows,
+                                         int64_t cols, const uint8_t* t_meta, void* t_vals,
+                                         cudaStream_t stream) {
+  return double_prune24_any<true>(vals, meta, rows, cols, t_vals, nullptr, t_meta, stream);
+}
+
+cudaError_t launch_recompress_frozen24(const void* W, const uint8_t* meta, const uint8_t* t_meta,
+                                       int64_t rows, int64_t cols, void* vals, void* t_vals,
+                                       cudaStream_t stream) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  if (cols % 128 == 0) {
+    const int64_t tiles_h = (rows + 255) / 256;
+    if (tiles_h * (cols / 128) >= sm_count())
+      return run_fused<8, 1, true, true>(W, meta, rows, cols, vals, nullptr, t_vals, nullptr, t_meta, stream);
+    if (tiles_h * (cols / 64) >= sm_count())
+      return run_fused<4, 2, true, true>(W, meta, rows, cols, vals, nullptr, t_vals, nullptr, t_meta, stream);
+    return run_fused<2, 4, true, true>(W, meta, rows, cols, vals, nullptr, t_vals, nullptr, t_meta, stream);
+  }
+  if (cudaError_t e = launch_gather24(W, meta, rows, cols, vals, stream)) return e;
+  return launch_double_prune24_frozen(vals, meta, rows, cols, t_meta, t_vals, stream);
 }
 
 }  // namespace slope

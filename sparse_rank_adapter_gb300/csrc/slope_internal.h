@@ -48,6 +48,12 @@ cudaError_t launch_gather24(const void* W, const uint8_t* meta, int64_t rows, in
                             cudaStream_t stream);
 cudaError_t launch_recompress_double24(const void* W, const uint8_t* meta, int64_t rows, int64_t cols,
                                        void* vals, void* t_vals, uint8_t* t_meta, cudaStream_t stream);
+cudaError_t launch_double_prune24_frozen(const void* vals, const uint8_t* meta, int64_t rows,
+                                         int64_t cols, const uint8_t* t_meta, void* t_vals,
+                                         cudaStream_t stream);
+cudaError_t launch_recompress_frozen24(const void* W, const uint8_t* meta, const uint8_t* t_meta,
+                                       int64_t rows, int64_t cols, void* vals, void* t_vals,
+                                       cudaStream_t stream);
 // dtype codes: 0 f32, 1 bf16
 cudaError_t launch_axpby(float beta, const void* a, int a_dt, float gamma, const void* b, int b_dt,
                          void* out, int out_dt, int64_t n, cudaStream_t stream);

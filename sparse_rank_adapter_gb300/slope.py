@@ -31,6 +31,8 @@ SIGNATURES = (
     ("slope_double_prune", _i, (_vp, _vp, _i64, _i64, _vp, _vp, _vp)),
     ("slope_prune_and_double_prune", _i, (_vp, _i64, _i64, _i, _i, _vp, _vp, _vp, _vp, _vp)),
     ("slope_recompress_double_prune", _i, (_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp)),
+    ("slope_double_prune_frozen", _i, (_vp, _vp, _i64, _i64, _vp, _vp, _vp)),
+    ("slope_recompress_frozen", _i, (_vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp)),
     ("slope_sparse_axpby", _i, (ctypes.c_float, _vp, _i, ctypes.c_float, _vp, _i, _vp, _i, _i64, _vp)),
     ("slope_linear_fwd", _i, (_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _vp, _sz, _vp)),
     ("slope_linear_bwd_input", _i, (_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _vp, _sz, _vp)),
@@ -162,6 +164,31 @@ def slope_recompress_double_prune(W, meta, vals, t_vals, t_meta, stream=None):
         _ptr(t_vals, torch.bfloat16, (cols, rows // 2), "t_vals"),
         _ptr(t_meta, torch.uint8, (cols, rows // 8), "t_meta"), _stream(stream))
     _check(st, "slope_recompress_double_prune")
+
+
+def slope_double_prune_frozen(vals, meta, rows: int, cols: int, t_meta, t_vals, stream=None):
+    """A2 with the column mask frozen: the transpose of (vals, meta) gathered
+    at the given t_meta into t_vals."""
+    import torch
+
+    st = lib().slope_double_prune_frozen(
+        _ptr(vals, torch.bfloat16, (rows, cols // 2), "vals"), _ptr(meta, torch.uint8, (rows, cols // 8), "meta"),
+        rows, cols, _ptr(t_meta, torch.uint8, (cols, rows // 8), "t_meta"),
+        _ptr(t_vals, torch.bfloat16, (cols, rows // 2), "t_vals"), _stream(stream))
+    _check(st, "slope_double_prune_frozen")
+
+
+def slope_recompress_frozen(W, meta, t_meta, vals, t_vals, stream=None):
+    """Both masks kept: W gathered at meta into vals, its transpose at t_meta into t_vals."""
+    import torch
+
+    rows, cols = W.shape
+    st = lib().slope_recompress_frozen(
+        _ptr(W, torch.bfloat16, name="W"), _ptr(meta, torch.uint8, (rows, cols // 8), "meta"),
+        _ptr(t_meta, torch.uint8, (cols, rows // 8), "t_meta"), rows, cols,
+        _ptr(vals, torch.bfloat16, (rows, cols // 2), "vals"),
+        _ptr(t_vals, torch.bfloat16, (cols, rows // 2), "t_vals"), _stream(stream))
+    _check(st, "slope_recompress_frozen")
 
 
 def slope_sparse_axpby(beta: float, A, gamma: float, B, out, stream=None):

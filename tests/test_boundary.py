@@ -105,6 +105,14 @@ def test_optimizer_side_argument_checks(L):
     assert f(A, A, 16, 24, A, A, A, None) == L.ERR_SHAPE
     assert f(A, None, 16, 16, A, A, A, None) == L.ERR_INVALID_ARG
     assert f(A, A, 16, 16, A, A, MIS, None) == L.ERR_ALIGNMENT
+    h = L.lib().slope_double_prune_frozen
+    assert h(A, A, 12, 16, A, A, None) == L.ERR_SHAPE
+    assert h(A, A, 16, 16, None, A, None) == L.ERR_INVALID_ARG
+    assert h(A, A, 16, 16, A, MIS, None) == L.ERR_ALIGNMENT
+    k = L.lib().slope_recompress_frozen
+    assert k(A, A, A, 16, 24, A, A, None) == L.ERR_SHAPE
+    assert k(A, A, None, 16, 16, A, A, None) == L.ERR_INVALID_ARG
+    assert k(A, A, A, 16, 16, MIS, A, None) == L.ERR_ALIGNMENT
     g = L.lib().slope_sparse_axpby
     assert g(1.0, A, 0, 1.0, A, 2, A, 0, 16, None) == L.ERR_INVALID_ARG  # unknown dtype
     assert g(1.0, A, 0, 1.0, A, 0, A, 0, 12, None) == L.ERR_SHAPE        # n % 8

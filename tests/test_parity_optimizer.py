@@ -2,6 +2,9 @@
 
 slope_recompress_double_prune: an updated weight re-compressed at the kept
 row mask and double-pruned again; values and metadata bit-exact.
+slope_double_prune_frozen / slope_recompress_frozen: the second pruning
+with its column mask kept (and, for the latter, the row mask too); values
+bit-exact.
 slope_sparse_axpby: beta·A + gamma·B on compressed values, every
 combination of fp32 and bf16 arrays, within the rounding the call states
 (fp32 arithmetic, then one rounding to the output type)."""
@@ -141,3 +144,51 @@ def test_sparse_axpby_in_place(S):
     ref = 0.5 * A + 2.0 * B
     S.slope_sparse_axpby(0.5, A, 2.0, B, A)  # out is A
     torch.testing.assert_close(A, ref, rtol=2e-7, atol=1e-7)
+
+
+def random_legal_meta(rng, rows, cols):
+    codes = np.array(sorted(O.LEGAL_NIBBLES), dtype=np.uint8)
+    nib = rng.choice(codes, size=(rows, cols // 4))
+    return (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+
+
+@pytest.mark.parametrize("rows,cols", SHAPES)
+def test_frozen_column_mask_bit_exact(S, rows, cols):
+    """An updated weight under both kept masks (the row mask from A1 of the
+    old weight, a column mask drawn at random among legal ones): the
+    frozen second pruning of its compressed form, and the one-pass form
+    from W, both against the oracle."""
+    import torch
+
+    rng = np.random.default_rng(rows * 3 + cols)
+    W0 = synth.normal_bf16(0, rows + 5 * cols, "W", (rows, cols))
+    _, meta, _ = O.prune24(W0)
+    t_meta = random_legal_meta(rng, cols, rows)
+    W1 = synth.normal_bf16(1, rows + 5 * cols, "W", (rows, cols))
+    ov, otv = O.recompress_frozen24(W1, meta, t_meta)
+    vals = torch.empty(rows, cols // 2, dtype=torch.bfloat16, device="cuda")
+    tv = torch.empty(cols, rows // 2, dtype=torch.bfloat16, device="cuda")
+    S.slope_recompress_frozen(to_dev(W1), u8_to_dev(meta), u8_to_dev(t_meta), vals, tv)
+    np.testing.assert_array_equal(bits_of(vals), ov)
+    np.testing.assert_array_equal(bits_of(tv), otv)
+    tv2 = torch.empty_like(tv)
+    S.slope_double_prune_frozen(to_dev(ov), u8_to_dev(meta), rows, cols, u8_to_dev(t_meta), tv2)
+    np.testing.assert_array_equal(bits_of(tv2), otv)
+
+
+@pytest.mark.parametrize("rows,cols", [(10240, 2560), (28672, 7168)])
+def test_frozen_at_own_masks_block_shapes(S, rows, cols):
+    """Full-size weights: frozen at the masks A1 and A2 chose, both forms
+    reproduce the selecting calls' values in full."""
+    import torch
+
+    W = to_dev(synth.normal_bf16(0, 4, "W", (rows, cols)))
+    vals = torch.empty(rows, cols // 2, dtype=torch.bfloat16, device="cuda")
+    meta = torch.empty(rows, cols // 8, dtype=torch.uint8, device="cuda")
+    tv = torch.empty(cols, rows // 2, dtype=torch.bfloat16, device="cuda")
+    tm = torch.empty(cols, rows // 8, dtype=torch.uint8, device="cuda")
+    S.slope_prune_and_double_prune(W, vals, meta, tv, tm)
+    v2, tv2, tv3 = torch.empty_like(vals), torch.empty_like(tv), torch.empty_like(tv)
+    S.slope_recompress_frozen(W, meta, tm, v2, tv2)
+    S.slope_double_prune_frozen(vals, meta, rows, cols, tm, tv3)
+    assert torch.equal(v2, vals) and torch.equal(tv2, tv) and torch.equal(tv3, tv)
