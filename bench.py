@@ -15,6 +15,18 @@ for the adapter), whole job, summed over ranks.
 
 --impl reference times the CPU oracle (the plain fp64 NumPy definition of
 the same step) on the host cores, on a bounded sample of the same workload.
+
+Step variants (the default is the five path calls per linear):
+  --fused-prune      A1 and A2 as one call (slope_prune_and_double_prune);
+  --optimizer        the training step with the row mask kept from
+                     initialisation: the updated weight re-compressed and
+                     double-pruned (slope_recompress_double_prune) in place of
+                     A1 and A2, and beta·A + gamma·B (slope_sparse_axpby) on an
+                     fp32 master copy of the kept values after the gradients;
+  --frozen-columns   with --optimizer, the column mask kept too
+                     (slope_recompress_frozen).
+Every memory-bound call's achieved bandwidth is reported in `hbm_calls`, and
+the library's tensor-pipe rate self test in `mma_rate_selftest`.
 """
 
 from __future__ import annotations
