@@ -339,15 +339,39 @@ class BlockStep:
                     fn()
 
     def launches_per_step(self):
+        import torch
+
+        slots = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count // 2
         n = 0
-        for _ in self.layers:
+        for b in self.layers:
             n += 0 if self.wl.forward_only else (1 if self.fused_prune or self.optimizer else 2)  # prune(s)
             n += 1 if self.optimizer else 0  # beta·A + gamma·B
             n += 2 if self.wl.rank else 1  # fwd: (XL) + sparse
             if not self.wl.forward_only:
                 n += 2 if self.wl.rank else 1  # bwd_input: (G) + sparse
                 n += 1  # dW with dL, dR alongside
+                # the zero-fill of the outputs the launch adds into: the adapter
+                # gradients always, dW when its K is split
+                if self.wl.rank or dw_splits(self.wl.tokens, b["inp"], b["out"], slots) > 1:
+                    n += 1
         return n
+
+
+def dw_splits(T: int, inp: int, out: int, slots: int) -> int:
+    """Split count the library picks for the pair dW GEMM without the adapter
+    (the same round-count model): 256 x 256 output tiles over `slots` SM
+    pairs, K = T in blocks of 64."""
+    tiles = (out // 256) * ((inp + 255) // 256)
+    num_kb = (T + 63) // 64
+    best, best_cost = 1, None
+    for s in range(1, max(num_kb // 4, 1) + 1):
+        waves = (tiles * s + slots - 1) // slots
+        per_unit = (num_kb + s - 1) // s + (8 if s > 1 else 4)
+        cost = waves * per_unit + (8 if s > 1 else 0)
+        if best_cost is None or cost < best_cost:
+            best, best_cost = s, cost
+    kbs = (num_kb + best - 1) // best
+    return (num_kb + kbs - 1) // kbs
 
 
 class Marks:

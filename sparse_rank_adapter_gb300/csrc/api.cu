@@ -413,12 +413,11 @@ extern "C" int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T,
   const bool dense = flags & SLOPE_DW_DENSE, acc = flags & SLOPE_ACCUMULATE;
   const size_t dw_bytes = static_cast<size_t>(out) * (dense ? in : in / 2) * sizeof(float);
   if (T == 0) {
-    if (!acc) {
-      if (do_dw && cudaMemsetAsync(dW, 0, dw_bytes, st) != cudaSuccess) return SLOPE_ERR_CUDA;
-      if (do_ad && (cudaMemsetAsync(dL, 0, sizeof(float) * in * r, st) != cudaSuccess ||
-                    cudaMemsetAsync(dR, 0, sizeof(float) * out * r, st) != cudaSuccess))
-        return SLOPE_ERR_CUDA;
-    }
+    if (!acc && launch_zero3(do_dw ? dW : nullptr, do_dw ? dw_bytes / sizeof(float) : 0,
+                             do_ad ? dL : nullptr, do_ad ? static_cast<size_t>(in) * r : 0,
+                             do_ad ? dR : nullptr, do_ad ? static_cast<size_t>(out) * r : 0,
+                             st) != cudaSuccess)
+      return SLOPE_ERR_CUDA;
     return SLOPE_OK;
   }
   // dW and the adapter gradients in one launch when the dW GEMM runs on CTA
@@ -438,11 +437,9 @@ extern "C" int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T,
     if (launch_dense_gemm(w, st) != cudaSuccess) return SLOPE_ERR_CUDA;
   }
   if (!do_ad || fuse) return SLOPE_OK;
-  if (!acc) {
-    if (cudaMemsetAsync(dL, 0, sizeof(float) * in * r, st) != cudaSuccess ||
-        cudaMemsetAsync(dR, 0, sizeof(float) * out * r, st) != cudaSuccess)
-      return SLOPE_ERR_CUDA;
-  }
+  if (!acc && launch_zero3(dL, static_cast<size_t>(in) * r, dR, static_cast<size_t>(out) * r, nullptr, 0,
+                           st) != cudaSuccess)
+    return SLOPE_ERR_CUDA;
   // dL = Xᵀ·G (in x r): M = in, N = 2r (hi and lo parts of G), K = T;
   // A = X MN-major, B = G MN-major; column j + r folds onto column j.
   DenseGemmArgs l{};

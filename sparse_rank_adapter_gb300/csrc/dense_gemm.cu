@@ -471,6 +471,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (cs > 1) cluster_sync();
 }
 
+// Zeroes up to three fp32 arrays, the outputs a split launch adds into, in
+// one launch.  Unlike memset nodes it is a programmatic dependent of the
+// kernel before it (set-up overlaps that kernel's tail) and lets the next
+// kernel launch early; it writes only after the previous kernel is done.
+__global__ void __launch_bounds__(256) zero3_kernel(float4* a, int64_t na, float4* b, int64_t nb, float4* c,
+                                                    int64_t nc) {
+  grid_dependency_wait();
+  allow_dependents_launch();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < na + nb + nc; i += stride) {
+    if (i < na) a[i] = z;
+    else if (i < na + nb) b[i - na] = z;
+    else c[i - na - nb] = z;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // dW on CTA pairs: the pair-wide MMA (M = 256 = two 128-row weight tiles, one
 // per CTA, N = 256 input columns, half of them in each CTA's shared memory)
@@ -800,15 +817,11 @@ cudaError_t run_dw_pair(const DenseGemmArgs& a, cudaStream_t stream) {
   p.dense_dw = a.dense_dw ? 1 : 0;
   p.accumulate = a.accumulate ? 1 : 0;
   p.atomic_out = splits > 1 ? 1 : 0;
-  if (p.atomic_out && !a.accumulate) {
-    if (cudaError_t e = cudaMemsetAsync(a.out, 0, static_cast<size_t>(M) * a.ldo * sizeof(float), stream))
-      return e;
-  }
-  if (fr > 0 && !a.accumulate) {  // the adapter gradients are always added atomically
-    if (cudaError_t e = cudaMemsetAsync(a.dl, 0, static_cast<size_t>(N) * fr * sizeof(float), stream))
-      return e;
-    if (cudaError_t e = cudaMemsetAsync(a.dr, 0, static_cast<size_t>(fr) * M * sizeof(float), stream))
-      return e;
+  if (!a.accumulate && (p.atomic_out || fr > 0)) {
+    // dW when split K adds its parts; the adapter gradients are always added
+    const size_t ndw = p.atomic_out ? static_cast<size_t>(M) * a.ldo : 0;
+    const size_t nl = fr > 0 ? static_cast<size_t>(N) * fr : 0, nr = fr > 0 ? static_cast<size_t>(fr) * M : 0;
+    if (cudaError_t e = launch_zero3(static_cast<float*>(a.out), ndw, a.dl, nl, a.dr, nr, stream)) return e;
   }
   p.status = device_status_ptr();
   if (!p.status) return cudaErrorInvalidDevicePointer;
@@ -886,8 +899,9 @@ cudaError_t run(const DenseGemmArgs& a, cudaStream_t stream) {
   if (EPI == DenseEpi::MaskedWeightGrad && splits > 1) {
     p.atomic_out = 1;
     if (!a.accumulate) {
-      const size_t bytes = static_cast<size_t>(M) * a.ldo * sizeof(float);
-      if (cudaError_t e = cudaMemsetAsync(a.out, 0, bytes, stream)) return e;
+      if (cudaError_t e = launch_zero3(static_cast<float*>(a.out), static_cast<size_t>(M) * a.ldo, nullptr, 0,
+                                       nullptr, 0, stream))
+        return e;
     }
   }
   p.status = device_status_ptr();
@@ -927,6 +941,26 @@ cudaError_t run_rank(const DenseGemmArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t launch_zero3(float* a, size_t na, float* b, size_t nb, float* c, size_t nc,
+                         cudaStream_t stream) {
+  // counts in floats, each a multiple of 4 (16-byte aligned arrays)
+  const int64_t n4 = static_cast<int64_t>((na + nb + nc) / 4);
+  if (n4 == 0) return cudaSuccess;
+  int64_t blocks = (n4 + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 4;
+  if (blocks > cap) blocks = cap;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attrs[1];
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  add_pdl_attr(cfg, attrs);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, zero3_kernel, reinterpret_cast<float4*>(a), static_cast<int64_t>(na / 4),
+                                     reinterpret_cast<float4*>(b), static_cast<int64_t>(nb / 4),
+                                     reinterpret_cast<float4*>(c), static_cast<int64_t>(nc / 4));
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 cudaError_t launch_dense_gemm(const DenseGemmArgs& a, cudaStream_t stream) {
   switch (a.epi) {

@@ -58,6 +58,11 @@ cudaError_t launch_recompress_frozen24(const void* W, const uint8_t* meta, const
 cudaError_t launch_axpby(float beta, const void* a, int a_dt, float gamma, const void* b, int b_dt,
                          void* out, int out_dt, int64_t n, cudaStream_t stream);
 
+// Zeroes up to three fp32 arrays (counts in floats, multiples of 4) in one
+// programmatic-dependent launch (dense_gemm.cu).
+cudaError_t launch_zero3(float* a, size_t na, float* b, size_t nb, float* c, size_t nc,
+                         cudaStream_t stream);
+
 // ---- tensor-core rate self test (mma_rate.cu): enqueues the launch and
 // writes the dense-equivalent flops it executes to *flops.
 // kind: 0 dense, 1 sparse with one fixed metadata pattern, 2 sparse with
