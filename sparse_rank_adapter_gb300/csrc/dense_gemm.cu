@@ -21,6 +21,13 @@
 // 2..5 epilogue.  The accumulator is double-buffered in TMEM so a tile's
 // epilogue overlaps the next tile's K-loop.  Every mbarrier wait is bounded.
 //
+// dw_pair_kernel (below) runs dW on CTA pairs (pair-wide MMA, 256 x 256
+// tiles) and, when asked, dL and dR as extra tiles of the same launch:
+// dRᵀ = dYᵀ·XL shares dW's A operand and dLᵀ = Gᵀ·X its B operand.  The
+// outputs a split launch adds into are zeroed first by zero3_kernel, a
+// programmatic dependent like the GEMMs (a memset node would break the
+// chain of early launches).
+//
 // The hi/lo store needs the whole sum before it rounds, so its split-K goes
 // through a thread-block cluster instead of atomics: the cluster's CTAs take
 // K ranges of the same tile; each writes its fp32 partial into its own

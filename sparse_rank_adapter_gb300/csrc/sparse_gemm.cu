@@ -19,7 +19,9 @@
 // Two kernels.  sparse_gemm_kernel: one CTA per tile, persistent, one CTA
 // per SM, tiles taken round-robin; it serves up to 128 tokens and weights
 // with an odd number of 128-row tiles.  sparse_pair_kernel (below): CTA
-// pairs on the pair-wide MMA for the large batches.
+// pairs on the pair-wide MMA for the large batches, with one 128-row weight
+// tile per CTA, or two (256 rows apart) for long K-loops, where a stage's
+// bytes then serve eight MMAs instead of four.
 //
 // Roles (576 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues
 // the MMAs (one thread), warps 2..5 and 14..17 drain the accumulator (two
