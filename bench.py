@@ -13,8 +13,17 @@ Metric: dense-equivalent TFLOP/s of fwd + bwd (2·T·in·out for each of the
 forward, input-gradient and weight-gradient products plus 6·T·r·(in+out)
 for the adapter), whole job, summed over ranks.
 
+The default workload is the largest single-GPU block, OPT-33B-shaped
+(d = 7168, FFN 28672, T = 16384, adapter rank 64).  `--linear NAME` keeps
+one linear of the block (profiling runs of one launch).
+
 --impl reference times the CPU oracle (the plain fp64 NumPy definition of
-the same step) on the host cores, on a bounded sample of the same workload.
+the same step) on the host cores, on a bounded sample of the same workload:
+row slabs of each weight (a slab of output rows is an exact share of the
+linear's work) over a token sample.
+
+--gpus N (N > 1, not already under torchrun) starts N replica processes, one
+per GPU, with RANK / LOCAL_RANK / WORLD_SIZE set, as torchrun would.
 
 Step variants (the default is the five path calls per linear):
   --fused-prune      A1 and A2 as one call (slope_prune_and_double_prune);
@@ -389,12 +398,25 @@ class Marks:
 
 
 def call_flops(name, T, inp, out, r):
-    """Dense-equivalent flops of one ABI call: every GEMM call runs its main
-    product 2·T·in·out (forward, input gradient, weight gradient) and two
-    rank-r products 2·T·r·(in + out) (XL and the adapter term; G and the
-    adapter term; dL and dR)."""
+    """Dense-equivalent flops the tensor cores execute in one ABI call: every
+    GEMM call runs its main product 2·T·in·out (forward, input gradient,
+    weight gradient) and two rank-r products 2·T·r·(in + out) (XL and the
+    adapter term; G and the adapter term; dL and dR)."""
     if name in ("fwd", "bwd_input", "bwd_weight"):
         return 2.0 * T * inp * out + 2.0 * T * r * (inp + out)
+    return 0.0
+
+
+def method_flops(name, T, inp, out, r):
+    """The method's own work in one ABI call.  The sparse products count
+    their dense-equivalent 2·T·in·out (judged against twice the dense
+    peak); the masked weight gradient counts T·in·out, because only the
+    kept half of dYᵀ·X is needed (the tensor cores still compute all of
+    it); the rank-r products count 2·T·r·(in + out)."""
+    if name in ("fwd", "bwd_input"):
+        return 2.0 * T * inp * out + 2.0 * T * r * (inp + out)
+    if name == "bwd_weight":
+        return 1.0 * T * inp * out + 2.0 * T * r * (inp + out)
     return 0.0
 
 
@@ -418,6 +440,24 @@ def dw_bytes(T, inp, out, r):
 # leaves dirty in L2 are not yet written).  Only kernels unchanged since their
 # capture are listed.
 NCU_TRAFFIC = {("opt-350m-block", "bwd_weight"): 30.44e6}
+
+
+def sub_workload(wl, linear):
+    """The workload restricted to one of its linears (by name)."""
+    keep = tuple(x for x in wl.linears if x.name == linear)
+    if not keep:
+        raise SystemExit(f"{wl.name} has no linear {linear!r}: {[x.name for x in wl.linears]}")
+    return synth.Workload(f"{wl.name}:{linear}", wl.tokens, wl.rank, keep, wl.forward_only)
+
+
+def pick_peak(clocks, bf16, bf16_sus):
+    """The dense bf16 peak a kernel timed inside this run is judged against:
+    the sustained figure (measured under the power cap) when the clock
+    record of the timed region shows the power cap, else the burst one."""
+    capped = "sw_power_cap" in (clocks.get("reasons") or [])
+    if capped:
+        return bf16_sus, "sustained (sw_power_cap seen in the timed region)"
+    return bf16, "burst (no power cap seen in the timed region)"
 
 
 def call_bytes(name, T, inp, out, r):
@@ -483,6 +523,8 @@ def gpu_arm(args):
     if world > 1:
         dist.barrier()
     wl = synth.WORKLOADS[args.workload]
+    if args.linear:
+        wl = sub_workload(wl, args.linear)
     stream = torch.cuda.Stream(device=dev)
     n_sets = max(1, args.sets)
     sets = [BlockStep(wl, seed=s + 10 * rank, device=dev, fused_prune=args.fused_prune, optimizer=args.optimizer,
@@ -521,7 +563,6 @@ def gpu_arm(args):
             mgraphs[i % n_sets].replay()
     torch.cuda.synchronize()
 
-    per_call = {}
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -537,23 +578,34 @@ def gpu_arm(args):
                     sets[i % n_sets].run(stream)
         t_end.record(stream)
         t_end.synchronize()
-    # per-call breakdown: one marked pass over every input set
-    with torch.cuda.stream(stream):
-        for i in range(n_sets):
-            if args.graph:
-                mgraphs[i].replay()
-            else:
-                sets[i].run(stream, marks[i])
-    stream.synchronize()
-    if world > 1:
-        dist.barrier()
-    for m in marks:
-        for name, inp, out, e0, e1 in m.pairs:
-            per_call.setdefault(name, []).append((inp, out, e0.elapsed_time(e1)))
-    n_obs = n_sets
     clocks = clk.summary()
     ms_step = t_start.elapsed_time(t_end) / args.steps
-    calls_ms = {k: sum(x[2] for x in v) / n_obs for k, v in per_call.items()}
+
+    # Per-call breakdown: `call_reps` marked passes over every input set; a
+    # call's time per step is the median over the passes of its summed
+    # event times in that pass.
+    reps = max(1, args.call_reps)
+    per_rep = []  # one {call: ms per step} per pass
+    obs = {}  # call -> [(in, out)] of one step
+    for rep in range(reps):
+        with torch.cuda.stream(stream):
+            for i in range(n_sets):
+                if args.graph:
+                    mgraphs[i].replay()
+                else:
+                    marks[i].pairs.clear()
+                    sets[i].run(stream, marks[i])
+        stream.synchronize()
+        tot = {}
+        for m in marks:
+            for name, inp, out, e0, e1 in m.pairs:
+                tot[name] = tot.get(name, 0.0) + e0.elapsed_time(e1)
+                if rep == 0 and m is marks[0]:
+                    obs.setdefault(name, []).append((inp, out))
+        per_rep.append({k: v / n_sets for k, v in tot.items()})
+    calls_ms = {k: statistics.median(r[k] for r in per_rep) for k in per_rep[0]}
+    if world > 1:
+        dist.barrier()
 
     ms_step = max_over_ranks(ms_step, dev)
     fl = flops_per_step(wl)
@@ -562,22 +614,36 @@ def gpu_arm(args):
     # roofline of the dominant call
     T, r = wl.tokens, wl.rank
     hbm, bf16, bf16_sus, src = peaks()
+    dense_peak, peak_why = pick_peak(clocks, bf16, bf16_sus)
     dom = max(calls_ms, key=calls_ms.get)
-    n_launch = len(per_call[dom]) / n_obs
+    n_launch = len(obs[dom])
     if dom == "fwd" and wl.forward_only and T <= 128:
         # small-batch inference streams the compressed weights: bytes-bound
-        byts = sum(fwd_bytes(T, i, o, r) for i, o, _ in per_call[dom]) / n_obs
+        byts = sum(fwd_bytes(T, i, o, r) for i, o in obs[dom])
         ach = byts / (calls_ms[dom] * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm}
+        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "peak_source": f"{src} hbm"}
     elif dom in ("prune", "double_prune", "prune_double", "recompress_double", "recompress_frozen", "axpby"):
-        alg = sum(call_bytes(dom, T, i, o, r) for i, o, _ in per_call[dom]) / n_obs
+        alg = sum(call_bytes(dom, T, i, o, r) for i, o in obs[dom])
         ach = alg / (calls_ms[dom] * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm}
+        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "peak_source": f"{src} hbm"}
     else:
-        alg = sum(call_flops(dom, T, i, o, r) for i, o, _ in per_call[dom]) / n_obs
-        ach = alg / (calls_ms[dom] * 1e-3) / 1e12
-        peak = bf16_sus * (2.0 if dom in ("fwd", "bwd_input") else 1.0)
-        roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak}
+        work = sum(method_flops(dom, T, i, o, r) for i, o in obs[dom])
+        ach = work / (calls_ms[dom] * 1e-3) / 1e12
+        sparse = dom in ("fwd", "bwd_input")
+        peak = dense_peak * (2.0 if sparse else 1.0)
+        roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                "work_flops_per_step": work,
+                "work": ("dense-equivalent 2*T*in*out + 2*T*r*(in+out) per linear, against 2x the dense peak"
+                         if sparse else
+                         "masked outputs T*in*out + adapter 2*T*r*(in+out) per linear, against the dense peak"),
+                "peak_source": f"{src} {'2x ' if sparse else ''}bf16 {peak_why}"}
+        if not sparse:
+            # what the tensor cores execute: the whole dYᵀ·X product
+            exe = sum(call_flops(dom, T, i, o, r) for i, o in obs[dom])
+            roof["dense_gemm_achieved"] = exe / (calls_ms[dom] * 1e-3) / 1e12
+            roof["dense_gemm_frac"] = roof["dense_gemm_achieved"] / peak
     kernel_of = {"prune": "prune24_kernel (slope_prune_nm)", "double_prune": "double_prune24_kernel (slope_double_prune)",
                  "fwd": "slope_linear_fwd (XL GEMM + sparse GEMM)", "bwd_input": "slope_linear_bwd_input (G GEMM + sparse GEMM)",
                  "bwd_weight": "dW GEMM with dL, dR (slope_linear_bwd_weight)",
@@ -587,20 +653,19 @@ def gpu_arm(args):
                  "axpby": "axpby_kernel (slope_sparse_axpby)"}
     # achieved bandwidth of every memory-bound call (algorithmic bytes over its time)
     hbm_calls = {}
-    for name, obs in per_call.items():
-        byts = sum(call_bytes(name, T, i, o, r) for i, o, _ in obs) / n_obs
+    for name, o_ in obs.items():
+        byts = sum(call_bytes(name, T, i, o, r) for i, o in o_)
         if byts > 0 and calls_ms.get(name):
             gbs = byts / (calls_ms[name] * 1e-3) / 1e9
             hbm_calls[name] = {"GB/s": round(gbs, 1), "frac": round(gbs / hbm, 3)}
     traffic = NCU_TRAFFIC.get((wl.name, dom))
     if traffic is not None:
-        roof["traffic_unit"] = "bytes per launch"
+        roof["traffic_unit"] = "bytes per launch (dram read + write, ncu)"
         if dom == "bwd_weight":
-            roof["algorithmic_bytes"] = sum(dw_bytes(T, i, o, r) for i, o, _ in per_call[dom]) / len(per_call[dom])
-    roof.update({"kernel": kernel_of.get(dom, dom), "traffic": traffic,
-                 "peak_source": f"{src} ({'2x ' if dom in ('fwd', 'bwd_input') else ''}bf16 sustained)"
-                 if roof['bound'] == 'tensor' else f"{src} hbm",
-                 "launches_per_step": n_launch})
+            roof["algorithmic_bytes"] = sum(dw_bytes(T, i, o, r) for i, o in obs[dom]) / n_launch
+    roof.update({"kernel": kernel_of.get(dom, dom), "traffic": traffic, "launches_per_step": n_launch,
+                 "call_ms_per_step": round(calls_ms[dom], 4),
+                 "call_time": f"median over {reps} marked passes of the step"})
 
     rates = mma_rates(stream) if args.mma_rate else None
     if rates and roof["bound"] == "tensor":
@@ -629,7 +694,8 @@ def gpu_arm(args):
                                  else "kept mask: re-compression + A2, then beta*A + gamma*B" if args.optimizer
                                  else "one call (A1 + A2)" if args.fused_prune else "two calls (A1, A2)")},
             "pct_of_sparse_peak": round(100 * value / (2 * bf16), 2),
-            "composite_roofline_frac": composite_frac(wl, ms_step, bf16_sus),
+            "composite_roofline_frac": composite_frac(wl, ms_step, dense_peak),
+            "composite_peak": f"{src} bf16 {peak_why}",
             "calls_ms_per_step": {k: round(v, 4) for k, v in calls_ms.items()},
             "hbm_calls": hbm_calls,
             "roofline": roof, "clocks": clocks, "gpu_launches": sets[0].launches_per_step() * args.steps,
@@ -649,7 +715,7 @@ def set_bytes(st):
     return tot
 
 
-def composite_frac(wl, ms_step, bf16_sus):
+def composite_frac(wl, ms_step, dense_peak):
     """Time the composite roofline allows (sparse products at 2x the dense
     peak, dense ones at the dense peak) over the measured step time."""
     T, r = wl.tokens, wl.rank
@@ -659,7 +725,7 @@ def composite_frac(wl, ms_step, bf16_sus):
         dense = 0.0 if wl.forward_only else 2.0 * T * lin.inp * lin.out
         if r:
             dense += (2.0 if wl.forward_only else 6.0) * T * r * (lin.inp + lin.out)
-        t += sparse / (2 * bf16_sus * 1e12) + dense / (bf16_sus * 1e12)
+        t += sparse / (2 * dense_peak * 1e12) + dense / (dense_peak * 1e12)
     return round(t / (ms_step * 1e-3), 4)
 
 
@@ -669,9 +735,14 @@ def e2e_measure(args, wl, st, stream, dev):
     result are inside the timed region."""
     import torch
 
+    def pinned_copy(t):
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        return h
+
     host_in, host_out = [], []
     for b in st.layers:
-        host_in.append({k: b[k].cpu().pin_memory() for k in st.input_names() if b[k] is not None})
+        host_in.append({k: pinned_copy(b[k]) for k in st.input_names() if b[k] is not None})
         host_out.append({k: torch.empty(b[k].shape, dtype=b[k].dtype, pin_memory=True)
                          for k in st.output_names() if b[k] is not None})
     h2d = sum(v.numel() * v.element_size() for d in host_in for v in d.values())
@@ -735,36 +806,84 @@ def e2e_measure(args, wl, st, stream, dev):
 # ------------------------------------------------------------- CPU arm ----
 
 
-def oracle_sample(wl, budget_s: float):
-    """Times the oracle (as it stands) on the block: full passes over its
-    linears (prune, double prune, forward, both gradients) for up to 2048
-    tokens, repeated until `budget_s` seconds of CPU work; returns
-    (dense-equivalent flops done, seconds, description)."""
-    from oracle import slope_oracle as O
+SLAB_ROWS = 512  # output rows of W per oracle sample unit
+SAMPLE_TOKENS = 2048  # token rows of X and dY per oracle sample unit
 
-    T = wl.tokens
-    sample_T = min(T, 2048)
-    inputs = [synth.layer_inputs(0, li, sample_T, lin.inp, lin.out, wl.rank)
-              for li, lin in enumerate(wl.linears)]
-    done, t_total, lins = 0.0, 0.0, 0
-    while t_total < budget_s:
-        for lin, d in zip(wl.linears, inputs):
-            L, R = (d["L"], d["R"]) if wl.rank else (None, None)
+
+class OracleSampler:
+    """The oracle (as it stands) over row slabs of a workload's weights.
+
+    A unit is one linear restricted to a slab of `SLAB_ROWS` output rows
+    (rows of W) on `SAMPLE_TOKENS` tokens: prune the slab, run the forward
+    for its output columns, double-prune it (the slab's rows are whole
+    groups of the transposed pruning, so its columns of D are exact), add
+    its share of the input gradient, and take its rows of dW and columns of
+    dR (and the full dL product).  A slab of o of the linear's `out` rows is
+    exactly o/out of the linear's work, which is what a unit counts; the
+    oracle also recomputes the rank-r products X·L and dY·Rᵀ per slab, which
+    is not counted.  Units rotate over the linears and their slabs."""
+
+    def __init__(self, wl):
+        from oracle import slope_oracle as O
+
+        self.O = O
+        self.wl = wl
+        self.T = min(wl.tokens, SAMPLE_TOKENS)
+        self.units = []
+        for li, lin in enumerate(wl.linears):
+            rows = min(SLAB_ROWS, lin.out)
+            for o0 in range(0, lin.out - rows + 1, rows):
+                self.units.append((li, lin, o0, rows))
+        # rotate linears first, so a short sample still touches every shape
+        self.units.sort(key=lambda u: (u[2], u[0]))
+        self.cache = {}
+        self.next = 0
+
+    def inputs(self, li, lin, o0, rows):
+        key = (li, o0)
+        if key not in self.cache:
+            T, r = self.T, self.wl.rank
+            X = synth.normal_bf16(1, li, "X", (T, lin.inp))
+            d = {"X": X, "W": synth.normal_bf16(1 + o0, li, "W", (rows, lin.inp)),
+                 "dY": synth.normal_bf16(1 + o0, li, "dY", (T, rows)),
+                 "L": synth.normal_bf16(1, li, "L", (lin.inp, r)) if r else None,
+                 "R": synth.normal_bf16(1 + o0, li, "R", (r, rows)) if r else None}
+            if len(self.cache) > 64:
+                self.cache.clear()
+            self.cache[key] = d
+        return self.cache[key]
+
+    def unit_flops(self, lin, rows):
+        one = synth.Workload(self.wl.name, self.T, self.wl.rank, (lin,), self.wl.forward_only)
+        return flops_per_step(one) * rows / lin.out
+
+    def run(self, budget_s: float, min_units: int = 1):
+        """Units until `budget_s` seconds of oracle time (at least
+        `min_units`); returns (flops counted, seconds, units done)."""
+        O = self.O
+        done, t_total, n = 0.0, 0.0, 0
+        while n < min_units or t_total < budget_s:
+            li, lin, o0, rows = self.units[self.next % len(self.units)]
+            self.next += 1
+            d = self.inputs(li, lin, o0, rows)
             s = time.perf_counter()
             vals, meta, _ = O.prune24(d["W"])
-            O.linear_fwd(d["X"], vals, meta, L, R)
-            if not wl.forward_only:
-                tv, tm, _ = O.double_prune24(vals, meta, lin.out, lin.inp)
-                O.linear_bwd_input(d["dY"], tv, tm, L, R)
-                O.linear_bwd_weight(d["dY"], d["X"], meta, L, R)
+            O.linear_fwd(d["X"], vals, meta, d["L"], d["R"])
+            if not self.wl.forward_only:
+                tv, tm, _ = O.double_prune24(vals, meta, rows, lin.inp)
+                O.linear_bwd_input(d["dY"], tv, tm, d["L"], d["R"])
+                O.linear_bwd_weight(d["dY"], d["X"], meta, d["L"], d["R"])
             t_total += time.perf_counter() - s
-            done += flops_per_step(synth.Workload(wl.name, sample_T, wl.rank, (lin,), wl.forward_only))
-            lins += 1
-            if t_total >= budget_s:
-                break
-    desc = (f"{lins} linear passes over {wl.name} ({len(wl.linears)} linears), {sample_T} of {T} tokens "
-            f"each, full prune and double prune of every weight; oracle fp64 NumPy")
-    return done, t_total, desc
+            done += self.unit_flops(lin, rows)
+            n += 1
+        return done, t_total, n
+
+    def describe(self, n):
+        wl = self.wl
+        steps = "prune, forward" if wl.forward_only else "prune, double prune, forward, both gradients"
+        return (f"{n} units of {wl.name}: row slabs of up to {SLAB_ROWS} output rows of each of its "
+                f"{len(wl.linears)} weights ({steps}) on {self.T} of {wl.tokens} tokens, counted as "
+                f"their exact share of the workload's flops; oracle fp64 NumPy")
 
 
 def cpu_cores():
@@ -774,10 +893,55 @@ def cpu_cores():
         return os.cpu_count()
 
 
+def one_core_sample(wl_name, linear, budget_s):
+    """The same oracle sample in a child process held to one core (BLAS
+    threads 1, CPU affinity one core); returns its JSON dict or None."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               VECLIB_MAXIMUM_THREADS="1", NUMEXPR_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--workload", wl_name,
+           "--oracle-sample", str(budget_s)]
+    if linear:
+        cmd += ["--linear", linear]
+    try:
+        res = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=budget_s * 4 + 300)
+        if res.returncode == 0:
+            return json.loads(res.stdout.strip().splitlines()[-1])
+    except Exception:
+        pass
+    return None
+
+
 def cpu_baseline(wl, budget_s):
-    done, secs, desc = oracle_sample(wl, budget_s)
-    return {"value": round(done / secs / 1e12, 6), "unit": "TFLOP/s", "cores": cpu_cores(),
-            "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+    """The oracle on all host cores, and on one core (a child process)."""
+    smp = OracleSampler(wl)
+    smp.run(0.0, 1)  # warm-up: first-touch costs and input generation
+    done, secs, n = smp.run(budget_s)
+    out = {"value": round(done / secs / 1e12, 6), "unit": "TFLOP/s", "cores": cpu_cores(),
+           "kind": "oracle", "sample": smp.describe(n), "seconds": round(secs, 2)}
+    name, _, linear = wl.name.partition(":")
+    one = one_core_sample(name, linear, budget_s)
+    if one is not None:
+        out["one_core"] = {"value": one["value"], "unit": "TFLOP/s", "cores": 1, "sample": one["sample"],
+                           "seconds": one["seconds"]}
+    return out
+
+
+def oracle_sample_child(args):
+    """--oracle-sample: time the oracle alone on this process's first
+    allowed core and print one JSON line (used for the one-core figure)."""
+    try:
+        core = sorted(os.sched_getaffinity(0))[0]
+        os.sched_setaffinity(0, {core})
+    except Exception:
+        pass
+    wl = synth.WORKLOADS[args.workload]
+    if args.linear:
+        wl = sub_workload(wl, args.linear)
+    smp = OracleSampler(wl)
+    smp.run(0.0, 1)
+    done, secs, n = smp.run(args.oracle_sample)
+    print(json.dumps({"value": round(done / secs / 1e12, 6), "seconds": round(secs, 2),
+                      "sample": smp.describe(n), "cores": 1}), flush=True)
 
 
 def reference_arm(args):
@@ -785,14 +949,20 @@ def reference_arm(args):
     if rank != 0:
         return
     wl = synth.WORKLOADS[args.workload]
-    vals, tot_flops, tot_s, desc = [], 0.0, 0.0, ""
+    if args.linear:
+        wl = sub_workload(wl, args.linear)
+    smp = OracleSampler(wl)
+    tot_flops, tot_s, n_units = 0.0, 0.0, 0
     for i in range(args.warmup + args.steps):
-        f, s, desc = oracle_sample(wl, args.cpu_seconds)
-        if i >= args.warmup:
-            vals.append(f / s / 1e12)
-            tot_flops += f
-            tot_s += s
+        if i < args.warmup:  # warm-up steps: one unit each, untimed
+            smp.run(0.0, 1)
+            continue
+        f, s, n = smp.run(args.ref_seconds)
+        tot_flops += f
+        tot_s += s
+        n_units += n
     value = tot_flops / tot_s / 1e12
+    desc = smp.describe(n_units) + f"; {args.steps} steps of about {args.ref_seconds:g} s"
     line = {
         "impl": "reference",
         "metric": "sparse+LoRA linear fwd+bwd TFLOP/s (dense-equiv) and % of 2:4-sparse bf16 peak",
@@ -807,18 +977,49 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+def free_port():
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launch_replicas(n, argv):
+    """Runs this script as n processes, one per GPU, with the environment a
+    torchrun launch would give them; returns the first non-zero exit code
+    (0 if every rank succeeded).  Only rank 0 prints."""
+    port = free_port()
+    procs = []
+    for rank in range(n):
+        env = dict(os.environ, RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE=str(n),
+                   LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        out = None if rank == 0 else subprocess.DEVNULL
+        procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__)] + list(argv), env=env,
+                                      stdout=out))
+    rcs = [p.wait() for p in procs]
+    return next((rc for rc in rcs if rc != 0), 0)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="slope", choices=["slope", "reference"])
-    ap.add_argument("--workload", default="opt-350m-block", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="opt-33b-block-r64", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--linear", default="", help="keep only this linear of the block (e.g. fc1)")
     ap.add_argument("--sets", type=int, default=4, help="rotating input sets (L2 defeat)")
+    ap.add_argument("--call-reps", type=int, default=5,
+                    help="marked passes for the per-call breakdown (median)")
     ap.add_argument("--no-graph", dest="graph", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
-    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="oracle seconds of the GPU arm's cpu_baseline (all cores, then one core)")
+    ap.add_argument("--ref-seconds", type=float, default=6.0,
+                    help="oracle seconds per step of --impl reference")
+    ap.add_argument("--oracle-sample", type=float, default=0.0, help=argparse.SUPPRESS)
     ap.add_argument("--no-mma-rate", dest="mma_rate", action="store_false",
                     help="skip the tensor-core rate self test")
     ap.add_argument("--optimizer", action="store_true",
@@ -833,6 +1034,11 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.oracle_sample > 0:
+        oracle_sample_child(args)
+        return
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(launch_replicas(args.gpus, sys.argv[1:]))
     if args.impl == "reference":
         reference_arm(args)
     else:

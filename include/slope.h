@@ -41,8 +41,19 @@
  *    The sparse GEMMs read this format as it is (no reordering pass).
  *  - Magnitude ranking uses the exact key (bf16 bits & 0x7FFF); ties go to
  *    the lower index.  No floating-point arithmetic decides a mask.
- *  - Thread safety: calls may be made from several host threads; the only
- *    shared state is a per-device capability cache and a device status word.
+ *  - Thread safety: calls may be made from several host threads.  Shared
+ *    state: a per-device capability cache, a device status word, and a
+ *    process-wide cache of encoded TMA tensor maps (256 slots behind one
+ *    lock) keyed by every field that goes into a map (address, element type,
+ *    extents, row stride, box, swizzle).  A hit is bit for bit the map that
+ *    encoding would produce, so a buffer freed and re-allocated at the same
+ *    address is still described correctly; the cache holds no reference to
+ *    device memory and nothing needs releasing.
+ *  - Adapter rank: 0 <= r <= 256 with r % 8 == 0.  The rank-r operands are
+ *    read by the tensor-memory-access unit, whose row strides must be
+ *    multiples of 16 bytes: L (in x r bf16) has rows of 2r bytes, so r must
+ *    be a multiple of 8.  A rank that is not can be zero-padded by the
+ *    caller (zero columns of L and zero rows of R add nothing).
  */
 #ifndef SLOPE_H_
 #define SLOPE_H_
@@ -80,9 +91,13 @@ int slope_version(void);
 
 /*
  * Bytes of scratch memory the compute calls below need for one linear of
- * these sizes (T tokens, in, out, rank r).  Passing at least this many bytes
- * as `workspace` to any of them is always enough; 0 means no scratch.
- * Returns 0 for invalid sizes as well (the call itself then reports them).
+ * these sizes (T tokens, in, out, rank r): the T x 2r bf16 plane of the
+ * rank-r intermediate (4·T·r bytes, rounded up to 256) that
+ * slope_linear_fwd and slope_linear_bwd_input use when the caller passes
+ * XL (or G) as NULL.  Passing at least this many bytes as `workspace` to any
+ * of them is always enough; slope_linear_bwd_weight needs none.  Returns 0
+ * for r == 0 (no scratch) and for invalid sizes (the call itself then
+ * reports them).
  */
 size_t slope_workspace_size(int64_t T, int64_t in, int64_t out, int r);
 
@@ -189,10 +204,15 @@ int slope_sparse_axpby(float beta, const void* A, int a_dtype, float gamma, cons
  *     XL = X·L                        (kept for the backward)
  * X: T x in bf16.  (Wv, Wm): the compressed out x in weight.  L: in x r
  * bf16, R: r x out bf16.  Y: T x out, `y_dtype` SLOPE_F32 or SLOPE_BF16.
- * XL: T x 2r bf16 output, required when r > 0: row t holds the r values of
- * (X·L)[t] as bf16 "hi" parts followed by their bf16 "lo" remainders
- * (hi = bf16(v), lo = bf16(v - hi)); hi + lo keeps about 16 significant
- * bits, and the adapter product uses both.
+ * XL: T x 2r bf16 output when r > 0: row t holds the r values of (X·L)[t]
+ * as bf16 "hi" parts followed by their bf16 "lo" remainders (hi = bf16(v),
+ * lo = bf16(v - hi)); hi + lo keeps about 16 significant bits, and the
+ * adapter product uses both.  XL may be NULL when the caller does not keep
+ * it (e.g. inference): the plane then lives in `workspace`, which must be
+ * 16-byte aligned and hold slope_workspace_size(T, in, out, r) bytes
+ * (else SLOPE_ERR_INVALID_ARG).  The workspace's contents on entry do not
+ * matter, and it must not be reused by another call until this one's work
+ * on `stream` is done.  With XL given, `workspace` is not used (NULL, 0).
  * Requires in % 128 == 0, out % 128 == 0, T >= 0 (T == 0 is a no-op),
  * 0 <= r <= 256 and r % 8 == 0; r == 0 disables the adapter (L, R, XL may
  * then be NULL).
@@ -206,8 +226,9 @@ int slope_linear_fwd(const void* X, int64_t T, int64_t in, int64_t out, const vo
  *     dX = dY·Dᵀ + (dY·Rᵀ)·Lᵀ        G = dY·Rᵀ (kept for dL)
  * dY: T x out bf16.  (Dv, Dm): the compressed in x out double-pruned matrix
  * from slope_double_prune.  dX: T x in, `dx_dtype` SLOPE_F32 or SLOPE_BF16.
- * G: T x 2r bf16 output (hi parts, then lo parts, as XL), required when
- * r > 0.  Size rules as slope_linear_fwd.
+ * G: T x 2r bf16 output (hi parts, then lo parts, as XL) when r > 0; it
+ * may be NULL, with the plane then in `workspace`, under the rules
+ * slope_linear_fwd gives for XL.  Size rules as slope_linear_fwd.
  */
 int slope_linear_bwd_input(const void* dY, int64_t T, int64_t in, int64_t out, const void* Dv,
                            const uint8_t* Dm, const void* L, const void* R, int r, void* dX,
@@ -229,7 +250,8 @@ int slope_linear_bwd_input(const void* dY, int64_t T, int64_t in, int64_t out, c
  * overwriting them.  SLOPE_SKIP_DW computes only dL and dR (dW and Wm may be
  * NULL); SLOPE_SKIP_ADAPTER computes only dW (XL, G, dL, dR may be NULL);
  * both together are SLOPE_ERR_INVALID_ARG.  T == 0 writes zeros (or leaves
- * them, when accumulating).  Size rules as slope_linear_fwd.
+ * them, when accumulating).  This call needs no scratch: `workspace` is
+ * not used (pass NULL, 0).  Size rules as slope_linear_fwd.
  */
 int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T, int64_t in, int64_t out,
                             const uint8_t* Wm, const void* XL, const void* G, int r, float* dW,

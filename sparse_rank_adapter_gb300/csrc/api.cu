@@ -228,9 +228,29 @@ extern "C" const char* slope_status_string(int s) {
 
 extern "C" int slope_version(void) { return 10000; }
 
+// Scratch of the two sparse-product calls: the T x 2r bf16 plane of the
+// rank-r intermediate (XL or G, hi parts then lo parts) when the caller does
+// not keep it, rounded up to 256 bytes.  The weight-gradient call needs none.
+static size_t plane_bytes(int64_t T, int r) {
+  const size_t b = static_cast<size_t>(T) * static_cast<size_t>(2 * r) * 2;
+  return (b + 255) & ~static_cast<size_t>(255);
+}
+
 extern "C" size_t slope_workspace_size(int64_t T, int64_t in, int64_t out, int r) {
-  (void)T; (void)in; (void)out; (void)r;
-  return 0;
+  if (T < 0 || in <= 0 || out <= 0 || in % 128 != 0 || out % 128 != 0) return 0;
+  if (r <= 0 || r > 256 || r % 8 != 0 || T > (int64_t(1) << 31) - 1) return 0;
+  return plane_bytes(T, r);
+}
+
+// The rank-r plane of a sparse-product call: the caller's output when given,
+// else the front of the workspace, which must then hold plane_bytes(T, r).
+static int rank_plane(void* given, void* workspace, size_t workspace_bytes, int64_t T, int r,
+                      void** plane) {
+  *plane = given;
+  if (r == 0 || given) return SLOPE_OK;
+  if (!workspace || workspace_bytes < plane_bytes(T, r)) return SLOPE_ERR_INVALID_ARG;
+  *plane = workspace;
+  return SLOPE_OK;
 }
 
 extern "C" int slope_prune_nm(const void* W, int64_t rows, int64_t cols, int n, int m, void* vals,
@@ -334,12 +354,12 @@ extern "C" int slope_linear_fwd(const void* X, int64_t T, int64_t in, int64_t ou
                                 const uint8_t* Wm, const void* L, const void* R, int r, void* Y,
                                 int y_dtype, void* XL, void* workspace, size_t workspace_bytes,
                                 void* stream) {
-  (void)workspace; (void)workspace_bytes;
   if (int s = check_linear(T, in, out, r)) return s;
   if (y_dtype != SLOPE_F32 && y_dtype != SLOPE_BF16) return SLOPE_ERR_INVALID_ARG;
   if (T == 0) return SLOPE_OK;
   if (!X || !Wv || !Wm || !Y) return SLOPE_ERR_INVALID_ARG;
-  if (r > 0 && (!L || !R || !XL)) return SLOPE_ERR_INVALID_ARG;
+  if (r > 0 && (!L || !R)) return SLOPE_ERR_INVALID_ARG;
+  if (int s = rank_plane(XL, workspace, workspace_bytes, T, r, &XL)) return s;
   if (!aligned16(X) || !aligned16(Wv) || !aligned16(Wm) || !aligned16(Y)) return SLOPE_ERR_ALIGNMENT;
   if (r > 0 && (!aligned16(L) || !aligned16(R) || !aligned16(XL))) return SLOPE_ERR_ALIGNMENT;
   if (int s = check_device()) return s;
@@ -363,12 +383,12 @@ extern "C" int slope_linear_bwd_input(const void* dY, int64_t T, int64_t in, int
                                       const void* Dv, const uint8_t* Dm, const void* L,
                                       const void* R, int r, void* dX, int dx_dtype, void* G,
                                       void* workspace, size_t workspace_bytes, void* stream) {
-  (void)workspace; (void)workspace_bytes;
   if (int s = check_linear(T, in, out, r)) return s;
   if (dx_dtype != SLOPE_F32 && dx_dtype != SLOPE_BF16) return SLOPE_ERR_INVALID_ARG;
   if (T == 0) return SLOPE_OK;
   if (!dY || !Dv || !Dm || !dX) return SLOPE_ERR_INVALID_ARG;
-  if (r > 0 && (!L || !R || !G)) return SLOPE_ERR_INVALID_ARG;
+  if (r > 0 && (!L || !R)) return SLOPE_ERR_INVALID_ARG;
+  if (int s = rank_plane(G, workspace, workspace_bytes, T, r, &G)) return s;
   if (!aligned16(dY) || !aligned16(Dv) || !aligned16(Dm) || !aligned16(dX))
     return SLOPE_ERR_ALIGNMENT;
   if (r > 0 && (!aligned16(L) || !aligned16(R) || !aligned16(G))) return SLOPE_ERR_ALIGNMENT;

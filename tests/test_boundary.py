@@ -134,7 +134,7 @@ def test_linear_argument_checks(L):
     assert fwd(A, -1, 256, 256, A, A, A, A, 8, A, 0, A, None, 0, None) == L.ERR_SHAPE
     assert fwd(A, 64, 256, 256, A, A, A, A, 8, A, 7, A, None, 0, None) == L.ERR_INVALID_ARG
     assert fwd(A, 64, 256, 256, A, A, None, A, 8, A, 0, A, None, 0, None) == L.ERR_INVALID_ARG
-    assert fwd(A, 64, 256, 256, A, A, A, A, 8, A, 0, None, None, 0, None) == L.ERR_INVALID_ARG
+    assert fwd(A, 64, 256, 256, A, A, A, A, 8, A, 0, None, None, 0, None) == L.ERR_INVALID_ARG  # no XL, no workspace
     assert fwd(A, 64, 256, 256, A, A, A, A, 8, MIS, 0, A, None, 0, None) == L.ERR_ALIGNMENT
     assert fwd(A, 0, 256, 256, A, A, A, A, 8, A, 0, A, None, 0, None) == L.OK  # T == 0
     assert bi(A, 64, 256, 384, A, A, A, A, 16, A, 1, None, None, 0, None) == L.ERR_INVALID_ARG
@@ -169,8 +169,30 @@ def test_selftest_argument_checks(L):
     assert f(1 << 40, None) == L.ERR_INVALID_ARG
 
 
-def test_workspace_size_is_a_query(L):
-    assert L.slope_workspace_size(4096, 1024, 1024, 16) >= 0
+def test_workspace_size_is_the_rank_plane(L):
+    # the T x 2r bf16 plane of XL or G, rounded up to 256 bytes
+    assert L.slope_workspace_size(4096, 1024, 1024, 16) == 4 * 4096 * 16
+    assert L.slope_workspace_size(1, 256, 256, 8) == 256
+    assert L.slope_workspace_size(16384, 7168, 28672, 64) == 4 * 16384 * 64
+    assert L.slope_workspace_size(4096, 1024, 1024, 0) == 0   # no adapter, no scratch
+    assert L.slope_workspace_size(4096, 1024, 1024, 12) == 0  # invalid rank
+    assert L.slope_workspace_size(-1, 1024, 1024, 16) == 0
+    assert L.slope_workspace_size(64, 200, 256, 8) == 0
+
+
+@cpu_only
+def test_workspace_argument_checks(L):
+    fwd = L.lib().slope_linear_fwd
+    bi = L.lib().slope_linear_bwd_input
+    need = L.slope_workspace_size(64, 256, 256, 8)
+    # XL (or G) NULL: the workspace must be there and large enough
+    assert fwd(A, 64, 256, 256, A, A, A, A, 8, A, 0, None, None, need, None) == L.ERR_INVALID_ARG
+    assert fwd(A, 64, 256, 256, A, A, A, A, 8, A, 0, None, A, need - 16, None) == L.ERR_INVALID_ARG
+    assert fwd(A, 64, 256, 256, A, A, A, A, 8, A, 0, None, MIS, need, None) == L.ERR_ALIGNMENT
+    assert bi(A, 64, 256, 256, A, A, A, A, 8, A, 0, None, A, 0, None) == L.ERR_INVALID_ARG
+    assert bi(A, 64, 256, 256, A, A, A, A, 8, A, 0, None, MIS, need, None) == L.ERR_ALIGNMENT
+    # no adapter: nothing is needed
+    assert fwd(A, 64, 256, 256, A, A, None, None, 0, MIS, 0, None, None, 0, None) == L.ERR_ALIGNMENT
 
 
 def test_binding_refuses_cpu_tensors(L):

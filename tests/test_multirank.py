@@ -52,3 +52,23 @@ def test_single_process_needs_no_group():
 
     assert bench.max_over_ranks(7.5, "cpu") == 7.5
     assert abs(bench.whole_job_tflops(2e12, 1, 10.0) - 200.0) < 1e-9
+
+
+def test_bench_launcher_runs_replicas():
+    """`bench.py --gpus 2` (no torchrun environment) starts two ranks with
+    RANK / WORLD_SIZE set; rank 0 alone prints the line, with n_gpus 2.  The
+    reference arm runs on the CPU, so this needs no GPU."""
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    res = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2",
+                          "--workload", "single-256", "--steps", "1", "--warmup", "3", "--ref-seconds", "0.1"],
+                         env=env, capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1  # only rank 0 prints
+    line = json.loads(lines[0])
+    assert line["n_gpus"] == 2 and line["impl"] == "reference"

@@ -124,6 +124,13 @@ def test_opt33b_fc1(S, r):
     check_layer(S, 4, 16384, 7168, 28672, r, n_t=32, n_o=192, n_i=192, n_slab=2)
 
 
+@pytest.mark.parametrize("name,inp,out", [("q", 7168, 7168), ("fc2", 28672, 7168)])
+def test_opt33b_q_and_fc2_r64(S, name, inp, out):
+    """The other two shapes of the OPT-33B block at rank 64 (Q stands for
+    K, V and O), whole on the GPU in the benchmark's launch configuration."""
+    check_layer(S, {"q": 0, "fc2": 5}[name], 16384, inp, out, 64, n_t=32, n_o=192, n_i=192, n_slab=2)
+
+
 @pytest.mark.parametrize("T", [1, 16, 128, 2048])
 def test_opt66b_inference_fc1(S, T):
     check_layer(S, 4, T, 9216, 36864, 64, forward_only=True, n_t=64, n_o=512)

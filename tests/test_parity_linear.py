@@ -186,3 +186,56 @@ def test_weight_grad_skip_flags(S):
     assert (dW == 7.0).all()
     torch.testing.assert_close(dL, g["dL"], rtol=1e-5, atol=1e-6)
     torch.testing.assert_close(dR, g["dR"], rtol=1e-5, atol=1e-6)
+
+
+@pytest.mark.parametrize("T,inp,out,r", [(200, 384, 512, 16), (4096, 1024, 4096, 16), (16, 4096, 2048, 64)])
+def test_rank_plane_in_workspace(S, T, inp, out, r):
+    """XL and G passed as NULL: the rank-r plane lives in the caller's
+    workspace (slope_workspace_size bytes).  The same kernels run, so Y and
+    dX are bit for bit those of the calls that keep XL and G, and match the
+    oracle."""
+    import torch
+
+    d = synth.layer_inputs(0, 7 * T + r, T, inp, out, r)
+    g = run_layer(S, d, T, inp, out, r)
+    need = S.slope_workspace_size(T, inp, out, r)
+    assert need == 4 * T * r + (-4 * T * r) % 256
+    ws = torch.full((need,), 0xAB, dtype=torch.uint8, device="cuda")  # contents must not matter
+    X, dY, L, R = to_dev(d["X"]), to_dev(d["dY"]), to_dev(d["L"]), to_dev(d["R"])
+    Y = torch.empty(T, out, dtype=torch.float32, device="cuda")
+    dX = torch.empty(T, inp, dtype=torch.float32, device="cuda")
+    S.slope_linear_fwd(X, g["Wv"], g["Wm"], L, R, Y, None, workspace=ws)
+    S.slope_linear_bwd_input(dY, g["Dv"], g["Dm"], L, R, dX, None, workspace=ws)
+    torch.cuda.synchronize()
+    S.slope_device_status()
+    assert torch.equal(Y, g["Y"]) and torch.equal(dX, g["dX"])
+    # the plane holds the last call's G (hi | lo), exactly as the output G
+    assert torch.equal(ws[: T * 4 * r].view(torch.bfloat16).view(T, 2 * r), g["G"])
+    vals, meta, _ = O.prune24(d["W"])
+    tv, tm, _ = O.double_prune24(vals, meta, out, inp)
+    assert_close_rel("Y", np64(Y), O.linear_fwd(d["X"], vals, meta, d["L"], d["R"])[0])
+    assert_close_rel("dX", np64(dX), O.linear_bwd_input(d["dY"], tv, tm, d["L"], d["R"])[0])
+
+
+def test_weight_grad_accumulates_under_split_k(S):
+    """Many tokens on a small weight: the dW launch splits K and adds its
+    parts atomically.  With SLOPE_ACCUMULATE the call adds dW, dL and dR
+    onto what the buffers held: result = before + oracle."""
+    import torch
+
+    T, inp, out, r = 16384, 256, 256, 8
+    d = synth.layer_inputs(0, 31, T, inp, out, r)
+    g = run_layer(S, d, T, inp, out, r)
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    before = {k: torch.randn(g[k].shape, generator=gen, device="cuda") * 50 for k in ("dW", "dL", "dR")}
+    acc = {k: v.clone() for k, v in before.items()}
+    S.slope_linear_bwd_weight(to_dev(d["dY"]), to_dev(d["X"]), g["Wm"], g["XL"], g["G"],
+                              acc["dW"], acc["dL"], acc["dR"], flags=S.ACCUMULATE)
+    torch.cuda.synchronize()
+    S.slope_device_status()
+    vals, meta, _ = O.prune24(d["W"])
+    dWc, _, dL, dR = O.linear_bwd_weight(d["dY"], d["X"], meta, d["L"], d["R"])
+    for name, ref in (("dW", dWc), ("dL", dL), ("dR", dR)):
+        assert_close_rel(name, np64(acc[name]), np64(before[name]) + ref)
+    # and the overwriting call on the same split matches the oracle alone
+    assert_close_rel("dW", np64(g["dW"]), dWc)
