@@ -439,7 +439,9 @@ def dw_bytes(T, inp, out, r):
 # (dram__bytes_read.sum + dram__bytes_write.sum; outputs a short kernel
 # leaves dirty in L2 are not yet written).  Only kernels unchanged since their
 # capture are listed.
-NCU_TRAFFIC = {("opt-350m-block", "bwd_weight"): 30.44e6}
+NCU_TRAFFIC = {("opt-350m-block", "bwd_weight"): 30.44e6,
+               # one launch of each linear shape, averaged over the block's six
+               ("opt-33b-block-r64", "bwd_weight"): 6.743e9}
 
 
 def sub_workload(wl, linear):
