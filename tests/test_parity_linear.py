@@ -71,6 +71,7 @@ CASES = [
     (4096, 1024, 1024, 16),  # OPT-350M block linears
     (4096, 1024, 4096, 16),
     (4096, 4096, 1024, 16),
+    (300, 256, 384, 256),   # the largest rank the ABI takes: four adapter blocks per part
 ]
 
 
