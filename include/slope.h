@@ -259,6 +259,44 @@ int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T, int64_t in
                             size_t workspace_bytes, void* stream);
 
 /*
+ * Size of the library's own scratch array used by
+ * slope_linear_fwd_static_scratch: 8 MiB, room for the rank-r plane of
+ * T·r <= 2,097,152 (for example T = 16384 tokens at rank 128).
+ */
+#define SLOPE_STATIC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * The forward A3 (as slope_linear_fwd) for callers that cannot allocate
+ * device memory and so have no workspace to pass: a plugin inside a host
+ * runtime that owns every allocation and hands it only inputs and outputs,
+ * or a serving loop that must never call cudaMalloc on its hot path (an
+ * allocation can synchronise the device and stall other streams).  This
+ * call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine): the rank-r plane X·L that slope_linear_fwd would keep in XL or
+ * in the workspace lives in a fixed SLOPE_STATIC_SCRATCH_BYTES array of
+ * device memory that the library declares and every GPU that loads the
+ * library holds until the process exits.  The caller still passes the
+ * inputs and Y; the plane itself is not returned (use slope_linear_fwd with
+ * XL when the backward needs it).  Arguments, layouts and results are those
+ * of slope_linear_fwd with XL = NULL: the same kernels run.
+ *  - Sizes whose plane (4·T·r bytes) exceeds SLOPE_STATIC_SCRATCH_BYTES
+ *    return SLOPE_ERR_SHAPE before any work; other argument errors are
+ *    slope_linear_fwd's.  r == 0 and T == 0 use no scratch.
+ *  - The first call on a device looks up the array's device address on that
+ *    device (with it current) and keeps it; make that first call before any
+ *    stream capture.
+ *  - All calls share the one array, which keeps the last call's plane.
+ *    Calls whose work overlaps on the GPU (different streams with no
+ *    ordering between them, or different host threads) race on it: order
+ *    them on one stream, or with events.
+ * The SLoPe pages have no counterpart: this is a deployment form of the
+ * forward, not a step of the method.
+ */
+int slope_linear_fwd_static_scratch(const void* X, int64_t T, int64_t in, int64_t out,
+                                    const void* Wv, const uint8_t* Wm, const void* L,
+                                    const void* R, int r, void* Y, int y_dtype, void* stream);
+
+/*
  * Synchronises `stream`, then reports and clears the device status word in
  * which kernels record a bounded wait that ran out (SLOPE_ERR_TIMEOUT), or
  * returns SLOPE_OK.  A CUDA error seen while synchronising returns

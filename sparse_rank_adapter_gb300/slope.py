@@ -37,6 +37,7 @@ SIGNATURES = (
     ("slope_linear_fwd", _i, (_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _vp, _sz, _vp)),
     ("slope_linear_bwd_input", _i, (_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _vp, _sz, _vp)),
     ("slope_linear_bwd_weight", _i, (_vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _i, _vp, _u32, _vp, _vp, _vp, _sz, _vp)),
+    ("slope_linear_fwd_static_scratch", _i, (_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp)),
     ("slope_device_status", _i, (_vp,)),
     ("slope_selftest_wait_timeout", _i, (_i64, _vp)),
     ("slope_selftest_mma_rate", _i, (_i, _i, _i64, ctypes.POINTER(ctypes.c_double), _vp)),
@@ -264,6 +265,28 @@ def slope_linear_bwd_weight(dY, X, Wm, XL, G, dW, dL=None, dR=None, flags: int =
         _ptr(dL, torch.float32, (inp, r), "dL"), _ptr(dR, torch.float32, (r, out), "dR"),
         _ptr(workspace, name="workspace"), ws_bytes, _stream(stream))
     _check(st, "slope_linear_bwd_weight")
+
+
+STATIC_SCRATCH_BYTES = 8 << 20  # SLOPE_STATIC_SCRATCH_BYTES
+
+
+def slope_linear_fwd_static_scratch(X, Wv, Wm, L, R, Y, stream=None):
+    """A3 for callers that cannot allocate device memory: Y = X·Wsᵀ + (X·L)·R
+    with the rank-r plane in the library's own fixed device array (4·T·r
+    bytes at most STATIC_SCRATCH_BYTES).  Calls that overlap on the GPU race
+    on that array; the first call on a device must come before any stream
+    capture."""
+    import torch
+
+    T, inp = X.shape
+    out = Wv.shape[0]
+    r = 0 if L is None else L.shape[1]
+    st = lib().slope_linear_fwd_static_scratch(
+        _ptr(X, torch.bfloat16, name="X"), T, inp, out,
+        _ptr(Wv, torch.bfloat16, (out, inp // 2), "Wv"), _ptr(Wm, torch.uint8, (out, inp // 8), "Wm"),
+        _ptr(L, torch.bfloat16, (inp, r), "L"), _ptr(R, torch.bfloat16, (r, out), "R"), r,
+        _ptr(Y, None, (T, out), "Y"), _dtype_code(Y), _stream(stream))
+    _check(st, "slope_linear_fwd_static_scratch")
 
 
 def slope_device_status(stream=None):
