@@ -441,7 +441,7 @@ def dw_bytes(T, inp, out, r):
 # capture are listed.
 NCU_TRAFFIC = {("opt-350m-block", "bwd_weight"): 30.44e6,
                # one launch of each linear shape, averaged over the block's six
-               ("opt-33b-block-r64", "bwd_weight"): 6.743e9}
+               ("opt-33b-block-r64", "bwd_weight"): 5.892e9}
 
 
 def sub_workload(wl, linear):

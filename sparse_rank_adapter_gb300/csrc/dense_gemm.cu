@@ -42,6 +42,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 
 #include "slope_internal.h"
@@ -77,7 +78,7 @@ struct DnParams {
   int M, N, K;
   int kb_per_split, num_kb;
   int tiles_m, tiles_n, num_tiles;  // tiles = tiles_m x tiles_n x splits
-  int group_n;                      // pair kernel: N tiles per raster band
+  int group_m;                      // pair kernel: M pairs per raster band
   int64_t ldo;
   void* out;
   const uint8_t* meta;  // masked dW: metadata, N/8 bytes per row
@@ -543,20 +544,21 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const int ustep = static_cast<int>(gridDim.x >> 1);
   // unit -> (this CTA's rows m0, the pair's columns n0, split z, kind: 0 dW,
   // 1 dRᵀ, 2 dLᵀ).  dW tiles in raster order within a split: bands of
-  // group_n N tiles; within a band the N tiles turn fastest, then the M
-  // pairs, so the band's X tiles stay in L2 while each dY tile is used by
-  // the whole band as soon as it is loaded.
+  // group_m M pairs; within a band the M pairs turn fastest, then the N
+  // tiles.  The pairs in flight (consecutive units) then cover a block about
+  // as tall as it is wide, which loads the fewest operand slabs (256 rows of
+  // dY or 256 columns of X over the split's K range) per wave of tiles.
   auto decode = [&](int u, int& m0, int& n0, int& z, int& kind) {
     const int mn = u % per_split;
     z = u / per_split;
     if (mn < w_tiles) {
       kind = 0;
-      const int per_band = p.group_n * pairs_m;
+      const int per_band = p.group_m * p.tiles_n;
       const int b = mn / per_band, w = mn % per_band;
-      const int first = b * p.group_n;
-      const int gn = min(p.group_n, p.tiles_n - first);
-      m0 = (2 * (w / gn) + static_cast<int>(rank)) * kBM;  // this CTA's 128 rows
-      n0 = (first + w % gn) * kPairBN;                       // the pair's 256 columns
+      const int first = b * p.group_m;
+      const int gm = min(p.group_m, pairs_m - first);
+      m0 = (2 * (first + w % gm) + static_cast<int>(rank)) * kBM;  // this CTA's 128 rows
+      n0 = (w / gm) * kPairBN;                                       // the pair's 256 columns
     } else if (mn < w_tiles + pairs_m) {
       kind = 1;
       m0 = (2 * (mn - w_tiles) + static_cast<int>(rank)) * kBM;
@@ -815,10 +817,16 @@ cudaError_t run_dw_pair(const DenseGemmArgs& a, cudaStream_t stream) {
   p.fuse_r = fr;
   p.dl = a.dl;
   p.dr = a.dr;
-  {  // a band of X tiles (256 columns over the split's K range) of about 40 MB
-    const double tile_bytes = 2.0 * kPairBN * kBK * kbs;
-    int g = static_cast<int>(40.0e6 / tile_bytes);
-    p.group_n = g < 1 ? 1 : (g > tiles_n ? tiles_n : g);
+  {
+    // The units in flight (about one per resident pair) should form a
+    // block whose slabs of dY (M) and X (N), equal in bytes, are fewest:
+    // about sqrt(pairs) M pairs tall.  Bands of as even a height as that
+    // allows, so no thin band is left at the bottom.
+    int want = static_cast<int>(std::lround(std::sqrt(static_cast<double>(clusters_max))));
+    const int pairs_m = tiles_m / 2;
+    want = want < 1 ? 1 : (want > pairs_m ? pairs_m : want);
+    const int bands = (pairs_m + want - 1) / want;
+    p.group_m = (pairs_m + bands - 1) / bands;
   }
   p.ldo = a.ldo; p.out = a.out; p.meta = a.meta;
   p.dense_dw = a.dense_dw ? 1 : 0;
