@@ -349,6 +349,128 @@ def linear_bwd_weight(dY, X, Wm, L, R):
 
 
 # ---------------------------------------------------------------------------
+# Other N:M patterns (§2.1 "Double-pruned backward pass" names 1:2, 2:4 and
+# 2:8, with §T.1's count of the zeros the second pruning adds to each)
+# ---------------------------------------------------------------------------
+#
+# 1:2 keeps one entry of every aligned pair.  Two aligned pairs make an
+# aligned quadruple with exactly two kept entries, one in each half, so a
+# 1:2-pruned matrix is also 2:4 and is stored in the 2:4 format above
+# (i0 in {0, 1}, i1 in {2, 3}).
+#
+# 2:8 keeps two entries of every aligned group of eight.  Its format:
+#   vals: rows x cols/4, the two kept entries of each group in ascending
+#         column order;
+#   meta: rows x cols/8 bytes, one per group: i0 | i1 << 3 (i0 < i1).
+# A 2:8-pruned matrix is also 2:4 (no quadruple holds more than two of the
+# group's two entries); its 2:4 form keeps, in each quadruple, the group's
+# entries that fall in it, padded to two with the quadruple's lowest-index
+# remaining positions, which hold +0.
+
+
+def prune12(bits: np.ndarray):
+    """1:2 prune-and-compress into the 2:4 format: per aligned pair the entry
+    of larger magnitude key, the lower column on ties.  Returns (vals rows x
+    cols/2, meta rows x cols/8, mask rows x cols)."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    rows, cols = bits.shape
+    if cols % 8:
+        raise ValueError("the 2:4 format needs cols % 8 == 0")
+    pair = select_nm(bits, 1, 2).reshape(rows, cols // 4, 2)  # index within each pair
+    sel = np.stack([pair[..., 0], 2 + pair[..., 1]], axis=-1)  # ascending quadruple indices
+    grouped = bits.reshape(rows, cols // 4, 4)
+    vals = np.take_along_axis(grouped, sel, axis=-1).reshape(rows, cols // 2)
+    return vals.astype(np.uint16), pack_meta24(sel), mask_from_selection(sel, 4)
+
+
+def double_prune12(vals: np.ndarray, meta: np.ndarray, rows: int, cols: int):
+    """Second 1:2 pruning: the rows x cols 1:2-pruned weight (2:4 format) is
+    expanded (pruned entries +0), transposed, and pruned 1:2 again along the
+    old out dimension.  Returns (t_vals cols x rows/2, t_meta cols x rows/8,
+    t_mask cols x rows), in the 2:4 format."""
+    if rows % 8:
+        raise ValueError("double pruning needs rows % 8 == 0")
+    ws = decompress24(vals, meta, cols)
+    return prune12(np.ascontiguousarray(ws.T))
+
+
+def pack_meta28(sel: np.ndarray) -> np.ndarray:
+    """[rows, groups, 2] ascending kept indices (0..7) -> rows x groups bytes."""
+    return (sel[..., 0] | (sel[..., 1] << 3)).astype(np.uint8)
+
+
+def unpack_meta28(meta: np.ndarray) -> np.ndarray:
+    """rows x cols/8 bytes -> [rows, cols/8, 2] kept indices."""
+    meta = np.asarray(meta, dtype=np.uint8).astype(np.int64)
+    return np.stack([meta & 7, (meta >> 3) & 7], axis=-1)
+
+
+def prune28(bits: np.ndarray):
+    """2:8 prune-and-compress: the two entries of largest magnitude key of
+    each aligned group of eight, lower columns first on ties.  Returns (vals
+    rows x cols/4, meta rows x cols/8, mask rows x cols)."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    rows, cols = bits.shape
+    if cols % 8:
+        raise ValueError("2:8 needs cols % 8 == 0")
+    sel = select_nm(bits, 2, 8)
+    grouped = bits.reshape(rows, cols // 8, 8)
+    vals = np.take_along_axis(grouped, sel, axis=-1).reshape(rows, cols // 4)
+    return vals.astype(np.uint16), pack_meta28(sel), mask_from_selection(sel, 8)
+
+
+def decompress28(vals: np.ndarray, meta: np.ndarray, cols: int) -> np.ndarray:
+    """2:8 (vals, meta) -> rows x cols bf16 patterns, zeros elsewhere."""
+    vals = np.asarray(vals, dtype=np.uint16)
+    rows = vals.shape[0]
+    out = np.zeros((rows, cols // 8, 8), dtype=np.uint16)
+    np.put_along_axis(out, unpack_meta28(meta), vals.reshape(rows, cols // 8, 2), axis=-1)
+    return out.reshape(rows, cols)
+
+
+def double_prune28(vals: np.ndarray, meta: np.ndarray, rows: int, cols: int):
+    """Second 2:8 pruning of the transposed 2:8-pruned weight, along the old
+    out dimension (pruned entries key 0, so a group with fewer than two
+    non-zeros keeps its lowest-index remaining positions, +0).  Returns
+    (t_vals cols x rows/4, t_meta cols x rows/8, t_mask cols x rows)."""
+    if rows % 8:
+        raise ValueError("double pruning needs rows % 8 == 0")
+    ws = decompress28(vals, meta, cols)
+    return prune28(np.ascontiguousarray(ws.T))
+
+
+def expand28_to_24(vals: np.ndarray, meta: np.ndarray, cols: int):
+    """The 2:4 form of a 2:8-compressed matrix: each quadruple keeps the
+    group's entries that fall in it, padded to two with its lowest-index
+    remaining positions (value +0), in ascending order.  Returns (vals24
+    rows x cols/2, meta24 rows x cols/8)."""
+    dense = decompress28(vals, meta, cols)
+    rows = dense.shape[0]
+    keep = mask_from_selection(unpack_meta28(meta), 8).reshape(rows, cols // 4, 4)
+    sel = np.zeros((rows, cols // 4, 2), dtype=np.int64)
+    for r in range(rows):
+        for q in range(cols // 4):
+            kept = [j for j in range(4) if keep[r, q, j]]
+            pad = [j for j in range(4) if not keep[r, q, j]]
+            sel[r, q] = sorted(kept + pad[: 2 - len(kept)])
+    v = np.take_along_axis(dense.reshape(rows, cols // 4, 4), sel, axis=-1).reshape(rows, cols // 2)
+    return v.astype(np.uint16), pack_meta24(sel)
+
+
+def linear_bwd_weight28(dY, X, Wm28, L, R):
+    """A5 + A6 with a 2:8 weight: dW = M ⊙ (dYᵀ·X), M the 2:8 mask of the
+    weight, compressed in the 2:8 format (out x in/4), and dense; dL, dR as
+    for 2:4.  Returns (dW_compressed, dW_dense, dL, dR)."""
+    dYf, Xf = bf16_to_f64(dY), bf16_to_f64(X)
+    out, inn = dYf.shape[1], Xf.shape[1]
+    sel = unpack_meta28(Wm28)
+    mask = mask_from_selection(sel, 8)
+    dW_dense, dL, dR = backward_weight_f64(dYf, Xf, mask, *_adapter(L, R))
+    dW_comp = np.take_along_axis(dW_dense.reshape(out, inn // 8, 8), sel, axis=-1)
+    return dW_comp.reshape(out, inn // 4), dW_dense, dL, dR
+
+
+# ---------------------------------------------------------------------------
 # Lemma 2.1 (§T.1): expected zeros added by the second N:M pruning
 # ---------------------------------------------------------------------------
 

@@ -460,3 +460,152 @@ def test_frozen_double_prune_fixed_point_and_gather():
     vals, tvals = O.recompress_frozen24(W, m, tmf)
     np.testing.assert_array_equal(vals, v)
     np.testing.assert_array_equal(tvals, got)
+
+
+# ---------------------------------------------------- 1:2 and 2:8 patterns --
+
+
+def _keys(bits):
+    return (np.asarray(bits, dtype=np.uint16).astype(np.int64) & 0x7FFF)
+
+
+def _best_pair(keys8):
+    """Brute force over all C(8, 2) pairs: the largest key sum, then the
+    lexicographically smallest pair (ascending indices)."""
+    best = None
+    for a, b in itertools.combinations(range(len(keys8)), 2):
+        cand = (keys8[a] + keys8[b], -a, -b)
+        if best is None or cand > best[0]:
+            best = (cand, (a, b))
+    return best[1]
+
+
+def test_prune12_hand_example():
+    # pairs: (1, -3) keeps -3; (2, 2) a tie, the lower; (0, -0) a tie at key 0,
+    # the lower; (5, -5) a tie, the lower
+    row = bits_of([[1, -3, 2, 2, 0, -0.0, 5, -5]])
+    vals, meta, mask = O.prune12(row)
+    np.testing.assert_array_equal(vals[0], row[0, [1, 2, 4, 6]])
+    # quadruple 0 keeps (1, 2) -> 0b1001, quadruple 1 keeps (0, 2) -> 0b1000
+    assert meta[0, 0] == 0x89
+    assert mask[0].tolist() == [False, True, True, False, True, False, True, False]
+
+
+def test_prune12_invariants():
+    W = synth.normal_bf16(0, 7, "W", (64, 96))
+    vals, meta, mask = O.prune12(W)
+    sel = O.unpack_meta24(meta)
+    assert ((sel[..., 0] < 2) & (sel[..., 1] >= 2)).all()  # one kept in each half
+    assert (mask.reshape(64, 48, 2).sum(-1) == 1).all()
+    np.testing.assert_array_equal(O.decompress24(vals, meta, 96), np.where(mask, W, np.uint16(0)))
+    # each pair keeps the entry of larger key, the lower on ties
+    k = _keys(W).reshape(64, 48, 2)
+    np.testing.assert_array_equal(mask.reshape(64, 48, 2)[..., 1], k[..., 1] > k[..., 0])
+
+
+def test_double_prune12_is_brute_force_on_the_transpose():
+    rng = np.random.default_rng(3)
+    W = bits_of(rng.integers(-3, 4, size=(16, 24)).astype(np.float32))  # many ties and zeros
+    vals, meta, mask = O.prune12(W)
+    tv, tm, tmask = O.double_prune12(vals, meta, 16, 24)
+    ws = np.where(mask, W, np.uint16(0))
+    wt, kt = ws.T, _keys(ws.T)
+    for i in range(24):
+        for p in range(8):
+            keep = 2 * p + (1 if kt[i, 2 * p + 1] > kt[i, 2 * p] else 0)
+            assert tmask[i, keep] and not tmask[i, keep ^ 1]
+    np.testing.assert_array_equal(O.decompress24(tv, tm, 16), np.where(tmask, wt, np.uint16(0)))
+    # the second pruning only removes: D's support is inside Wsᵀ's
+    assert not (np.where(tmask, kt, 0) > 0)[~mask.T].any()
+
+
+def test_prune28_hand_example():
+    row = bits_of([[1, -7, 3, 7, 0, 2, -2, 5, 2, 2, 2, 2, 2, 2, 2, 2]])
+    vals, meta, mask = O.prune28(row)
+    # group 0: |-7| and |7| at 1 and 3 -> 1 | 3 << 3 = 0x19; group 1: all tie -> (0, 1)
+    assert meta[0].tolist() == [0x19, 0x08]
+    np.testing.assert_array_equal(vals[0], row[0, [1, 3, 8, 9]])
+    assert mask[0].sum() == 4
+
+
+def test_prune28_invariants_and_decompress():
+    W = synth.normal_bf16(0, 8, "W", (40, 64))
+    vals, meta, mask = O.prune28(W)
+    assert (meta >> 6 == 0).all()
+    sel = O.unpack_meta28(meta)
+    assert (sel[..., 0] < sel[..., 1]).all()
+    assert (mask.reshape(40, 8, 8).sum(-1) == 2).all()
+    np.testing.assert_array_equal(O.decompress28(vals, meta, 64), np.where(mask, W, np.uint16(0)))
+    k = _keys(W).reshape(40, 8, 8)
+    for r in range(40):
+        for g in range(8):
+            assert tuple(sel[r, g]) == _best_pair([int(x) for x in k[r, g]])
+
+
+def test_double_prune28_is_brute_force_on_the_transpose():
+    rng = np.random.default_rng(4)
+    W = bits_of(rng.integers(-2, 3, size=(32, 16)).astype(np.float32))
+    vals, meta, mask = O.prune28(W)
+    tv, tm, tmask = O.double_prune28(vals, meta, 32, 16)
+    ws = np.where(mask, W, np.uint16(0))
+    kt = _keys(ws.T)
+    sel = O.unpack_meta28(tm)
+    for i in range(16):
+        for h in range(4):
+            assert tuple(sel[i, h]) == _best_pair([int(x) for x in kt[i, 8 * h:8 * h + 8]])
+    np.testing.assert_array_equal(O.decompress28(tv, tm, 32), np.where(tmask, ws.T, np.uint16(0)))
+
+
+@pytest.mark.parametrize("n,m", [(1, 2), (2, 8)])
+def test_double_prunes_drop_what_lemma21_counts(n, m):
+    """The zeros each double prune adds equal the count of the lemma's
+    measurement helper, and sit within 5 sigma of its binomial value."""
+    W = synth.normal_bf16(0, 9, "W", (512, 512))
+    if (n, m) == (1, 2):
+        v, mt, mask = O.prune12(W)
+        _, _, tmask = O.double_prune12(v, mt, 512, 512)
+    else:
+        v, mt, mask = O.prune28(W)
+        _, _, tmask = O.double_prune28(v, mt, 512, 512)
+    ws = np.where(mask, W, np.uint16(0)).T
+    before = np.count_nonzero(_keys(ws))
+    after = np.count_nonzero(_keys(np.where(tmask, ws, np.uint16(0))))
+    added = (before - after) / W.size
+    assert added == pytest.approx(O.added_sparsity_measured(W, n, m), abs=0)
+    expect = O.added_sparsity_expected(n, m)
+    assert expect == pytest.approx(0.125 if m == 2 else 0.05840, abs=1e-4)
+    assert abs(added - expect) < 0.01
+
+
+def test_expand28_to_24_hand_example_and_invariants():
+    row = bits_of([[1, -7, 3, 7, 0, 2, -2, 5, 9, 0, 0, 0, 0, 0, 0, 8]])
+    vals, meta, _ = O.prune28(row)
+    v24, m24 = O.expand28_to_24(vals, meta, 16)
+    # group 0: both kept in quadruple 0 at (1, 3) -> 0xD; quadruple 1 pads (0, 1) -> 0x4
+    # group 1: 9 at 0 and 8 at 7: quadruple 2 keeps 0 and pads 1 -> 0x4; quadruple 3 keeps 3, pads 0 -> 0xC
+    assert m24[0].tolist() == [0x4D, 0xC4]
+    z = np.uint16(0)
+    np.testing.assert_array_equal(v24[0], [row[0, 1], row[0, 3], z, z, row[0, 8], z, z, row[0, 15]])
+    W = synth.normal_bf16(0, 10, "W", (24, 64))
+    vals, meta, mask = O.prune28(W)
+    v24, m24 = O.expand28_to_24(vals, meta, 64)
+    np.testing.assert_array_equal(O.decompress24(v24, m24, 64), O.decompress28(vals, meta, 64))
+    sel24 = O.mask_from_selection(O.unpack_meta24(m24), 4)
+    assert (sel24 | ~mask).all()  # the 2:4 form keeps every 2:8 entry
+
+
+def test_weight_grad28_is_an_explicit_gather():
+    d = synth.layer_inputs(0, 12, 10, 32, 16, 4)
+    vals, meta, mask = O.prune28(d["W"])
+    dWc, dWd, dL, dR = O.linear_bwd_weight28(d["dY"], d["X"], meta, d["L"], d["R"])
+    dY, X = O.bf16_to_f64(d["dY"]), O.bf16_to_f64(d["X"])
+    sel = O.unpack_meta28(meta)
+    for o in range(16):
+        for g in range(4):
+            for j in range(2):
+                i = 8 * g + int(sel[o, g, j])
+                assert dWc[o, 2 * g + j] == pytest.approx(sum(dY[t, o] * X[t, i] for t in range(10)), rel=1e-12)
+    assert (dWd[~mask] == 0).all()
+    _, _, dL24, dR24 = O.linear_bwd_weight(d["dY"], d["X"], O.prune24(d["W"])[1], d["L"], d["R"])
+    np.testing.assert_allclose(dL, dL24, rtol=1e-12)  # the adapter gradients ignore the mask
+    np.testing.assert_allclose(dR, dR24, rtol=1e-12)
