@@ -70,7 +70,7 @@ typedef enum {
   SLOPE_ERR_INVALID_ARG = 1, /* NULL pointer, bad flag or dtype, short workspace */
   SLOPE_ERR_SHAPE = 2,       /* a size breaks the rules of the call */
   SLOPE_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned */
-  SLOPE_ERR_UNSUPPORTED = 4, /* device is not sm_103, or n:m other than 2:4 */
+  SLOPE_ERR_UNSUPPORTED = 4, /* device is not sm_103, or an n:m the call does not take */
   SLOPE_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
   SLOPE_ERR_TIMEOUT = 6      /* a bounded device-side wait ran out */
 } slope_status;
@@ -82,6 +82,7 @@ typedef enum { SLOPE_F32 = 0, SLOPE_BF16 = 1 } slope_dtype;
 #define SLOPE_ACCUMULATE 2u   /* add into dW, dL, dR instead of overwriting */
 #define SLOPE_SKIP_DW 4u      /* compute dL, dR only (dW is not touched) */
 #define SLOPE_SKIP_ADAPTER 8u /* compute dW only (dL, dR are not touched) */
+#define SLOPE_DW_NM28 16u     /* Wm is a 2:8 metadata; compressed dW is out x in/4 */
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* slope_status_string(int status);
@@ -103,11 +104,18 @@ size_t slope_workspace_size(int64_t T, int64_t in, int64_t out, int r);
 
 /*
  * A1 — N:M magnitude prune-and-compress (§1, §2.1, §2.3; App. K, where the
- * weight is pruned and packed for the sparse product).  For each row of W (rows x cols bf16) and each aligned group
- * of 4 columns, keep the 2 entries of largest |w| (lower index on ties) and
- * write them to `vals` (rows x cols/2 bf16) with their positions in `meta`
- * (rows x cols/8 bytes), in the compressed format above.
- * Requires n == 2 and m == 4 (else SLOPE_ERR_UNSUPPORTED), rows >= 1 and
+ * weight is pruned and packed for the sparse product).  For each row of W
+ * (rows x cols bf16), keep the n entries of largest |w| (lower index on
+ * ties) of every aligned group of m columns:
+ *   2:4 — `vals` rows x cols/2 bf16, `meta` rows x cols/8, the 2:4 format;
+ *   1:2 — one entry per aligned pair, written in the 2:4 format (each
+ *         quadruple keeps one entry of each half: i0 in {0, 1}, i1 in
+ *         {2, 3}), so the 2:4 sparse products take it as it is;
+ *   2:8 — the 2:8 format: `vals` rows x cols/4 bf16 (a group's two kept
+ *         entries, ascending), `meta` rows x cols/8 bytes, one per group of
+ *         eight columns: i0 | i1 << 3 (i0 < i1).  slope_expand_nm_to_24
+ *         gives the 2:4 form the sparse products read.
+ * Other n:m return SLOPE_ERR_UNSUPPORTED.  Requires rows >= 0 and
  * cols % 8 == 0 (else SLOPE_ERR_SHAPE).  rows == 0 is a no-op.
  */
 int slope_prune_nm(const void* W, int64_t rows, int64_t cols, int n, int m, void* vals,
@@ -126,6 +134,35 @@ int slope_prune_nm(const void* W, int64_t rows, int64_t cols, int n, int m, void
  */
 int slope_double_prune(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols,
                        void* t_vals, uint8_t* t_meta, void* stream);
+
+/*
+ * A2 for any of the library's patterns (§2.1: the transpose is pruned with
+ * the same N:M pattern along the input gradient's reduction dimension).
+ * n:m = 2:4 is slope_double_prune.  1:2: `vals`/`meta` are a rows x cols
+ * matrix in the 2:4 format (e.g. slope_prune_nm's 1:2 output); `t_vals`
+ * (cols x rows/2) and `t_meta` (cols x rows/8) receive its transpose pruned
+ * 1:2 along the old rows, in the 2:4 format.  2:8: `vals` (rows x cols/4)
+ * and `meta` (rows x cols/8) in the 2:8 format; `t_vals` (cols x rows/4)
+ * and `t_meta` (cols x rows/8) receive the transpose pruned 2:8, in the 2:8
+ * format.  Pruned-away positions count as +0 (key 0): a group with fewer
+ * than n non-zeros keeps its lowest-index remaining positions, +0 there.
+ * Requires rows % 8 == 0 and cols % 16 == 0 (else SLOPE_ERR_SHAPE); other
+ * n:m return SLOPE_ERR_UNSUPPORTED.
+ */
+int slope_double_prune_nm(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols,
+                          int n, int m, void* t_vals, uint8_t* t_meta, void* stream);
+
+/*
+ * The 2:4 form of a 2:8-format rows x cols matrix (§2.1's 2:8 pattern run on
+ * the 2:4 sparse tensor cores): `vals24` (rows x cols/2 bf16) and `meta24`
+ * (rows x cols/8) in the 2:4 format.  Each quadruple keeps the group's
+ * entries that fall in it, padded to two with its lowest-index other
+ * positions, which hold +0; the dense matrix is unchanged.  Only n:m = 2:8
+ * (else SLOPE_ERR_UNSUPPORTED).  Requires cols % 8 == 0 (else
+ * SLOPE_ERR_SHAPE); rows == 0 is a no-op.
+ */
+int slope_expand_nm_to_24(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols,
+                          int n, int m, void* vals24, uint8_t* meta24, void* stream);
 
 /*
  * A1 + A2 in one call (§2.3: both compressed copies are made from the same
@@ -247,7 +284,10 @@ int slope_linear_bwd_input(const void* dY, int64_t T, int64_t in, int64_t out, c
  * XL (T x 2r) and G (T x 2r) are the hi/lo outputs of the two calls above;
  * dL (in x r f32) and dR (r x out f32) are written when r > 0.
  * SLOPE_ACCUMULATE adds into dW, dL, dR (gradient accumulation) instead of
- * overwriting them.  SLOPE_SKIP_DW computes only dL and dR (dW and Wm may be
+ * overwriting them.  SLOPE_DW_NM28: Wm is the 2:8 metadata of a 2:8 weight
+ * (out x in/8 bytes, slope_prune_nm's 2:8 output) and M its 2:8 mask; the
+ * compressed dW is then out x in/4 (the kept entries in the 2:8 `vals`
+ * order).  SLOPE_SKIP_DW computes only dL and dR (dW and Wm may be
  * NULL); SLOPE_SKIP_ADAPTER computes only dW (XL, G, dL, dR may be NULL);
  * both together are SLOPE_ERR_INVALID_ARG.  T == 0 writes zeros (or leaves
  * them, when accumulating).  This call needs no scratch: `workspace` is

@@ -446,13 +446,10 @@ def expand28_to_24(vals: np.ndarray, meta: np.ndarray, cols: int):
     rows x cols/2, meta24 rows x cols/8)."""
     dense = decompress28(vals, meta, cols)
     rows = dense.shape[0]
-    keep = mask_from_selection(unpack_meta28(meta), 8).reshape(rows, cols // 4, 4)
-    sel = np.zeros((rows, cols // 4, 2), dtype=np.int64)
-    for r in range(rows):
-        for q in range(cols // 4):
-            kept = [j for j in range(4) if keep[r, q, j]]
-            pad = [j for j in range(4) if not keep[r, q, j]]
-            sel[r, q] = sorted(kept + pad[: 2 - len(kept)])
+    keep = mask_from_selection(unpack_meta28(meta), 8)
+    # "kept entries first, then the lowest free index" is the 2:4 selection
+    # itself, run on keys that are 1 at kept positions and 0 elsewhere
+    sel = select_nm(keep.astype(np.uint16), 2, 4)
     v = np.take_along_axis(dense.reshape(rows, cols // 4, 4), sel, axis=-1).reshape(rows, cols // 2)
     return v.astype(np.uint16), pack_meta24(sel)
 

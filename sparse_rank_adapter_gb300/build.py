@@ -16,7 +16,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libslope.so")
-SOURCES = ("api.cu", "prune.cu", "sparse_gemm.cu", "dense_gemm.cu", "mma_rate.cu", "static_scratch.cu")
+SOURCES = ("api.cu", "prune.cu", "sparse_gemm.cu", "dense_gemm.cu", "mma_rate.cu", "static_scratch.cu", "nm_patterns.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-cudart", "shared"]

@@ -253,15 +253,53 @@ static int rank_plane(void* given, void* workspace, size_t workspace_bytes, int6
   return SLOPE_OK;
 }
 
+// The N:M patterns the library prunes: 2:4, 1:2 (written in the 2:4
+// format) and 2:8 (its own format).
+static bool known_pattern(int n, int m) {
+  return (n == 2 && m == 4) || (n == 1 && m == 2) || (n == 2 && m == 8);
+}
+
 extern "C" int slope_prune_nm(const void* W, int64_t rows, int64_t cols, int n, int m, void* vals,
                               uint8_t* meta, void* stream) {
-  if (n != 2 || m != 4) return SLOPE_ERR_UNSUPPORTED;
+  if (!known_pattern(n, m)) return SLOPE_ERR_UNSUPPORTED;
   if (rows < 0 || cols <= 0 || cols % 8 != 0) return SLOPE_ERR_SHAPE;
   if (rows == 0) return SLOPE_OK;
   if (!W || !vals || !meta) return SLOPE_ERR_INVALID_ARG;
   if (!aligned16(W) || !aligned16(vals) || !aligned16(meta)) return SLOPE_ERR_ALIGNMENT;
   if (int s = check_device()) return s;
-  return from_cuda(launch_prune24(W, rows, cols, vals, meta, static_cast<cudaStream_t>(stream)));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (m == 8) return from_cuda(launch_prune28(W, rows, cols, vals, meta, st));
+  if (m == 2) return from_cuda(launch_prune12(W, rows, cols, vals, meta, st));
+  return from_cuda(launch_prune24(W, rows, cols, vals, meta, st));
+}
+
+extern "C" int slope_double_prune_nm(const void* vals, const uint8_t* meta, int64_t rows,
+                                     int64_t cols, int n, int m, void* t_vals, uint8_t* t_meta,
+                                     void* stream) {
+  if (!known_pattern(n, m)) return SLOPE_ERR_UNSUPPORTED;
+  if (m == 4) return slope_double_prune(vals, meta, rows, cols, t_vals, t_meta, stream);
+  if (rows <= 0 || cols <= 0 || rows % 8 != 0 || cols % 16 != 0) return SLOPE_ERR_SHAPE;
+  if (!vals || !meta || !t_vals || !t_meta) return SLOPE_ERR_INVALID_ARG;
+  if (!aligned16(vals) || !aligned16(meta) || !aligned16(t_vals) || !aligned16(t_meta))
+    return SLOPE_ERR_ALIGNMENT;
+  if (int s = check_device()) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (m == 8) return from_cuda(launch_double_prune28(vals, meta, rows, cols, t_vals, t_meta, st));
+  return from_cuda(launch_double_prune12(vals, meta, rows, cols, t_vals, t_meta, st));
+}
+
+extern "C" int slope_expand_nm_to_24(const void* vals, const uint8_t* meta, int64_t rows,
+                                     int64_t cols, int n, int m, void* vals24, uint8_t* meta24,
+                                     void* stream) {
+  if (n != 2 || m != 8) return SLOPE_ERR_UNSUPPORTED;
+  if (rows < 0 || cols <= 0 || cols % 8 != 0) return SLOPE_ERR_SHAPE;
+  if (rows == 0) return SLOPE_OK;
+  if (!vals || !meta || !vals24 || !meta24) return SLOPE_ERR_INVALID_ARG;
+  if (!aligned16(vals) || !aligned16(meta) || !aligned16(vals24) || !aligned16(meta24))
+    return SLOPE_ERR_ALIGNMENT;
+  if (int s = check_device()) return s;
+  return from_cuda(launch_expand28(vals, meta, rows, cols, vals24, meta24,
+                                   static_cast<cudaStream_t>(stream)));
 }
 
 extern "C" int slope_double_prune(const void* vals, const uint8_t* meta, int64_t rows,
@@ -416,7 +454,8 @@ extern "C" int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T,
                                        void* stream) {
   (void)workspace; (void)workspace_bytes;
   if (int s = check_linear(T, in, out, r)) return s;
-  const uint32_t known = SLOPE_DW_DENSE | SLOPE_ACCUMULATE | SLOPE_SKIP_DW | SLOPE_SKIP_ADAPTER;
+  const uint32_t known =
+      SLOPE_DW_DENSE | SLOPE_ACCUMULATE | SLOPE_SKIP_DW | SLOPE_SKIP_ADAPTER | SLOPE_DW_NM28;
   if (flags & ~known) return SLOPE_ERR_INVALID_ARG;
   if ((flags & SLOPE_SKIP_DW) && (flags & SLOPE_SKIP_ADAPTER)) return SLOPE_ERR_INVALID_ARG;
   const bool do_dw = !(flags & SLOPE_SKIP_DW);
@@ -431,7 +470,9 @@ extern "C" int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T,
   if (int s = check_device()) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool dense = flags & SLOPE_DW_DENSE, acc = flags & SLOPE_ACCUMULATE;
-  const size_t dw_bytes = static_cast<size_t>(out) * (dense ? in : in / 2) * sizeof(float);
+  const bool nm28 = flags & SLOPE_DW_NM28;
+  const int64_t dw_cols = dense ? in : (nm28 ? in / 4 : in / 2);  // fp32 per row of dW
+  const size_t dw_bytes = static_cast<size_t>(out) * dw_cols * sizeof(float);
   if (T == 0) {
     if (!acc && launch_zero3(do_dw ? dW : nullptr, do_dw ? dw_bytes / sizeof(float) : 0,
                              do_ad ? dL : nullptr, do_ad ? static_cast<size_t>(in) * r : 0,
@@ -449,8 +490,8 @@ extern "C" int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T,
     DenseGemmArgs w{};
     w.a = dY; w.b = X; w.a_mn_major = true; w.b_mn_major = true;
     w.M = out; w.N = in; w.K = T; w.lda = out; w.ldb = in;
-    w.epi = DenseEpi::MaskedWeightGrad; w.out = dW; w.ldo = dense ? in : in / 2;
-    w.meta = Wm; w.dense_dw = dense; w.accumulate = acc; w.splits = 0;
+    w.epi = DenseEpi::MaskedWeightGrad; w.out = dW; w.ldo = dw_cols;
+    w.meta = Wm; w.dense_dw = dense; w.accumulate = acc; w.splits = 0; w.nm28 = nm28;
     if (fuse) {
       w.fuse_r = r; w.xl = XL; w.g = G; w.dl = dL; w.dr = dR;
     }

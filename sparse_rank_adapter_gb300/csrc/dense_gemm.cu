@@ -83,6 +83,7 @@ struct DnParams {
   void* out;
   const uint8_t* meta;  // masked dW: metadata, N/8 bytes per row
   int dense_dw, accumulate, atomic_out;
+  int nm28;  // masked dW: `meta` holds 2:8 bytes (i0 | i1 << 3 per 8 columns); compressed dW has N/4 per row
   int lo_off, fold;
   int csplit;  // CTAs of a cluster that split one tile's K (hi/lo store only); 1 = none
   int fuse_r;  // pair dW kernel: r of the adapter gradients computed alongside; 0 = none
@@ -142,7 +143,45 @@ __device__ __forceinline__ void epilogue_chunk(const DnParams& p, const uint32_t
     if (nb >= p.N) return;
     const uint32_t word = reinterpret_cast<const uint32_t*>(mrow)[c0 / 32];
     float* orow = static_cast<float*>(p.out) + static_cast<size_t>(m) * p.ldo;
-    if (p.dense_dw) {
+    if (p.nm28) {
+      // 2:8 mask: the word's four bytes are the 32 columns' four groups of
+      // eight; group b keeps columns 8b + i0 and 8b + i1
+      float d[32];
+      float kept[8];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const uint32_t byte = (word >> (8 * b)) & 0xFFu;
+        const uint32_t i0 = byte & 7u, i1 = (byte >> 3) & 7u;
+        float k0 = 0.0f, k1 = 0.0f;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const float x = __uint_as_float(v[8 * b + jj]);
+          const bool on0 = jj == static_cast<int>(i0), on1 = jj == static_cast<int>(i1);
+          k0 = on0 ? x : k0;
+          k1 = on1 ? x : k1;
+          d[8 * b + jj] = (on0 || on1) ? x : 0.0f;
+        }
+        kept[2 * b] = k0;
+        kept[2 * b + 1] = k1;
+      }
+      const int nvec = p.dense_dw ? 8 : 2;
+      float4* dst = reinterpret_cast<float4*>(orow + (p.dense_dw ? nb : nb / 4));
+      const float* src = p.dense_dw ? d : kept;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (u >= nvec) break;
+        float4 x = make_float4(src[4 * u], src[4 * u + 1], src[4 * u + 2], src[4 * u + 3]);
+        if (p.atomic_out) {
+          red_add_f32x4(reinterpret_cast<float*>(&dst[u]), x);
+        } else {
+          if (p.accumulate) {
+            const float4 y = dst[u];
+            x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+          }
+          dst[u] = x;
+        }
+      }
+    } else if (p.dense_dw) {
       float d[32];
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
@@ -829,6 +868,7 @@ cudaError_t run_dw_pair(const DenseGemmArgs& a, cudaStream_t stream) {
     p.group_m = (pairs_m + bands - 1) / bands;
   }
   p.ldo = a.ldo; p.out = a.out; p.meta = a.meta;
+  p.nm28 = a.nm28 ? 1 : 0;
   p.dense_dw = a.dense_dw ? 1 : 0;
   p.accumulate = a.accumulate ? 1 : 0;
   p.atomic_out = splits > 1 ? 1 : 0;
@@ -905,6 +945,7 @@ cudaError_t run(const DenseGemmArgs& a, cudaStream_t stream) {
   p.M = static_cast<int>(M); p.N = static_cast<int>(N); p.K = static_cast<int>(K);
   p.kb_per_split = kbs; p.num_kb = num_kb;
   p.ldo = a.ldo; p.out = a.out; p.meta = a.meta;
+  p.nm28 = a.nm28 ? 1 : 0;
   p.dense_dw = a.dense_dw ? 1 : 0;
   p.accumulate = a.accumulate ? 1 : 0;
   p.atomic_out = 0;

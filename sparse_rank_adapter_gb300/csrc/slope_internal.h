@@ -58,6 +58,21 @@ cudaError_t launch_recompress_frozen24(const void* W, const uint8_t* meta, const
 cudaError_t launch_axpby(float beta, const void* a, int a_dt, float gamma, const void* b, int b_dt,
                          void* out, int out_dt, int64_t n, cudaStream_t stream);
 
+// ---- the 1:2 and 2:8 patterns (nm_patterns.cu)
+// 1:2 prune of W into the 2:4 format; its double pruning (2:4 format in and out).
+cudaError_t launch_prune12(const void* W, int64_t rows, int64_t cols, void* vals, uint8_t* meta,
+                           cudaStream_t stream);
+cudaError_t launch_double_prune12(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols,
+                                  void* t_vals, uint8_t* t_meta, cudaStream_t stream);
+// 2:8 prune of W into the 2:8 format (vals rows x cols/4, meta rows x cols/8);
+// its double pruning (2:8 format in and out); its 2:4 form.
+cudaError_t launch_prune28(const void* W, int64_t rows, int64_t cols, void* vals, uint8_t* meta,
+                           cudaStream_t stream);
+cudaError_t launch_double_prune28(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols,
+                                  void* t_vals, uint8_t* t_meta, cudaStream_t stream);
+cudaError_t launch_expand28(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols, void* vals24,
+                            uint8_t* meta24, cudaStream_t stream);
+
 // Zeroes up to three fp32 arrays (counts in floats, multiples of 4) in one
 // programmatic-dependent launch (dense_gemm.cu).
 cudaError_t launch_zero3(float* a, size_t na, float* b, size_t nb, float* c, size_t nc,
@@ -118,6 +133,7 @@ struct DenseGemmArgs {
   int64_t ldo;       // elements between rows of the output
   const uint8_t* meta;  // MaskedWeightGrad: out x in/8 metadata
   bool dense_dw, accumulate;
+  bool nm28 = false;    // MaskedWeightGrad: meta is the 2:8 format (one byte per 8 columns)
   int splits;        // split-K factor; 0 chooses one from the grid size
   int lo_off;        // StoreBf16HiLo: column offset of the low parts (= r)
   int fold;          // AddF32*: columns n >= fold add into column n - fold (0: none)

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(PKG, "libslope.so")
 
 OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(7)
 F32, BF16 = 0, 1
-DW_DENSE, ACCUMULATE, SKIP_DW, SKIP_ADAPTER = 1, 2, 4, 8
+DW_DENSE, ACCUMULATE, SKIP_DW, SKIP_ADAPTER, DW_NM28 = 1, 2, 4, 8, 16
 
 # (name, restype, argtypes) of every exported function, in header order.
 _vp, _i64, _i, _u32, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32, ctypes.c_size_t
@@ -29,6 +29,8 @@ SIGNATURES = (
     ("slope_workspace_size", _sz, (_i64, _i64, _i64, _i)),
     ("slope_prune_nm", _i, (_vp, _i64, _i64, _i, _i, _vp, _vp, _vp)),
     ("slope_double_prune", _i, (_vp, _vp, _i64, _i64, _vp, _vp, _vp)),
+    ("slope_double_prune_nm", _i, (_vp, _vp, _i64, _i64, _i, _i, _vp, _vp, _vp)),
+    ("slope_expand_nm_to_24", _i, (_vp, _vp, _i64, _i64, _i, _i, _vp, _vp, _vp)),
     ("slope_prune_and_double_prune", _i, (_vp, _i64, _i64, _i, _i, _vp, _vp, _vp, _vp, _vp)),
     ("slope_recompress_double_prune", _i, (_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp)),
     ("slope_double_prune_frozen", _i, (_vp, _vp, _i64, _i64, _vp, _vp, _vp)),
@@ -114,16 +116,51 @@ def slope_workspace_size(T: int, inp: int, out: int, r: int) -> int:
     return lib().slope_workspace_size(T, inp, out, r)
 
 
+def _vals_cols(cols: int, m: int) -> int:
+    """Stored values per row: half the columns (2:4, and 1:2 in the 2:4
+    format), a quarter for 2:8."""
+    return cols // 4 if m == 8 else cols // 2
+
+
 def slope_prune_nm(W, vals, meta, n: int = 2, m: int = 4, stream=None):
-    """A1: 2:4 prune-and-compress of W (rows x cols bf16) into vals/meta."""
+    """A1: n:m prune-and-compress of W (rows x cols bf16) into vals/meta:
+    2:4 and 1:2 in the 2:4 format (vals cols/2), 2:8 in the 2:8 format
+    (vals cols/4); meta is cols/8 bytes per row in every case."""
     import torch
 
     rows, cols = W.shape
     st = lib().slope_prune_nm(
         _ptr(W, torch.bfloat16, name="W"), rows, cols, n, m,
-        _ptr(vals, torch.bfloat16, (rows, cols // 2), "vals"),
+        _ptr(vals, torch.bfloat16, (rows, _vals_cols(cols, m)), "vals"),
         _ptr(meta, torch.uint8, (rows, cols // 8), "meta"), _stream(stream))
     _check(st, "slope_prune_nm")
+
+
+def slope_double_prune_nm(vals, meta, rows: int, cols: int, t_vals, t_meta, n: int = 2, m: int = 4,
+                          stream=None):
+    """A2 for 2:4, 1:2 (2:4 format) or 2:8 (2:8 format): the transpose of the
+    compressed rows x cols matrix pruned n:m again along the old rows."""
+    import torch
+
+    st = lib().slope_double_prune_nm(
+        _ptr(vals, torch.bfloat16, (rows, _vals_cols(cols, m)), "vals"),
+        _ptr(meta, torch.uint8, (rows, cols // 8), "meta"), rows, cols, n, m,
+        _ptr(t_vals, torch.bfloat16, (cols, _vals_cols(rows, m)), "t_vals"),
+        _ptr(t_meta, torch.uint8, (cols, rows // 8), "t_meta"), _stream(stream))
+    _check(st, "slope_double_prune_nm")
+
+
+def slope_expand_nm_to_24(vals, meta, rows: int, cols: int, vals24, meta24, n: int = 2, m: int = 8,
+                          stream=None):
+    """The 2:4 form (vals24 cols/2, meta24 cols/8) of a 2:8-format matrix."""
+    import torch
+
+    st = lib().slope_expand_nm_to_24(
+        _ptr(vals, torch.bfloat16, (rows, _vals_cols(cols, m)), "vals"),
+        _ptr(meta, torch.uint8, (rows, cols // 8), "meta"), rows, cols, n, m,
+        _ptr(vals24, torch.bfloat16, (rows, cols // 2), "vals24"),
+        _ptr(meta24, torch.uint8, (rows, cols // 8), "meta24"), _stream(stream))
+    _check(st, "slope_expand_nm_to_24")
 
 
 def slope_double_prune(vals, meta, rows: int, cols: int, t_vals, t_meta, stream=None):
@@ -255,7 +292,7 @@ def slope_linear_bwd_weight(dY, X, Wm, XL, G, dW, dL=None, dR=None, flags: int =
     r = 0 if XL is None else XL.shape[1] // 2
     if r == 0 and dL is not None:
         r = dL.shape[1]
-    dw_shape = (out, inp) if flags & DW_DENSE else (out, inp // 2)
+    dw_shape = (out, inp) if flags & DW_DENSE else (out, inp // 4 if flags & DW_NM28 else inp // 2)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib().slope_linear_bwd_weight(
         _ptr(dY, torch.bfloat16, name="dY"), _ptr(X, torch.bfloat16, (T, inp), "X"), T, inp, out,

@@ -70,7 +70,11 @@ cpu_only = pytest.mark.skipif(not no_gpu(), reason="fake pointers are only safe 
 @cpu_only
 def test_prune_argument_checks(L):
     f = L.lib().slope_prune_nm
-    assert f(A, 4, 16, 1, 2, A, A, None) == L.ERR_UNSUPPORTED
+    assert f(A, 4, 16, 1, 4, A, A, None) == L.ERR_UNSUPPORTED  # 2:4, 1:2 and 2:8 only
+    assert f(A, 4, 16, 4, 8, A, A, None) == L.ERR_UNSUPPORTED
+    assert f(A, 4, 12, 1, 2, A, A, None) == L.ERR_SHAPE
+    assert f(A, 4, 12, 2, 8, A, A, None) == L.ERR_SHAPE
+    assert f(A, 4, 16, 2, 8, A, MIS, None) == L.ERR_ALIGNMENT
     assert f(A, 4, 12, 2, 4, A, A, None) == L.ERR_SHAPE
     assert f(A, -1, 16, 2, 4, A, A, None) == L.ERR_SHAPE
     assert f(None, 4, 16, 2, 4, A, A, None) == L.ERR_INVALID_ARG
@@ -85,6 +89,27 @@ def test_double_prune_argument_checks(L):
     assert f(A, A, 16, 24, A, A, None) == L.ERR_SHAPE
     assert f(A, None, 16, 16, A, A, None) == L.ERR_INVALID_ARG
     assert f(A, A, 16, 16, A, MIS, None) == L.ERR_ALIGNMENT
+
+
+@cpu_only
+def test_pattern_argument_checks(L):
+    d = L.lib().slope_double_prune_nm
+    assert d(A, A, 16, 16, 3, 4, A, A, None) == L.ERR_UNSUPPORTED
+    for n, m in ((1, 2), (2, 8), (2, 4)):
+        assert d(A, A, 12, 16, n, m, A, A, None) == L.ERR_SHAPE  # rows % 8
+        assert d(A, A, 16, 24, n, m, A, A, None) == L.ERR_SHAPE  # cols % 16
+        assert d(A, None, 16, 16, n, m, A, A, None) == L.ERR_INVALID_ARG
+        assert d(A, A, 16, 16, n, m, MIS, A, None) == L.ERR_ALIGNMENT
+    e = L.lib().slope_expand_nm_to_24
+    assert e(A, A, 16, 16, 2, 4, A, A, None) == L.ERR_UNSUPPORTED  # 2:8 only
+    assert e(A, A, 16, 12, 2, 8, A, A, None) == L.ERR_SHAPE
+    assert e(A, A, 16, 16, 2, 8, A, None, None) == L.ERR_INVALID_ARG
+    assert e(A, A, 16, 16, 2, 8, A, MIS, None) == L.ERR_ALIGNMENT
+    assert e(None, None, 0, 16, 2, 8, None, None, None) == L.OK  # no rows
+    bw = L.lib().slope_linear_bwd_weight
+    # the 2:8 flag is known: a bad dW alignment is what fails next
+    assert bw(A, A, 64, 256, 256, A, A, A, 8, MIS, 16, A, A, None, 0, None) == L.ERR_ALIGNMENT
+    assert bw(A, A, 64, 256, 256, A, A, A, 8, A, 32, A, A, None, 0, None) == L.ERR_INVALID_ARG
 
 
 @cpu_only
@@ -139,7 +164,7 @@ def test_linear_argument_checks(L):
     assert fwd(A, 0, 256, 256, A, A, A, A, 8, A, 0, A, None, 0, None) == L.OK  # T == 0
     assert bi(A, 64, 256, 384, A, A, A, A, 16, A, 1, None, None, 0, None) == L.ERR_INVALID_ARG
     assert bi(A, 64, 256, 130, A, A, A, A, 16, A, 1, A, None, 0, None) == L.ERR_SHAPE
-    assert bw(A, A, 64, 256, 256, A, A, A, 8, A, 16, A, A, None, 0, None) == L.ERR_INVALID_ARG  # unknown flag
+    assert bw(A, A, 64, 256, 256, A, A, A, 8, A, 32, A, A, None, 0, None) == L.ERR_INVALID_ARG  # unknown flag
     assert bw(A, A, 64, 256, 256, A, A, A, 8, A, 4 | 8, A, A, None, 0, None) == L.ERR_INVALID_ARG  # skip both
     assert bw(A, A, 64, 256, 256, A, A, A, 8, None, 4, None, A, None, 0, None) == L.ERR_INVALID_ARG  # no dL
     assert bw(A, A, 64, 256, 256, None, A, A, 8, A, 0, A, A, None, 0, None) == L.ERR_INVALID_ARG
