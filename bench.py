@@ -235,13 +235,16 @@ class BlockStep:
     """Device buffers and the ordered ABI calls of one block step."""
 
     def __init__(self, wl, seed: int, device, fused_prune: bool = False, optimizer: bool = False,
-                 frozen_columns: bool = False):
+                 frozen_columns: bool = False, pattern: str = "2:4"):
         import torch
 
         from sparse_rank_adapter_gb300 import slope
 
         self.S = slope
         self.wl = wl
+        # N:M pattern of the weights: 2:4, 1:2 (in the 2:4 format) or 2:8
+        # (its own format, expanded to its 2:4 form for the sparse products)
+        self.n, self.m = (int(x) for x in pattern.split(":"))
         self.fused_prune = fused_prune
         self.optimizer = optimizer  # kept row mask: re-compression + A2, then beta·A + gamma·B
         self.frozen_columns = frozen_columns  # the column mask kept too: no second selection
@@ -266,7 +269,12 @@ class BlockStep:
                 XL=torch.empty(T, 2 * r, dtype=torch.bfloat16, device=device) if r else None,
                 dX=torch.empty(T, inp, dtype=torch.bfloat16, device=device),
                 G=torch.empty(T, 2 * r, dtype=torch.bfloat16, device=device) if r else None,
-                dW=torch.empty(out, inp // 2, dtype=torch.float32, device=device),
+                dW=torch.empty(out, inp // 4 if self.m == 8 else inp // 2, dtype=torch.float32, device=device),
+                # 2:8: the weight and its double pruning in the 2:8 format
+                Wv8=torch.empty(out, inp // 4, dtype=torch.bfloat16, device=device) if self.m == 8 else None,
+                Wm8=torch.empty(out, inp // 8, dtype=torch.uint8, device=device) if self.m == 8 else None,
+                Dv8=torch.empty(inp, out // 4, dtype=torch.bfloat16, device=device) if self.m == 8 else None,
+                Dm8=torch.empty(inp, out // 8, dtype=torch.uint8, device=device) if self.m == 8 else None,
                 dL=torch.empty(inp, r, dtype=torch.float32, device=device) if r else None,
                 dR=torch.empty(r, out, dtype=torch.float32, device=device) if r else None,
                 # the optimizer's fp32 master copy of the kept values
@@ -290,8 +298,12 @@ class BlockStep:
             for b in self.layers:
                 if self.frozen_columns:  # both masks from initialisation
                     self.S.slope_prune_and_double_prune(b["W"], b["Wv"], b["Wm"], b["Dv"], b["Dm"], stream=stream)
+                elif self.m == 8:  # the 2:8 weight's 2:4 form is what the forward reads
+                    self.S.slope_prune_nm(b["W"], b["Wv8"], b["Wm8"], n=2, m=8, stream=stream)
+                    self.S.slope_expand_nm_to_24(b["Wv8"], b["Wm8"], b["out"], b["inp"], b["Wv"], b["Wm"],
+                                                 stream=stream)
                 else:
-                    self.S.slope_prune_nm(b["W"], b["Wv"], b["Wm"], stream=stream)
+                    self.S.slope_prune_nm(b["W"], b["Wv"], b["Wm"], n=self.n, m=self.m, stream=stream)
                 if self.optimizer:
                     b["Wmaster"].copy_(b["Wv"].float())
 
@@ -315,6 +327,22 @@ class BlockStep:
             elif self.fused_prune:  # A1 and A2 from one read of W
                 calls = [("prune_double", lambda b=b: S.slope_prune_and_double_prune(
                     b["W"], b["Wv"], b["Wm"], b["Dv"], b["Dm"], stream=stream))]
+            elif self.m == 2:  # 1:2, written in the 2:4 format
+                calls = [
+                    ("prune12", lambda b=b: S.slope_prune_nm(b["W"], b["Wv"], b["Wm"], n=1, m=2, stream=stream)),
+                    ("double_prune12", lambda b=b: S.slope_double_prune_nm(
+                        b["Wv"], b["Wm"], b["out"], b["inp"], b["Dv"], b["Dm"], n=1, m=2, stream=stream)),
+                ]
+            elif self.m == 8:  # 2:8, and the 2:4 forms the sparse products read
+                calls = [
+                    ("prune28", lambda b=b: S.slope_prune_nm(b["W"], b["Wv8"], b["Wm8"], n=2, m=8, stream=stream)),
+                    ("expand28", lambda b=b: S.slope_expand_nm_to_24(
+                        b["Wv8"], b["Wm8"], b["out"], b["inp"], b["Wv"], b["Wm"], stream=stream)),
+                    ("double_prune28", lambda b=b: S.slope_double_prune_nm(
+                        b["Wv8"], b["Wm8"], b["out"], b["inp"], b["Dv8"], b["Dm8"], n=2, m=8, stream=stream)),
+                    ("expand28_t", lambda b=b: S.slope_expand_nm_to_24(
+                        b["Dv8"], b["Dm8"], b["inp"], b["out"], b["Dv"], b["Dm"], stream=stream)),
+                ]
             else:
                 calls = [
                     ("prune", lambda b=b: S.slope_prune_nm(b["W"], b["Wv"], b["Wm"], stream=stream)),
@@ -332,8 +360,8 @@ class BlockStep:
                     # dW and the adapter gradients dL, dR in one call (one
                     # launch: the dW GEMM computes the two rank-r products too)
                     ("bwd_weight", lambda b=b: S.slope_linear_bwd_weight(
-                        b["dY"], b["X"], b["Wm"], b["XL"], b["G"], b["dW"], b["dL"], b["dR"],
-                        stream=stream)),
+                        b["dY"], b["X"], b["Wm8"] if self.m == 8 else b["Wm"], b["XL"], b["G"], b["dW"],
+                        b["dL"], b["dR"], flags=S.DW_NM28 if self.m == 8 else 0, stream=stream)),
                 ]
                 if self.optimizer:  # decayed master values plus the scaled gradient, in place
                     calls += [("axpby", lambda b=b: S.slope_sparse_axpby(
@@ -354,6 +382,7 @@ class BlockStep:
         n = 0
         for b in self.layers:
             n += 0 if self.wl.forward_only else (1 if self.fused_prune or self.optimizer else 2)  # prune(s)
+            n += 2 if self.m == 8 and not self.wl.forward_only else 0  # the two 2:4 forms
             n += 1 if self.optimizer else 0  # beta·A + gamma·B
             n += 2 if self.wl.rank else 1  # fwd: (XL) + sparse
             if not self.wl.forward_only:
@@ -407,16 +436,17 @@ def call_flops(name, T, inp, out, r):
     return 0.0
 
 
-def method_flops(name, T, inp, out, r):
+def method_flops(name, T, inp, out, r, keep=0.5):
     """The method's own work in one ABI call.  The sparse products count
     their dense-equivalent 2·T·in·out (judged against twice the dense
     peak); the masked weight gradient counts T·in·out, because only the
     kept half of dYᵀ·X is needed (the tensor cores still compute all of
-    it); the rank-r products count 2·T·r·(in + out)."""
+    it); the rank-r products count 2·T·r·(in + out).  `keep` is the
+    pattern's density (0.5 for 2:4 and 1:2, 0.25 for 2:8)."""
     if name in ("fwd", "bwd_input"):
         return 2.0 * T * inp * out + 2.0 * T * r * (inp + out)
     if name == "bwd_weight":
-        return 1.0 * T * inp * out + 2.0 * T * r * (inp + out)
+        return 2.0 * keep * T * inp * out + 2.0 * T * r * (inp + out)
     return 0.0
 
 
@@ -463,10 +493,16 @@ def pick_peak(clocks, bf16, bf16_sus):
 
 
 def call_bytes(name, T, inp, out, r):
-    if name == "prune":
+    if name in ("prune", "prune12"):  # W in; values (half) and metadata out
         return out * inp * (2 + 1 + 0.125)
-    if name == "double_prune":
+    if name in ("double_prune", "double_prune12"):
         return out * inp * (1.125 + 1.125)
+    if name == "prune28":  # W in; a quarter of the values and the metadata out
+        return out * inp * (2 + 0.5 + 0.125)
+    if name == "double_prune28":
+        return out * inp * (0.625 + 0.625)
+    if name in ("expand28", "expand28_t"):  # 2:8 format in, 2:4 form out
+        return out * inp * (0.625 + 1.125)
     if name == "prune_double":  # W in once; both compressed formats out
         return out * inp * (2 + 1.125 + 1.125)
     if name == "recompress_double":  # W and the kept metadata in; values, D values and metadata out
@@ -530,7 +566,7 @@ def gpu_arm(args):
     stream = torch.cuda.Stream(device=dev)
     n_sets = max(1, args.sets)
     sets = [BlockStep(wl, seed=s + 10 * rank, device=dev, fused_prune=args.fused_prune, optimizer=args.optimizer,
-                      frozen_columns=args.frozen_columns) for s in range(n_sets)]
+                      frozen_columns=args.frozen_columns, pattern=args.pattern) for s in range(n_sets)]
     torch.cuda.synchronize()
 
     with torch.cuda.stream(stream):
@@ -625,13 +661,13 @@ def gpu_arm(args):
         ach = byts / (calls_ms[dom] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                 "peak_source": f"{src} hbm"}
-    elif dom in ("prune", "double_prune", "prune_double", "recompress_double", "recompress_frozen", "axpby"):
+    elif call_bytes(dom, T, 1, 1, r) > 0:  # a memory-bound call
         alg = sum(call_bytes(dom, T, i, o, r) for i, o in obs[dom])
         ach = alg / (calls_ms[dom] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                 "peak_source": f"{src} hbm"}
     else:
-        work = sum(method_flops(dom, T, i, o, r) for i, o in obs[dom])
+        work = sum(method_flops(dom, T, i, o, r, keep=0.25 if sets[0].m == 8 else 0.5) for i, o in obs[dom])
         ach = work / (calls_ms[dom] * 1e-3) / 1e12
         sparse = dom in ("fwd", "bwd_input")
         peak = dense_peak * (2.0 if sparse else 1.0)
@@ -652,7 +688,13 @@ def gpu_arm(args):
                  "prune_double": "prune_double24_kernel (slope_prune_and_double_prune)",
                  "recompress_double": "prune_double24_kernel, kept mask (slope_recompress_double_prune)",
                  "recompress_frozen": "prune_double24_kernel, both masks kept (slope_recompress_frozen)",
-                 "axpby": "axpby_kernel (slope_sparse_axpby)"}
+                 "axpby": "axpby_kernel (slope_sparse_axpby)",
+                 "prune12": "prune12_kernel (slope_prune_nm 1:2)",
+                 "double_prune12": "double_prune12_kernel (slope_double_prune_nm 1:2)",
+                 "prune28": "prune28_kernel (slope_prune_nm 2:8)",
+                 "double_prune28": "double_prune28_kernel (slope_double_prune_nm 2:8)",
+                 "expand28": "expand28_kernel (slope_expand_nm_to_24)",
+                 "expand28_t": "expand28_kernel (slope_expand_nm_to_24)"}
     # achieved bandwidth of every memory-bound call (algorithmic bytes over its time)
     hbm_calls = {}
     for name, o_ in obs.items():
@@ -694,7 +736,10 @@ def gpu_arm(args):
                        "prune": ("both masks kept: re-compression, then beta*A + gamma*B"
                                  if args.optimizer and args.frozen_columns
                                  else "kept mask: re-compression + A2, then beta*A + gamma*B" if args.optimizer
-                                 else "one call (A1 + A2)" if args.fused_prune else "two calls (A1, A2)")},
+                                 else "one call (A1 + A2)" if args.fused_prune else "two calls (A1, A2)"),
+                       "pattern": args.pattern + (" (2:8 format; the sparse products on its 2:4 form)"
+                                                  if args.pattern == "2:8" else
+                                                  " (in the 2:4 format)" if args.pattern == "1:2" else "")},
             "pct_of_sparse_peak": round(100 * value / (2 * bf16), 2),
             "composite_roofline_frac": composite_frac(wl, ms_step, dense_peak),
             "composite_peak": f"{src} bf16 {peak_why}",
@@ -979,6 +1024,73 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+def tiling_study(args):
+    """SLoPe §2.4 / App. E split the "upsample" weights (FC1: d -> 4d) into
+    square tiles to avoid a dip of the sparse product's speed-up at some
+    dimensions.  This times, on this library's kernels, each FC1 forward as
+    one call against its four square d x d row tiles (four calls, each
+    writing its own T x d output), for the OPT hidden sizes and token
+    counts; rank 0 (the sparse product alone), weights pre-compressed, L2
+    flushed before every timed call, median of `reps` calls.  Prints one
+    JSON line."""
+    import torch
+
+    from sparse_rank_adapter_gb300 import build as B
+    from sparse_rank_adapter_gb300 import slope as S
+
+    B.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    reps = 10
+
+    def timed(fn):
+        out = []
+        with torch.cuda.stream(stream):
+            for i in range(reps + 2):
+                flush.fill_(i & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                if i >= 2:
+                    out.append(e0.elapsed_time(e1))
+        return statistics.median(out)
+
+    rows = []
+    for d in (2560, 4096, 7168, 9216):
+        W = synth.device_normal_bf16((4 * d, d), 0.02, d, dev)
+        Wv = torch.empty(4 * d, d // 2, dtype=torch.bfloat16, device=dev)
+        Wm = torch.empty(4 * d, d // 8, dtype=torch.uint8, device=dev)
+        S.slope_prune_nm(W, Wv, Wm, stream=stream)
+        tiles = [(Wv[k * d:(k + 1) * d], Wm[k * d:(k + 1) * d]) for k in range(4)]
+        del W
+        for T in (16, 2048, 16384):
+            X = synth.device_normal_bf16((T, d), 1.0, d + T, dev)
+            Y = torch.empty(T, 4 * d, dtype=torch.bfloat16, device=dev)
+            Yk = [torch.empty(T, d, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+            one = timed(lambda: S.slope_linear_fwd(X, Wv, Wm, None, None, Y, stream=stream))
+
+            def four():
+                for (v, m), y in zip(tiles, Yk):
+                    S.slope_linear_fwd(X, v, m, None, None, y, stream=stream)
+
+            sq = timed(four)
+            flops = 2.0 * T * d * 4 * d
+            rows.append({"d": d, "T": T, "one_call_ms": round(one, 4), "square_tiles_ms": round(sq, 4),
+                         "tiles_over_one": round(sq / one, 3),
+                         "one_call_tflops": round(flops / (one * 1e-3) / 1e12, 1)})
+            del X, Y, Yk
+        del Wv, Wm, tiles
+    S.slope_device_status(stream)
+    print(json.dumps({"study": "FC1 (d -> 4d) forward: one call vs four square d x d tiles",
+                      "source": "SLoPe §2.4 and App. E (weight tiling)", "unit": "ms", "rank": 0,
+                      "pattern": "2:4", "timing": f"median of {reps} calls, L2 flushed before each",
+                      "rows": rows}), flush=True)
+
+
 def free_port():
     import socket
 
@@ -1033,11 +1145,20 @@ def main():
                          "(slope_recompress_frozen in place of the re-compression + A2)")
     ap.add_argument("--fused-prune", action="store_true",
                     help="A1 and A2 through the one-call slope_prune_and_double_prune")
+    ap.add_argument("--tiling-study", action="store_true",
+                    help="time FC1 forwards as one call against four square tiles (one JSON line)")
+    ap.add_argument("--pattern", default="2:4", choices=["2:4", "1:2", "2:8"],
+                    help="N:M pattern of the weights (1:2 in the 2:4 format; 2:8 with its 2:4 form)")
     args = ap.parse_args()
+    if args.pattern != "2:4" and (args.fused_prune or args.optimizer):
+        ap.error("--pattern 1:2 / 2:8 runs the plain training step (no --fused-prune, --optimizer)")
     if args.warmup < 3:
         args.warmup = 3
     if args.oracle_sample > 0:
         oracle_sample_child(args)
+        return
+    if args.tiling_study:
+        tiling_study(args)
         return
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
         sys.exit(launch_replicas(args.gpus, sys.argv[1:]))

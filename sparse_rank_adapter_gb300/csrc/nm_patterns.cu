@@ -8,7 +8,8 @@
 // 1:2 keeps the entry of larger magnitude of every aligned pair.  Two pairs
 // make a quadruple with exactly two kept entries, one per half, so a 1:2
 // matrix is a 2:4 matrix and is written in the 2:4 format (slope.h): the
-// 2:4 sparse tensor-core GEMMs take it as it is.
+// 2:4 sparse tensor-core GEMMs take it as it is, and its double pruning is
+// the 2:4 A2 kernels' data movement with a per-pair selection (prune.cu).
 //
 // 2:8 keeps the two entries of largest magnitude of every aligned group of
 // eight, in its own format: vals rows x cols/4 (the two kept values of a
@@ -70,91 +71,35 @@ __global__ void __launch_bounds__(kThreads) prune12_kernel(const uint4* __restri
   }
 }
 
-// Column j (0-3) of a quadruple stored as a kept pair `word` with nibble
-// `nib`: the kept value at its position, +0 elsewhere.
-__device__ __forceinline__ uint32_t quad_col(uint32_t word, uint32_t nib, uint32_t j) {
-  const uint32_t i0 = nib & 3u, i1 = nib >> 2;
-  return j == i0 ? (word & 0xFFFFu) : (j == i1 ? (word >> 16) : 0u);
-}
-
-// A2 for 1:2: the transpose of a rows x cols 2:4-format matrix, pruned 1:2
-// along the old rows.  Work item: 8 consecutive rows (octet h8) x one
-// 16-column chunk c16 (16 B of values and 2 B of metadata per row).  Lanes
-// take consecutive octets, the block's 8 warps adjacent chunks (their loads
-// of a row share 128 B in L1); the 16 output rows a thread writes get 8 B
-// of values (4 pairs of old rows) and one metadata byte at column octet h8,
-// 256 B / 32 B contiguous per warp.
-__global__ void __launch_bounds__(kThreads) double_prune12_kernel(const uint4* __restrict__ vals,
-                                                                  const uint16_t* __restrict__ meta,
-                                                                  uint2* __restrict__ t_vals,
-                                                                  uint8_t* __restrict__ t_meta,
-                                                                  int64_t rows, int64_t cols) {
-  grid_dependency_wait();
-  allow_dependents_launch();
-  const int64_t n_h8 = rows / 8, n_c16 = cols / 16;
-  const int64_t tiles_h = (n_h8 + 31) / 32, tiles_c = (n_c16 + 7) / 8;
-  const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
-  for (int64_t tile = blockIdx.x; tile < tiles_h * tiles_c; tile += gridDim.x) {
-    const int64_t h8 = (tile % tiles_h) * 32 + lane;
-    const int64_t c16 = (tile / tiles_h) * 8 + warp;
-    if (h8 >= n_h8 || c16 >= n_c16) continue;
-    uint4 pw[8];
-    uint32_t m[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int64_t at = (8 * h8 + k) * n_c16 + c16;
-      pw[k] = __ldg(vals + at);
-      m[k] = __ldg(meta + at);
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {  // quadruple q of the chunk: columns 4q .. 4q + 3
-#pragma unroll
-      for (uint32_t j = 0; j < 4; ++j) {
-        uint32_t e[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t word = q == 0 ? pw[k].x : q == 1 ? pw[k].y : q == 2 ? pw[k].z : pw[k].w;
-          e[k] = quad_col(word, (m[k] >> (4 * q)) & 15u, j);
-        }
-        // old rows (2p, 2p + 1) form pair p; pairs 0-1 and 2-3 form the two
-        // output quadruples of this octet
-        uint32_t n0, n1;
-        const uint32_t a = keep12(e[0] | (e[1] << 16), e[2] | (e[3] << 16), n0);
-        const uint32_t b = keep12(e[4] | (e[5] << 16), e[6] | (e[7] << 16), n1);
-        const int64_t i = 16 * c16 + 4 * q + j;  // output row = old column
-        __stcs(t_vals + i * n_h8 + h8, make_uint2(a, b));
-        t_meta[i * n_h8 + h8] = static_cast<uint8_t>(n0 | (n1 << 4));
-      }
-    }
-  }
-}
-
 // ------------------------------------------------------------------ 2:8 ---
 
-// The two largest of eight candidates e[0..7] (bf16 patterns) by magnitude,
-// the lower index first on ties: keys (magnitude << 3) | (7 - index) are
-// distinct, so a running top two decides.  Returns the packed values (lower
-// index in the low half) and the byte i0 | i1 << 3.
-__device__ __forceinline__ uint32_t top2_of_8(const uint32_t (&e)[8], uint32_t& byte) {
-  uint32_t t1 = (key15(e[0]) << 3) | 7u, t2 = 0;
-#pragma unroll
-  for (uint32_t j = 1; j < 8; ++j) {
-    const uint32_t k = (key15(e[j]) << 3) | (7u - j);
-    const uint32_t nt2 = max(t2, min(t1, k));
-    t1 = max(t1, k);
-    t2 = nt2;
-  }
-  const uint32_t ia = 7u - (t1 & 7u), ib = 7u - (t2 & 7u);
-  const uint32_t i0 = min(ia, ib), i1 = max(ia, ib);
-  uint32_t v0 = 0, v1 = 0;
-#pragma unroll
-  for (uint32_t j = 0; j < 8; ++j) {
-    v0 = j == i0 ? e[j] : v0;
-    v1 = j == i1 ? e[j] : v1;
-  }
-  byte = i0 | (i1 << 3);
-  return v0 | (v1 << 16);
+// Rank key of a candidate bf16 value v at index j of its group of eight:
+// (|v| << 4) | ((7 - j) << 1) | sign.  Keys of one group are distinct and
+// order by magnitude, then the lower index; the value is recovered from
+// its key (value_of_key), so a running top two yields the kept values too.
+__device__ __forceinline__ uint32_t key28(uint32_t v, uint32_t j) {
+  return ((v & 0x7FFFu) << 4) | ((7u - j) << 1) | (v >> 15);
 }
+__device__ __forceinline__ uint32_t value_of_key(uint32_t k) { return ((k & 1u) << 15) | (k >> 4); }
+__device__ __forceinline__ uint32_t index_of_key(uint32_t k) { return 7u - ((k >> 1) & 7u); }
+
+// Running top two of keys (t1 > t2): insert k.
+__device__ __forceinline__ void top2_insert(uint32_t& t1, uint32_t& t2, uint32_t k) {
+  t2 = max(t2, min(t1, k));
+  t1 = max(t1, k);
+}
+
+// The group's output from its top two keys: the two values in ascending
+// index order (lower index in the low half) and the byte i0 | i1 << 3.
+__device__ __forceinline__ uint32_t pack28(uint32_t t1, uint32_t t2, uint32_t& byte) {
+  const uint32_t ia = index_of_key(t1), ib = index_of_key(t2);
+  const bool a_first = ia < ib;
+  const uint32_t lo = a_first ? t1 : t2, hi = a_first ? t2 : t1;
+  byte = index_of_key(lo) | (index_of_key(hi) << 3);
+  return value_of_key(lo) | (value_of_key(hi) << 16);
+}
+
+constexpr int kUnroll = 4;  // groups in flight per thread in the elementwise kernels
 
 // A1 for 2:8: one group of eight (16 B) per item -> 4 B of values, 1 byte.
 __global__ void __launch_bounds__(kThreads) prune28_kernel(const uint4* __restrict__ W,
@@ -164,28 +109,65 @@ __global__ void __launch_bounds__(kThreads) prune28_kernel(const uint4* __restri
   grid_dependency_wait();
   allow_dependents_launch();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < ngroups; g += stride) {
-    const uint4 w = __ldcs(W + g);
-    const uint32_t e[8] = {w.x & 0xFFFFu, w.x >> 16, w.y & 0xFFFFu, w.y >> 16,
-                           w.z & 0xFFFFu, w.z >> 16, w.w & 0xFFFFu, w.w >> 16};
-    uint32_t byte;
-    __stcs(vals + g, top2_of_8(e, byte));
-    meta[g] = static_cast<uint8_t>(byte);
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < ngroups;
+       base += stride * kUnroll) {
+    uint4 w[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (base + u * stride < ngroups) w[u] = __ldcs(W + base + u * stride);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t g = base + u * stride;
+      if (g >= ngroups) break;
+      const uint32_t words[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+      uint32_t t1 = key28(words[0] & 0xFFFFu, 0), t2 = 0;
+#pragma unroll
+      for (uint32_t j = 1; j < 8; ++j) top2_insert(t1, t2, key28((words[j >> 1] >> (16 * (j & 1))) & 0xFFFFu, j));
+      uint32_t byte;
+      __stcs(vals + g, pack28(t1, t2, byte));
+      meta[g] = static_cast<uint8_t>(byte);
+    }
   }
 }
 
-// A2 for 2:8: the transpose of a rows x cols 2:8-format matrix, pruned 2:8
-// along the old rows.  Work item: 8 consecutive rows (octet h8) x one group
-// of 8 columns g (4 B of values and 1 byte per row).  Lanes take consecutive
-// octets, the block's 8 warps adjacent groups (a row's loads share one
-// 32 B sector); each of the 8 output rows (old columns 8g .. 8g + 7) gets
-// 4 B of values and one byte at column octet h8, 128 B / 32 B contiguous
-// per warp.
-__global__ void __launch_bounds__(kThreads) double_prune28_kernel(const uint32_t* __restrict__ vals,
-                                                                  const uint8_t* __restrict__ meta,
-                                                                  uint32_t* __restrict__ t_vals,
-                                                                  uint8_t* __restrict__ t_meta,
-                                                                  int64_t rows, int64_t cols) {
+// A2 for 2:8 at any width (rows % 8 == 0, cols % 8 == 0): work item = 8
+// consecutive rows (octet h8) x one group of 8 columns g (4 B of values and
+// one byte per row), read straight from global memory.  Lanes take
+// consecutive octets, the block's 8 warps adjacent groups (a row's loads
+// share one 32 B sector); each of the 8 output rows (old columns 8g ..
+// 8g + 7) gets 4 B of values and one byte at column octet h8.
+__device__ __forceinline__ void transpose_prune28_group(const uint32_t (&w)[8], const uint32_t (&mb)[8],
+                                                        int shift, int64_t g, int64_t h8, int64_t n_h8,
+                                                        uint32_t* __restrict__ t_vals,
+                                                        uint8_t* __restrict__ t_meta) {
+  uint32_t klo[8], khi[8], a[8], b[8];
+#pragma unroll
+  for (uint32_t k = 0; k < 8; ++k) {
+    const uint32_t byte = (mb[k] >> shift) & 0xFFu;
+    a[k] = byte & 7u;
+    b[k] = (byte >> 3) & 7u;
+    klo[k] = key28(w[k] & 0xFFFFu, k);
+    khi[k] = key28(w[k] >> 16, k);
+  }
+#pragma unroll
+  for (uint32_t c = 0; c < 8; ++c) {
+    // candidate of old row k at column c: its kept value there, or +0
+    uint32_t t1 = a[0] == c ? klo[0] : (b[0] == c ? khi[0] : key28(0, 0)), t2 = 0;
+#pragma unroll
+    for (uint32_t k = 1; k < 8; ++k) top2_insert(t1, t2, a[k] == c ? klo[k] : (b[k] == c ? khi[k] : key28(0, k)));
+    uint32_t byte;
+    const uint32_t v = pack28(t1, t2, byte);
+    const int64_t i = 8 * g + c;  // output row = old column
+    __stcs(t_vals + i * n_h8 + h8, v);
+    t_meta[i * n_h8 + h8] = static_cast<uint8_t>(byte);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) double_prune28_direct_kernel(const uint32_t* __restrict__ vals,
+                                                                         const uint8_t* __restrict__ meta,
+                                                                         uint32_t* __restrict__ t_vals,
+                                                                         uint8_t* __restrict__ t_meta,
+                                                                         int64_t rows, int64_t cols) {
   grid_dependency_wait();
   allow_dependents_launch();
   const int64_t n_h8 = rows / 8, n_g = cols / 8;
@@ -195,25 +177,101 @@ __global__ void __launch_bounds__(kThreads) double_prune28_kernel(const uint32_t
     const int64_t h8 = (tile % tiles_h) * 32 + lane;
     const int64_t g = (tile / tiles_h) * 8 + warp;
     if (h8 >= n_h8 || g >= n_g) continue;
-    uint32_t w[8], a[8], b[8];
+    uint32_t w[8], mb[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int64_t at = (8 * h8 + k) * n_g + g;
       w[k] = __ldg(vals + at);
-      const uint32_t byte = __ldg(meta + at);
-      a[k] = byte & 7u;
-      b[k] = (byte >> 3) & 7u;
+      mb[k] = __ldg(meta + at);
+    }
+    transpose_prune28_group(w, mb, 0, g, h8, n_h8, t_vals, t_meta);
+  }
+}
+
+// A2 for 2:8, cols % 256 == 0 (every row's segment of a tile is whole
+// 16-byte pieces): tiles of 256 rows x 256 columns (32
+// groups): the tile's rows (128 B of values, 32 B of metadata each) are
+// copied into shared memory with whole-row, coalesced loads; then thread
+// (lane o, warp G) takes row octet o and the four groups 4G .. 4G + 3, and
+// writes, for each of their 32 columns (output rows), 4 B of values and one
+// byte at column octet o, so a warp's stores to an output row are 128 B /
+// 32 B contiguous.  Shared layout: value word (row, group g) at
+// row·32 + (g ^ (row / 8 % 32)) and metadata word (row, G) at
+// row·8 + (G ^ (row / 8 % 8)), which spreads the lanes of a read over the
+// banks.
+constexpr int kDp8Rows = 256, kDp8Groups = 32;
+constexpr int kDp8Pieces = kDp8Rows * 10 / kThreads;  // 16 B pieces per thread and tile (8 of values, 2 of metadata per row)
+
+__global__ void __launch_bounds__(kThreads, 2) double_prune28_kernel(const uint32_t* __restrict__ vals,
+                                                                     const uint8_t* __restrict__ meta,
+                                                                     uint32_t* __restrict__ t_vals,
+                                                                     uint8_t* __restrict__ t_meta,
+                                                                     int64_t rows, int64_t cols) {
+  __shared__ uint32_t sv[kDp8Rows * kDp8Groups];      // 32 KB
+  __shared__ uint32_t sm[kDp8Rows * kDp8Groups / 4];  // 8 KB
+  grid_dependency_wait();
+  allow_dependents_launch();
+  const int64_t n_g = cols / 8, n_h8 = rows / 8;
+  const int64_t tiles_h = (rows + kDp8Rows - 1) / kDp8Rows, tiles = tiles_h * (n_g / kDp8Groups);
+  const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+  // piece u = threadIdx.x + kThreads·i of a tile: row u / 10, piece u % 10
+  // (0-7: four value words each, 8-9: sixteen metadata bytes each)
+  auto fetch = [&](int64_t tile, uint4 (&x)[kDp8Pieces]) {
+    const int64_t row0 = (tile % tiles_h) * kDp8Rows, g0 = (tile / tiles_h) * kDp8Groups;
+#pragma unroll
+    for (int i = 0; i < kDp8Pieces; ++i) {
+      const int u = static_cast<int>(threadIdx.x) + kThreads * i, piece = u % 10;
+      const int64_t row = row0 + u / 10;
+      x[i] = make_uint4(0, 0, 0, 0);
+      if (row < rows)
+        x[i] = piece < 8 ? __ldcs(reinterpret_cast<const uint4*>(vals + row * n_g + g0 + 4 * piece))
+                         : __ldcs(reinterpret_cast<const uint4*>(meta + row * n_g + g0 + 16 * (piece - 8)));
+    }
+  };
+  uint4 x[kDp8Pieces];
+  int64_t tile = blockIdx.x;
+  if (tile < tiles) fetch(tile, x);
+  for (; tile < tiles; tile += gridDim.x) {
+    const int64_t row0 = (tile % tiles_h) * kDp8Rows, g0 = (tile / tiles_h) * kDp8Groups;
+    __syncthreads();  // the previous tile's reads of shared memory are done
+#pragma unroll
+    for (int i = 0; i < kDp8Pieces; ++i) {
+      const int u = static_cast<int>(threadIdx.x) + kThreads * i, r = u / 10, piece = u % 10;
+      if (piece < 8) {
+        const uint32_t sw = static_cast<uint32_t>(r >> 3) & 31u;
+        uint32_t* d = sv + r * kDp8Groups;
+        d[(4 * piece + 0) ^ sw] = x[i].x;
+        d[(4 * piece + 1) ^ sw] = x[i].y;
+        d[(4 * piece + 2) ^ sw] = x[i].z;
+        d[(4 * piece + 3) ^ sw] = x[i].w;
+      } else {
+        const uint32_t sw = static_cast<uint32_t>(r >> 3) & 7u, w0 = 4 * (piece - 8);
+        uint32_t* d = sm + r * (kDp8Groups / 4);
+        d[(w0 + 0) ^ sw] = x[i].x;
+        d[(w0 + 1) ^ sw] = x[i].y;
+        d[(w0 + 2) ^ sw] = x[i].z;
+        d[(w0 + 3) ^ sw] = x[i].w;
+      }
+    }
+    __syncthreads();
+    // the next tile's pieces are in flight while this one is pruned
+    if (tile + gridDim.x < tiles) fetch(tile + gridDim.x, x);
+    const int64_t h8 = row0 / 8 + lane;
+    if (h8 >= n_h8) continue;
+    uint32_t w[8][4], mb[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int r = 8 * static_cast<int>(lane) + k;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[k][j] = sv[r * kDp8Groups + ((4 * warp + j) ^ lane)];
+      mb[k] = sm[r * (kDp8Groups / 4) + (warp ^ (lane & 7u))];
     }
 #pragma unroll
-    for (uint32_t c = 0; c < 8; ++c) {
-      uint32_t e[8];
+    for (int j = 0; j < 4; ++j) {  // group 4·warp + j of the tile
+      uint32_t wj[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) e[k] = a[k] == c ? (w[k] & 0xFFFFu) : (b[k] == c ? (w[k] >> 16) : 0u);
-      uint32_t byte;
-      const uint32_t v = top2_of_8(e, byte);
-      const int64_t i = 8 * g + c;  // output row = old column
-      __stcs(t_vals + i * n_h8 + h8, v);
-      t_meta[i * n_h8 + h8] = static_cast<uint8_t>(byte);
+      for (int k = 0; k < 8; ++k) wj[k] = w[k][j];
+      transpose_prune28_group(wj, mb, 8 * j, g0 + 4 * warp + j, h8, n_h8, t_vals, t_meta);
     }
   }
 }
@@ -237,24 +295,37 @@ __global__ void __launch_bounds__(kThreads) expand28_kernel(const uint32_t* __re
   grid_dependency_wait();
   allow_dependents_launch();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < ngroups; g += stride) {
-    const uint32_t w = __ldcs(vals + g), byte = meta[g];
-    const uint32_t i0 = byte & 7u, i1 = (byte >> 3) & 7u;
-    const uint32_t va = w & 0xFFFFu, vb = w >> 16;
-    uint32_t lo, hi, n0, n1;
-    if (i1 < 4) {  // both in quadruple 0
-      lo = quad24(i0, va, i1, vb, n0);
-      hi = quad24(0, 0, 1, 0, n1);
-    } else if (i0 >= 4) {  // both in quadruple 1
-      lo = quad24(0, 0, 1, 0, n0);
-      hi = quad24(i0 - 4, va, i1 - 4, vb, n1);
-    } else {  // one in each: pad with the lowest other position
-      const uint32_t p0 = i0 == 0 ? 1u : 0u, j1 = i1 - 4, p1 = j1 == 0 ? 1u : 0u;
-      lo = p0 < i0 ? quad24(p0, 0, i0, va, n0) : quad24(i0, va, p0, 0, n0);
-      hi = p1 < j1 ? quad24(p1, 0, j1, vb, n1) : quad24(j1, vb, p1, 0, n1);
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < ngroups;
+       base += stride * kUnroll) {
+    uint32_t wv[kUnroll], mv[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (base + u * stride < ngroups) {
+        wv[u] = __ldcs(vals + base + u * stride);
+        mv[u] = meta[base + u * stride];
+      }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t g = base + u * stride;
+      if (g >= ngroups) break;
+      const uint32_t w = wv[u], byte = mv[u];
+      const uint32_t i0 = byte & 7u, i1 = (byte >> 3) & 7u;
+      const uint32_t va = w & 0xFFFFu, vb = w >> 16;
+      uint32_t lo, hi, n0, n1;
+      if (i1 < 4) {  // both in quadruple 0
+        lo = quad24(i0, va, i1, vb, n0);
+        hi = quad24(0, 0, 1, 0, n1);
+      } else if (i0 >= 4) {  // both in quadruple 1
+        lo = quad24(0, 0, 1, 0, n0);
+        hi = quad24(i0 - 4, va, i1 - 4, vb, n1);
+      } else {  // one in each: pad with the lowest other position
+        const uint32_t p0 = i0 == 0 ? 1u : 0u, j1 = i1 - 4, p1 = j1 == 0 ? 1u : 0u;
+        lo = p0 < i0 ? quad24(p0, 0, i0, va, n0) : quad24(i0, va, p0, 0, n0);
+        hi = p1 < j1 ? quad24(p1, 0, j1, vb, n1) : quad24(j1, vb, p1, 0, n1);
+      }
+      __stcs(vals24 + g, make_uint2(lo, hi));
+      meta24[g] = static_cast<uint8_t>(n0 | (n1 << 4));
     }
-    __stcs(vals24 + g, make_uint2(lo, hi));
-    meta24[g] = static_cast<uint8_t>(n0 | (n1 << 4));
   }
 }
 
@@ -286,15 +357,6 @@ cudaError_t launch_prune12(const void* W, int64_t rows, int64_t cols, void* vals
                 meta, n);
 }
 
-cudaError_t launch_double_prune12(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols,
-                                  void* t_vals, uint8_t* t_meta, cudaStream_t stream) {
-  const int64_t tiles = ((rows / 8 + 31) / 32) * ((cols / 16 + 7) / 8);
-  if (tiles == 0) return cudaSuccess;
-  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
-  return launch(double_prune12_kernel, tiles < cap ? tiles : cap, stream, static_cast<const uint4*>(vals),
-                reinterpret_cast<const uint16_t*>(meta), static_cast<uint2*>(t_vals), t_meta, rows, cols);
-}
-
 cudaError_t launch_prune28(const void* W, int64_t rows, int64_t cols, void* vals, uint8_t* meta,
                            cudaStream_t stream) {
   const int64_t n = rows * cols / 8;
@@ -305,11 +367,17 @@ cudaError_t launch_prune28(const void* W, int64_t rows, int64_t cols, void* vals
 
 cudaError_t launch_double_prune28(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols,
                                   void* t_vals, uint8_t* t_meta, cudaStream_t stream) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  if (cols % 256 == 0) {  // whole 16-byte row pieces: the staged kernel
+    const int64_t tiles = ((rows + kDp8Rows - 1) / kDp8Rows) * (cols / 8 / kDp8Groups);
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 2;
+    return launch(double_prune28_kernel, tiles < cap ? tiles : cap, stream, static_cast<const uint32_t*>(vals),
+                  meta, static_cast<uint32_t*>(t_vals), t_meta, rows, cols);
+  }
   const int64_t tiles = ((rows / 8 + 31) / 32) * ((cols / 8 + 7) / 8);
-  if (tiles == 0) return cudaSuccess;
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
-  return launch(double_prune28_kernel, tiles < cap ? tiles : cap, stream, static_cast<const uint32_t*>(vals),
-                meta, static_cast<uint32_t*>(t_vals), t_meta, rows, cols);
+  return launch(double_prune28_direct_kernel, tiles < cap ? tiles : cap, stream,
+                static_cast<const uint32_t*>(vals), meta, static_cast<uint32_t*>(t_vals), t_meta, rows, cols);
 }
 
 cudaError_t launch_expand28(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols, void* vals24,

@@ -8,6 +8,8 @@
 //                             through shared memory, the other reads global
 //                             memory directly and takes any legal shape.
 //   prune_double24_kernel     A1 and A2 from one read of W (cols % 128 == 0).
+//   The two A2 kernels also prune the transpose 1:2 (one entry per row pair)
+//   for the 1:2 pattern, whose matrices are written in the 2:4 format.
 //
 // Source: "SLoPe: Double-Pruned Sparse Plus Lazy Low-Rank Adapter Pretraining
 // of LLMs", §1 and §2.1 (N:M pruning of the weight, then of its transpose)
@@ -107,6 +109,19 @@ __device__ __forceinline__ uint32_t top2_entry(uint32_t w01, uint32_t w23, const
   return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(out) + off);
 }
 
+// The 1:2 counterpart of top2_entry: each of the transposed group's two
+// row pairs (w01: rows 0 and 1, w23: rows 2 and 3, lower row in the low
+// half) keeps its entry of larger magnitude, the lower row on ties.  Same
+// encoding: the permute selector that packs the two kept entries in the low
+// 16 bits (below 0x8000), the nibble i0 | i1 << 2 (i0 in {0, 1}, i1 in
+// {2, 3}) at bit 16 + nib_shift.
+__device__ __forceinline__ uint32_t pair12_entry(uint32_t w01, uint32_t w23, uint32_t nib_shift) {
+  const uint32_t p0 = ((w01 >> 16) & 0x7FFFu) > (w01 & 0x7FFFu) ? 1u : 0u;
+  const uint32_t p1 = ((w23 >> 16) & 0x7FFFu) > (w23 & 0x7FFFu) ? 1u : 0u;
+  const uint32_t sel = (p0 ? 0x32u : 0x10u) | ((p1 ? 0x76u : 0x54u) << 8);
+  return sel | ((p0 | ((2u + p1) << 2)) << (16 + nib_shift));
+}
+
 // ---------------------------------------------------------------- A1 ------
 // One 16-byte chunk = 8 consecutive weights of a row = 2 groups -> 8 bytes of
 // kept values and one metadata byte.  Row-major contiguity makes chunk c of
@@ -166,7 +181,10 @@ __global__ void __launch_bounds__(kPruneThreads) prune24_kernel(const uint4* __r
 // kept): each transposed group takes the two positions its byte of
 // `t_meta_in` names, through the byte-permute selector of the nibble, and
 // no metadata is written.
-template <int Q, bool FROZEN = false>
+// P12: the transposed groups are pruned 1:2 (one entry per row pair)
+// instead of 2:4; the input format, the output format and the data
+// movement are the same.
+template <int Q, bool FROZEN = false, bool P12 = false>
 __device__ __forceinline__ void transpose_prune_octet(const uint32_t (&pw)[8][Q], const uint32_t (&m)[8],
                                                       const DpTables& tab,
                                                       uint2* __restrict__ t_vals,
@@ -212,6 +230,9 @@ __device__ __forceinline__ void transpose_prune_octet(const uint32_t (&pw)[8][Q]
         const uint32_t dm = dmv[q][j];  // low nibble: rows 0-3 of the octet
         ea = tab.gather[dm & 15u];
         eb = tab.gather[dm >> 4];
+      } else if constexpr (P12) {
+        ea = pair12_entry(a01, a23, 0);
+        eb = pair12_entry(b01, b23, 4);
       } else {
         ea = top2_entry(a01, a23, tab.out[0], k17, k1);
         eb = top2_entry(b01, b23, tab.out[1], k17, k1);
@@ -226,7 +247,7 @@ __device__ __forceinline__ void transpose_prune_octet(const uint32_t (&pw)[8][Q]
 // Any shape (rows % 8 == 0, cols % 16 == 0): each thread loads its octet's
 // rows straight from global memory; the eight warps of a block take
 // adjacent chunks, whose loads share sectors in L1.
-template <bool FROZEN>
+template <bool FROZEN, bool P12 = false>
 __global__ void __launch_bounds__(kDpThreads) double_prune24_kernel(
     const uint4* __restrict__ vals, const uint16_t* __restrict__ meta, uint2* __restrict__ t_vals,
     uint8_t* __restrict__ t_meta, int64_t rows, int64_t cols, uint32_t k17,
@@ -252,7 +273,7 @@ __global__ void __launch_bounds__(kDpThreads) double_prune24_kernel(
       pw[k][0] = v.x; pw[k][1] = v.y; pw[k][2] = v.z; pw[k][3] = v.w;
       m[k] = __ldg(meta + at);
     }
-    transpose_prune_octet<4, FROZEN>(pw, m, tab, t_vals, t_meta, rows / 8, h8, c16, k17, 0, t_meta_in);
+    transpose_prune_octet<4, FROZEN, P12>(pw, m, tab, t_vals, t_meta, rows / 8, h8, c16, k17, 0, t_meta_in);
   }
 }
 
@@ -288,7 +309,7 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
-template <int CH, int QS, bool FROZEN>
+template <int CH, int QS, bool FROZEN, bool P12 = false>
 __global__ void __launch_bounds__(32 * CH * QS) double_prune24_staged_kernel(
     const uint8_t* __restrict__ vals, const uint8_t* __restrict__ meta, uint2* __restrict__ t_vals,
     uint8_t* __restrict__ t_meta, int64_t rows, int64_t cols, uint32_t k17,
@@ -368,8 +389,8 @@ __global__ void __launch_bounds__(32 * CH * QS) double_prune24_staged_kernel(
         m[k] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(st + C::kValBytes + k * 512 +
                                                                           lane * 16 + moff + 2 * warp)) >> (4 * q0);
       }
-      transpose_prune_octet<kQ, FROZEN>(pw, m, tab, t_vals, t_meta, rows / 8, h8, ch0 + warp, k17, q0,
-                                        t_meta_in);
+      transpose_prune_octet<kQ, FROZEN, P12>(pw, m, tab, t_vals, t_meta, rows / 8, h8, ch0 + warp, k17, q0,
+                                             t_meta_in);
     }
     __syncthreads();
     th = nh;
@@ -624,12 +645,12 @@ cudaError_t launch_prune24(const void* W, int64_t rows, int64_t cols, void* vals
 }
 
 
-template <int CH, int QS, bool FROZEN = false>
+template <int CH, int QS, bool FROZEN = false, bool P12 = false>
 static cudaError_t run_staged(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols,
                               void* t_vals, uint8_t* t_meta, const uint8_t* t_meta_in,
                               cudaStream_t stream) {
   using C = DpStaged<CH, QS>;
-  auto kernel = double_prune24_staged_kernel<CH, QS, FROZEN>;
+  auto kernel = double_prune24_staged_kernel<CH, QS, FROZEN, P12>;
   static std::atomic<int> per_sm[64];
   int per = 0;
   if (cudaError_t e = blocks_per_sm(kernel, C::kThreads, C::kSmem, per_sm, per)) return e;
@@ -761,7 +782,7 @@ cudaError_t launch_axpby(float beta, const void* a, int a_dt, float gamma, const
   }
 }
 
-template <bool FROZEN>
+template <bool FROZEN, bool P12 = false>
 static cudaError_t double_prune24_any(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols,
                                       void* t_vals, uint8_t* t_meta, const uint8_t* t_meta_in,
                                       cudaStream_t stream) {
@@ -771,10 +792,10 @@ static cudaError_t double_prune24_any(const void* vals, const uint8_t* meta, int
     const int64_t tiles_h = (rows + 255) / 256;
     // (narrower tiles split each octet's columns over more threads)
     if (tiles_h * (cols / 128) >= sm_count())
-      return run_staged<8, 1, FROZEN>(vals, meta, rows, cols, t_vals, t_meta, t_meta_in, stream);
+      return run_staged<8, 1, FROZEN, P12>(vals, meta, rows, cols, t_vals, t_meta, t_meta_in, stream);
     if (tiles_h * (cols / 64) >= sm_count())
-      return run_staged<4, 2, FROZEN>(vals, meta, rows, cols, t_vals, t_meta, t_meta_in, stream);
-    return run_staged<2, 4, FROZEN>(vals, meta, rows, cols, t_vals, t_meta, t_meta_in, stream);
+      return run_staged<4, 2, FROZEN, P12>(vals, meta, rows, cols, t_vals, t_meta, t_meta_in, stream);
+    return run_staged<2, 4, FROZEN, P12>(vals, meta, rows, cols, t_vals, t_meta, t_meta_in, stream);
   }
   const int64_t tiles = ((rows / 8 + 31) / 32) * ((cols / 16 + 7) / 8);
   int64_t blocks = tiles;
@@ -786,7 +807,7 @@ static cudaError_t double_prune24_any(const void* vals, const uint8_t* meta, int
   cfg.blockDim = dim3(kDpThreads);
   cfg.stream = stream;
   add_pdl_attr(cfg, attrs);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, double_prune24_kernel<FROZEN>, static_cast<const uint4*>(vals),
+  cudaError_t e = cudaLaunchKernelEx(&cfg, double_prune24_kernel<FROZEN, P12>, static_cast<const uint4*>(vals),
                                      reinterpret_cast<const uint16_t*>(meta),
                                      static_cast<uint2*>(t_vals), t_meta, rows, cols, kKeyShift, t_meta_in);
   return e != cudaSuccess ? e : cudaGetLastError();
@@ -796,6 +817,11 @@ cudaError_t launch_double_prune24(const void* vals, const uint8_t* meta, int64_t
                                   int64_t cols, void* t_vals, uint8_t* t_meta,
                                   cudaStream_t stream) {
   return double_prune24_any<false>(vals, meta, rows, cols, t_vals, t_meta, nullptr, stream);
+}
+
+cudaError_t launch_double_prune12(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols,
+                                  void* t_vals, uint8_t* t_meta, cudaStream_t stream) {
+  return double_prune24_any<false, true>(vals, meta, rows, cols, t_vals, t_meta, nullptr, stream);
 }
 
 cudaError_t launch_double_prune24_frozen(const void* vals, const uint8_t* meta, int64_t rows,
