@@ -91,14 +91,14 @@ const char* slope_status_string(int status);
 int slope_version(void);
 
 /*
- * Bytes of scratch memory the compute calls below need for one linear of
- * these sizes (T tokens, in, out, rank r): the T x 2r bf16 plane of the
- * rank-r intermediate (4·T·r bytes, rounded up to 256) that
- * slope_linear_fwd and slope_linear_bwd_input use when the caller passes
- * XL (or G) as NULL.  Passing at least this many bytes as `workspace` to any
- * of them is always enough; slope_linear_bwd_weight needs none.  Returns 0
- * for r == 0 (no scratch) and for invalid sizes (the call itself then
- * reports them).
+ * Bytes of scratch memory that is always enough as the `workspace` of any of
+ * the compute calls below for one linear of these sizes (T tokens, in, out,
+ * rank r): the larger of the T x 2r bf16 plane of the rank-r intermediate
+ * (4·T·r bytes, rounded up to 256), which slope_linear_fwd and
+ * slope_linear_bwd_input use when the caller passes XL (or G) as NULL, and
+ * 256 bytes (slope_linear_bwd_weight uses 16 of them, when given, to keep
+ * its launch's tiles in step).  Returns 0 for invalid sizes (the call
+ * itself then reports them).
  */
 size_t slope_workspace_size(int64_t T, int64_t in, int64_t out, int r);
 
@@ -290,8 +290,16 @@ int slope_linear_bwd_input(const void* dY, int64_t T, int64_t in, int64_t out, c
  * order).  SLOPE_SKIP_DW computes only dL and dR (dW and Wm may be
  * NULL); SLOPE_SKIP_ADAPTER computes only dW (XL, G, dL, dR may be NULL);
  * both together are SLOPE_ERR_INVALID_ARG.  T == 0 writes zeros (or leaves
- * them, when accumulating).  This call needs no scratch: `workspace` is
- * not used (pass NULL, 0).  Size rules as slope_linear_fwd.
+ * them, when accumulating).  `workspace` is optional (NULL, 0 works): given
+ * at least 16 bytes, 16-byte aligned (else SLOPE_ERR_INVALID_ARG or
+ * SLOPE_ERR_ALIGNMENT), the call keeps a counter there that holds the dW
+ * launch's waves of tiles in step, so the tiles in flight share their
+ * slabs of dY and X in L2 and DRAM re-reads fall; its contents on entry do
+ * not matter, and it must not be used by another call until this one's
+ * work on `stream` is done.  The waves wait for each other, so the launch
+ * expects its CTAs to become resident together (kernels that hold SMs for
+ * seconds on other streams make it report SLOPE_ERR_TIMEOUT).  Size rules
+ * as slope_linear_fwd.
  */
 int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T, int64_t in, int64_t out,
                             const uint8_t* Wm, const void* XL, const void* G, int r, float* dW,

@@ -230,7 +230,11 @@ extern "C" int slope_version(void) { return 10000; }
 
 // Scratch of the two sparse-product calls: the T x 2r bf16 plane of the
 // rank-r intermediate (XL or G, hi parts then lo parts) when the caller does
-// not keep it, rounded up to 256 bytes.  The weight-gradient call needs none.
+// not keep it, rounded up to 256 bytes.  The weight-gradient call uses the
+// first kWaveSyncBytes of a workspace, when given, for the counter that
+// keeps its waves of tiles in step.
+constexpr size_t kWaveSyncBytes = 16;
+
 static size_t plane_bytes(int64_t T, int r) {
   const size_t b = static_cast<size_t>(T) * static_cast<size_t>(2 * r) * 2;
   return (b + 255) & ~static_cast<size_t>(255);
@@ -238,8 +242,9 @@ static size_t plane_bytes(int64_t T, int r) {
 
 extern "C" size_t slope_workspace_size(int64_t T, int64_t in, int64_t out, int r) {
   if (T < 0 || in <= 0 || out <= 0 || in % 128 != 0 || out % 128 != 0) return 0;
-  if (r <= 0 || r > 256 || r % 8 != 0 || T > (int64_t(1) << 31) - 1) return 0;
-  return plane_bytes(T, r);
+  if (r < 0 || r > 256 || r % 8 != 0 || T > (int64_t(1) << 31) - 1) return 0;
+  const size_t plane = r > 0 ? plane_bytes(T, r) : 0;
+  return plane > 256 ? plane : 256;
 }
 
 // The rank-r plane of a sparse-product call: the caller's output when given,
@@ -452,7 +457,6 @@ extern "C" int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T,
                                        const void* G, int r, float* dW, uint32_t flags, float* dL,
                                        float* dR, void* workspace, size_t workspace_bytes,
                                        void* stream) {
-  (void)workspace; (void)workspace_bytes;
   if (int s = check_linear(T, in, out, r)) return s;
   const uint32_t known =
       SLOPE_DW_DENSE | SLOPE_ACCUMULATE | SLOPE_SKIP_DW | SLOPE_SKIP_ADAPTER | SLOPE_DW_NM28;
@@ -467,6 +471,13 @@ extern "C" int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T,
   if (T > 0 && (!aligned16(dY) || !aligned16(X))) return SLOPE_ERR_ALIGNMENT;
   if (do_ad && (!aligned16(dL) || !aligned16(dR) || (T > 0 && (!aligned16(XL) || !aligned16(G)))))
     return SLOPE_ERR_ALIGNMENT;
+  // an optional workspace keeps the dW launch's waves of tiles in step
+  unsigned int* wave_ctr = nullptr;
+  if (workspace != nullptr) {
+    if (workspace_bytes < kWaveSyncBytes) return SLOPE_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return SLOPE_ERR_ALIGNMENT;
+    wave_ctr = static_cast<unsigned int*>(workspace);
+  }
   if (int s = check_device()) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool dense = flags & SLOPE_DW_DENSE, acc = flags & SLOPE_ACCUMULATE;
@@ -492,6 +503,7 @@ extern "C" int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T,
     w.M = out; w.N = in; w.K = T; w.lda = out; w.ldb = in;
     w.epi = DenseEpi::MaskedWeightGrad; w.out = dW; w.ldo = dw_cols;
     w.meta = Wm; w.dense_dw = dense; w.accumulate = acc; w.splits = 0; w.nm28 = nm28;
+    w.wave_ctr = wave_ctr;
     if (fuse) {
       w.fuse_r = r; w.xl = XL; w.g = G; w.dl = dL; w.dr = dR;
     }

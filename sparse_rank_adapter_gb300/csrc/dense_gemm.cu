@@ -84,6 +84,7 @@ struct DnParams {
   const uint8_t* meta;  // masked dW: metadata, N/8 bytes per row
   int dense_dw, accumulate, atomic_out;
   int nm28;  // masked dW: `meta` holds 2:8 bytes (i0 | i1 << 3 per 8 columns); compressed dW has N/4 per row
+  unsigned int* wave_ctr;  // pair dW: producers' arrival counter (zeroed before the launch), or NULL
   int lo_off, fold;
   int csplit;  // CTAs of a cluster that split one tile's K (hi/lo store only); 1 = none
   int fuse_r;  // pair dW kernel: r of the adapter gradients computed alongside; 0 = none
@@ -523,15 +524,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 // kernel before it (set-up overlaps that kernel's tail) and lets the next
 // kernel launch early; it writes only after the previous kernel is done.
 __global__ void __launch_bounds__(256) zero3_kernel(float4* a, int64_t na, float4* b, int64_t nb, float4* c,
-                                                    int64_t nc) {
+                                                    int64_t nc, float4* d, int64_t nd) {
   grid_dependency_wait();
   allow_dependents_launch();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < na + nb + nc; i += stride) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < na + nb + nc + nd; i += stride) {
     if (i < na) a[i] = z;
     else if (i < na + nb) b[i - na] = z;
-    else c[i - na - nb] = z;
+    else if (i < na + nb + nc) c[i - na - nb] = z;
+    else d[i - na - nb - nc] = z;
   }
 }
 
@@ -644,7 +646,21 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       }
       int it = 0;
       bool stop = false;
-      for (int u = unit0; u < units && !stop; u += ustep) {
+      // Waves in step: before the loads of its unit of wave w (w >= 1), every
+      // producer of the grid waits until all have issued wave w - 1's.  The
+      // units in flight then stay one compact raster block, whose slabs of
+      // dY and X the pairs share in L2.  Only waves in which every pair has
+      // a unit take part.
+      const int full_waves = units / ustep;
+      int wave = 0;
+      for (int u = unit0; u < units && !stop; u += ustep, ++wave) {
+        if (p.wave_ctr != nullptr && wave >= 1 && wave < full_waves) {
+          atomicAdd(p.wave_ctr, 1u);
+          if (!counter_wait_geq(p.wave_ctr, static_cast<unsigned int>(wave) * gridDim.x, abort_flag, p.status)) {
+            stop = true;
+            break;
+          }
+        }
         int m0, n0, z, kind;
         decode(u, m0, n0, z, kind);
         const CUtensorMap* mA = kind == 2 ? &tmG : &tmA;   // rows: weight rows, or G's columns
@@ -872,11 +888,19 @@ cudaError_t run_dw_pair(const DenseGemmArgs& a, cudaStream_t stream) {
   p.dense_dw = a.dense_dw ? 1 : 0;
   p.accumulate = a.accumulate ? 1 : 0;
   p.atomic_out = splits > 1 ? 1 : 0;
-  if (!a.accumulate && (p.atomic_out || fr > 0)) {
-    // dW when split K adds its parts; the adapter gradients are always added
-    const size_t ndw = p.atomic_out ? static_cast<size_t>(M) * a.ldo : 0;
-    const size_t nl = fr > 0 ? static_cast<size_t>(N) * fr : 0, nr = fr > 0 ? static_cast<size_t>(fr) * M : 0;
-    if (cudaError_t e = launch_zero3(static_cast<float*>(a.out), ndw, a.dl, nl, a.dr, nr, stream)) return e;
+  p.wave_ctr = a.wave_ctr;
+  {
+    // dW when split K adds its parts; the adapter gradients are always
+    // added; the wave counter starts at zero (4 floats: 16 bytes)
+    const bool zero_out = !a.accumulate;
+    const size_t ndw = zero_out && p.atomic_out ? static_cast<size_t>(M) * a.ldo : 0;
+    const size_t nl = zero_out && fr > 0 ? static_cast<size_t>(N) * fr : 0;
+    const size_t nr = zero_out && fr > 0 ? static_cast<size_t>(fr) * M : 0;
+    const size_t nw = a.wave_ctr != nullptr ? 4 : 0;
+    if (ndw + nl + nr + nw > 0)
+      if (cudaError_t e = launch_zero3(static_cast<float*>(a.out), ndw, a.dl, nl, a.dr, nr, stream,
+                                       reinterpret_cast<float*>(a.wave_ctr), nw))
+        return e;
   }
   p.status = device_status_ptr();
   if (!p.status) return cudaErrorInvalidDevicePointer;
@@ -999,9 +1023,9 @@ cudaError_t run_rank(const DenseGemmArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_zero3(float* a, size_t na, float* b, size_t nb, float* c, size_t nc,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, float* d, size_t nd) {
   // counts in floats, each a multiple of 4 (16-byte aligned arrays)
-  const int64_t n4 = static_cast<int64_t>((na + nb + nc) / 4);
+  const int64_t n4 = static_cast<int64_t>((na + nb + nc + nd) / 4);
   if (n4 == 0) return cudaSuccess;
   int64_t blocks = (n4 + 255) / 256;
   const int64_t cap = static_cast<int64_t>(sm_count()) * 4;
@@ -1014,7 +1038,8 @@ cudaError_t launch_zero3(float* a, size_t na, float* b, size_t nb, float* c, siz
   add_pdl_attr(cfg, attrs);
   cudaError_t e = cudaLaunchKernelEx(&cfg, zero3_kernel, reinterpret_cast<float4*>(a), static_cast<int64_t>(na / 4),
                                      reinterpret_cast<float4*>(b), static_cast<int64_t>(nb / 4),
-                                     reinterpret_cast<float4*>(c), static_cast<int64_t>(nc / 4));
+                                     reinterpret_cast<float4*>(c), static_cast<int64_t>(nc / 4),
+                                     reinterpret_cast<float4*>(d), static_cast<int64_t>(nd / 4));
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -73,10 +73,10 @@ cudaError_t launch_double_prune28(const void* vals, const uint8_t* meta, int64_t
 cudaError_t launch_expand28(const void* vals, const uint8_t* meta, int64_t rows, int64_t cols, void* vals24,
                             uint8_t* meta24, cudaStream_t stream);
 
-// Zeroes up to three fp32 arrays (counts in floats, multiples of 4) in one
-// programmatic-dependent launch (dense_gemm.cu).
+// Zeroes up to three fp32 arrays, and a fourth small one (counts in floats,
+// multiples of 4) in one programmatic-dependent launch (dense_gemm.cu).
 cudaError_t launch_zero3(float* a, size_t na, float* b, size_t nb, float* c, size_t nc,
-                         cudaStream_t stream);
+                         cudaStream_t stream, float* d = nullptr, size_t nd = 0);
 
 // ---- tensor-core rate self test (mma_rate.cu): enqueues the launch and
 // writes the dense-equivalent flops it executes to *flops.
@@ -145,6 +145,9 @@ struct DenseGemmArgs {
   const void* g = nullptr;
   float* dl = nullptr;
   float* dr = nullptr;
+  // MaskedWeightGrad on CTA pairs: 16 bytes of the caller's workspace for the
+  // counter that keeps the pairs' waves of tiles in step, or NULL
+  unsigned int* wave_ctr = nullptr;
 };
 cudaError_t launch_dense_gemm(const DenseGemmArgs& a, cudaStream_t stream);
 

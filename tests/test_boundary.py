@@ -199,7 +199,7 @@ def test_workspace_size_is_the_rank_plane(L):
     assert L.slope_workspace_size(4096, 1024, 1024, 16) == 4 * 4096 * 16
     assert L.slope_workspace_size(1, 256, 256, 8) == 256
     assert L.slope_workspace_size(16384, 7168, 28672, 64) == 4 * 16384 * 64
-    assert L.slope_workspace_size(4096, 1024, 1024, 0) == 0   # no adapter, no scratch
+    assert L.slope_workspace_size(4096, 1024, 1024, 0) == 256  # the weight gradient's wave counter
     assert L.slope_workspace_size(4096, 1024, 1024, 12) == 0  # invalid rank
     assert L.slope_workspace_size(-1, 1024, 1024, 16) == 0
     assert L.slope_workspace_size(64, 200, 256, 8) == 0
@@ -218,6 +218,10 @@ def test_workspace_argument_checks(L):
     assert bi(A, 64, 256, 256, A, A, A, A, 8, A, 0, None, MIS, need, None) == L.ERR_ALIGNMENT
     # no adapter: nothing is needed
     assert fwd(A, 64, 256, 256, A, A, None, None, 0, MIS, 0, None, None, 0, None) == L.ERR_ALIGNMENT
+    # the weight gradient's optional workspace: at least 16 bytes, aligned
+    bw = L.lib().slope_linear_bwd_weight
+    assert bw(A, A, 64, 256, 256, A, A, A, 8, A, 0, A, A, A, 8, None) == L.ERR_INVALID_ARG
+    assert bw(A, A, 64, 256, 256, A, A, A, 8, A, 0, A, A, MIS, 16, None) == L.ERR_ALIGNMENT
 
 
 def test_binding_refuses_cpu_tensors(L):

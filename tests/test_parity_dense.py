@@ -51,3 +51,48 @@ def test_weight_and_adapter_grads(S, T, inp, out, r, dense):
         assert_close_rel("dW", got, dWc)
     assert_close_rel("dL", gdL.double().cpu().numpy(), dL)
     assert_close_rel("dR", gdR.double().cpu().numpy(), dR)
+
+
+@pytest.mark.parametrize("T,inp,out,r", [(2048, 4096, 4096, 16), (16384, 1024, 1024, 8), (4096, 2048, 6144, 0)])
+def test_weight_grad_with_waves_in_step(S, T, inp, out, r):
+    """With a workspace the dW launch keeps its waves of tiles in step (a
+    grid-wide counter between waves).  The tiles and their arithmetic are
+    unchanged: the outputs match the call without a workspace (bit for bit
+    where K is not split) and the oracle."""
+    import torch
+
+    d = synth.layer_inputs(0, 60 + r, T, inp, out, r)
+    X, dY = to_dev(d["X"]), to_dev(d["dY"])
+    W = to_dev(d["W"])
+    Wv = torch.empty(out, inp // 2, dtype=torch.bfloat16, device="cuda")
+    Wm = torch.empty(out, inp // 8, dtype=torch.uint8, device="cuda")
+    S.slope_prune_nm(W, Wv, Wm)
+    XL = torch.empty(T, 2 * r, dtype=torch.bfloat16, device="cuda") if r else None
+    G = torch.empty(T, 2 * r, dtype=torch.bfloat16, device="cuda") if r else None
+    L = to_dev(d["L"]) if r else None
+    R = to_dev(d["R"]) if r else None
+    if r:
+        S.slope_linear_fwd(X, Wv, Wm, L, R, torch.empty(T, out, device="cuda"), XL)
+        Dv = torch.empty(inp, out // 2, dtype=torch.bfloat16, device="cuda")
+        Dm = torch.empty(inp, out // 8, dtype=torch.uint8, device="cuda")
+        S.slope_double_prune(Wv, Wm, out, inp, Dv, Dm)
+        S.slope_linear_bwd_input(dY, Dv, Dm, L, R, torch.empty(T, inp, device="cuda"), G)
+    ws = torch.full((256,), 0x5A, dtype=torch.uint8, device="cuda")  # contents must not matter
+    outs = []
+    for workspace in (None, ws, ws):  # twice with the workspace: the counter restarts
+        dW = torch.full((out, inp // 2), float("nan"), device="cuda")
+        dL = torch.full((inp, r), float("nan"), device="cuda") if r else None
+        dR = torch.full((r, out), float("nan"), device="cuda") if r else None
+        S.slope_linear_bwd_weight(dY, X, Wm, XL, G, dW, dL, dR, workspace=workspace)
+        torch.cuda.synchronize()
+        S.slope_device_status()
+        outs.append((dW, dL, dR))
+    vals, meta, _ = O.prune24(d["W"])
+    dWc, _, dLr, dRr = O.linear_bwd_weight(d["dY"], d["X"], meta, d["L"] if r else None, d["R"] if r else None)
+    for dW, dL, dR in outs[1:]:
+        assert_close_rel("dW", dW.double().cpu().numpy(), dWc)
+        if r:
+            assert_close_rel("dL", dL.double().cpu().numpy(), dLr)
+            assert_close_rel("dR", dR.double().cpu().numpy(), dRr)
+    if T <= 4096:  # no split of K: the same tiles, the same sums
+        assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[1][0], outs[2][0])
