@@ -33,7 +33,11 @@ Step variants (the default is the five path calls per linear):
                      A1 and A2, and beta·A + gamma·B (slope_sparse_axpby) on an
                      fp32 master copy of the kept values after the gradients;
   --frozen-columns   with --optimizer, the column mask kept too
-                     (slope_recompress_frozen).
+                     (slope_recompress_frozen);
+  --streams N        the block's linears (independent in this synthetic
+                     step) issued on N streams, linear i on stream i % N,
+                     forked from and joined into the step's stream; the
+                     default, one stream, runs them as a dependent chain.
 Every memory-bound call's achieved bandwidth is reported in `hbm_calls`, and
 the library's tensor-pipe rate self test in `mma_rate_selftest`.
 """
@@ -245,13 +249,15 @@ class BlockStep:
         # N:M pattern of the weights: 2:4, 1:2 (in the 2:4 format) or 2:8
         # (its own format, expanded to its 2:4 form for the sparse products)
         self.n, self.m = (int(x) for x in pattern.split(":"))
+        self.extra_streams = []  # streams beside the step's own (see run)
         self.fused_prune = fused_prune
         self.optimizer = optimizer  # kept row mask: re-compression + A2, then beta·A + gamma·B
         self.frozen_columns = frozen_columns  # the column mask kept too: no second selection
         T, r = wl.tokens, wl.rank
-        # workspace of the weight-gradient calls (its wave counter); the
-        # calls of a step run one after another on one stream
-        self.workspace = torch.empty(256, dtype=torch.uint8, device=device)
+        # workspaces of the weight-gradient calls (their wave counters), one
+        # per stream the step may use: calls on one stream run one after
+        # another, calls on two streams may overlap
+        self.workspaces = [torch.empty(256, dtype=torch.uint8, device=device) for _ in range(8)]
         self.layers = []
         for li, lin in enumerate(wl.linears):
             inp, out = lin.inp, lin.out
@@ -318,66 +324,75 @@ class BlockStep:
         and both gradients; an inference step runs the forward on the
         pre-compressed weights."""
         S = self.S
-        for b in (self.layers if only is None else [self.layers[only]]):
+        # the block's linears are independent: with extra streams, linear i
+        # goes to stream i % n (forked from and joined back into `stream`)
+        lanes = [stream] + (list(self.extra_streams) if only is None else [])
+        for x in lanes[1:]:
+            x.wait_stream(stream)
+        for li, b in enumerate(self.layers if only is None else [self.layers[only]]):
+            sl = lanes[li % len(lanes)]
             if self.wl.forward_only:
                 calls = []
             elif self.optimizer and self.frozen_columns:  # the updated W at both kept masks
                 calls = [("recompress_frozen", lambda b=b: S.slope_recompress_frozen(
-                    b["W"], b["Wm"], b["Dm"], b["Wv"], b["Dv"], stream=stream))]
+                    b["W"], b["Wm"], b["Dm"], b["Wv"], b["Dv"], stream=sl))]
             elif self.optimizer:  # the updated W at the kept mask, and the second pruning
                 calls = [("recompress_double", lambda b=b: S.slope_recompress_double_prune(
-                    b["W"], b["Wm"], b["Wv"], b["Dv"], b["Dm"], stream=stream))]
+                    b["W"], b["Wm"], b["Wv"], b["Dv"], b["Dm"], stream=sl))]
             elif self.fused_prune:  # A1 and A2 from one read of W
                 calls = [("prune_double", lambda b=b: S.slope_prune_and_double_prune(
-                    b["W"], b["Wv"], b["Wm"], b["Dv"], b["Dm"], stream=stream))]
+                    b["W"], b["Wv"], b["Wm"], b["Dv"], b["Dm"], stream=sl))]
             elif self.m == 2:  # 1:2, written in the 2:4 format
                 calls = [
-                    ("prune12", lambda b=b: S.slope_prune_nm(b["W"], b["Wv"], b["Wm"], n=1, m=2, stream=stream)),
+                    ("prune12", lambda b=b: S.slope_prune_nm(b["W"], b["Wv"], b["Wm"], n=1, m=2, stream=sl)),
                     ("double_prune12", lambda b=b: S.slope_double_prune_nm(
-                        b["Wv"], b["Wm"], b["out"], b["inp"], b["Dv"], b["Dm"], n=1, m=2, stream=stream)),
+                        b["Wv"], b["Wm"], b["out"], b["inp"], b["Dv"], b["Dm"], n=1, m=2, stream=sl)),
                 ]
             elif self.m == 8:  # 2:8, and the 2:4 forms the sparse products read
                 calls = [
-                    ("prune28", lambda b=b: S.slope_prune_nm(b["W"], b["Wv8"], b["Wm8"], n=2, m=8, stream=stream)),
+                    ("prune28", lambda b=b: S.slope_prune_nm(b["W"], b["Wv8"], b["Wm8"], n=2, m=8, stream=sl)),
                     ("expand28", lambda b=b: S.slope_expand_nm_to_24(
-                        b["Wv8"], b["Wm8"], b["out"], b["inp"], b["Wv"], b["Wm"], stream=stream)),
+                        b["Wv8"], b["Wm8"], b["out"], b["inp"], b["Wv"], b["Wm"], stream=sl)),
                     ("double_prune28", lambda b=b: S.slope_double_prune_nm(
-                        b["Wv8"], b["Wm8"], b["out"], b["inp"], b["Dv8"], b["Dm8"], n=2, m=8, stream=stream)),
+                        b["Wv8"], b["Wm8"], b["out"], b["inp"], b["Dv8"], b["Dm8"], n=2, m=8, stream=sl)),
                     ("expand28_t", lambda b=b: S.slope_expand_nm_to_24(
-                        b["Dv8"], b["Dm8"], b["inp"], b["out"], b["Dv"], b["Dm"], stream=stream)),
+                        b["Dv8"], b["Dm8"], b["inp"], b["out"], b["Dv"], b["Dm"], stream=sl)),
                 ]
             else:
                 calls = [
-                    ("prune", lambda b=b: S.slope_prune_nm(b["W"], b["Wv"], b["Wm"], stream=stream)),
+                    ("prune", lambda b=b: S.slope_prune_nm(b["W"], b["Wv"], b["Wm"], stream=sl)),
                     ("double_prune", lambda b=b: S.slope_double_prune(b["Wv"], b["Wm"], b["out"], b["inp"],
-                                                                      b["Dv"], b["Dm"], stream=stream)),
+                                                                      b["Dv"], b["Dm"], stream=sl)),
                 ]
             calls += [
                 ("fwd", lambda b=b: S.slope_linear_fwd(b["X"], b["Wv"], b["Wm"], b["L"], b["R"], b["Y"],
-                                                       b["XL"], stream=stream)),
+                                                       b["XL"], stream=sl)),
             ]
             if not self.wl.forward_only:
                 calls += [
                     ("bwd_input", lambda b=b: S.slope_linear_bwd_input(b["dY"], b["Dv"], b["Dm"], b["L"], b["R"],
-                                                                       b["dX"], b["G"], stream=stream)),
+                                                                       b["dX"], b["G"], stream=sl)),
                     # dW and the adapter gradients dL, dR in one call (one
                     # launch: the dW GEMM computes the two rank-r products too)
                     ("bwd_weight", lambda b=b: S.slope_linear_bwd_weight(
                         b["dY"], b["X"], b["Wm8"] if self.m == 8 else b["Wm"], b["XL"], b["G"], b["dW"],
-                        b["dL"], b["dR"], flags=S.DW_NM28 if self.m == 8 else 0, workspace=self.workspace,
-                        stream=stream)),
+                        b["dL"], b["dR"], flags=S.DW_NM28 if self.m == 8 else 0,
+                        workspace=self.workspaces[li % len(lanes)],
+                        stream=sl)),
                 ]
                 if self.optimizer:  # decayed master values plus the scaled gradient, in place
                     calls += [("axpby", lambda b=b: S.slope_sparse_axpby(
-                        0.9999, b["Wmaster"], -1e-3, b["dW"], b["Wmaster"], stream=stream))]
+                        0.9999, b["Wmaster"], -1e-3, b["dW"], b["Wmaster"], stream=sl))]
             for name, fn in calls:
                 if marks is not None:
                     e0, e1 = marks.new(name, b)
-                    e0.record(stream)
+                    e0.record(sl)
                     fn()
-                    e1.record(stream)
+                    e1.record(sl)
                 else:
                     fn()
+        for x in lanes[1:]:
+            stream.wait_stream(x)
 
     def launches_per_step(self):
         import torch
@@ -571,6 +586,9 @@ def gpu_arm(args):
     n_sets = max(1, args.sets)
     sets = [BlockStep(wl, seed=s + 10 * rank, device=dev, fused_prune=args.fused_prune, optimizer=args.optimizer,
                       frozen_columns=args.frozen_columns, pattern=args.pattern) for s in range(n_sets)]
+    extra = [torch.cuda.Stream(device=dev) for _ in range(min(max(1, args.streams), 8) - 1)]
+    for st in sets:
+        st.extra_streams = extra
     torch.cuda.synchronize()
 
     with torch.cuda.stream(stream):
@@ -737,6 +755,7 @@ def gpu_arm(args):
                        "linears": [f"{x.name}:{x.inp}->{x.out}" for x in wl.linears],
                        "l2": f"{n_sets} rotating input sets of {set_bytes(sets[0]) / 2**20:.0f} MiB (> L2 {L2_BYTES // 2**20} MiB)",
                        "graph": bool(args.graph), "parallelism": f"replicas x{world}",
+                       "streams": max(1, min(args.streams, 8)),
                        "prune": ("both masks kept: re-compression, then beta*A + gamma*B"
                                  if args.optimizer and args.frozen_columns
                                  else "kept mask: re-compression + A2, then beta*A + gamma*B" if args.optimizer
@@ -1149,6 +1168,8 @@ def main():
                          "(slope_recompress_frozen in place of the re-compression + A2)")
     ap.add_argument("--fused-prune", action="store_true",
                     help="A1 and A2 through the one-call slope_prune_and_double_prune")
+    ap.add_argument("--streams", type=int, default=1,
+                    help="issue the block's independent linears on this many streams")
     ap.add_argument("--tiling-study", action="store_true",
                     help="time FC1 forwards as one call against four square tiles (one JSON line)")
     ap.add_argument("--pattern", default="2:4", choices=["2:4", "1:2", "2:8"],
