@@ -640,6 +640,8 @@ def gpu_arm(args):
         t_end.synchronize()
     clocks = clk.summary()
     ms_step = t_start.elapsed_time(t_end) / args.steps
+    S = sets[0].S
+    S.slope_device_status(stream)  # raises if a kernel-side wait ran out during the timed steps
 
     # Per-call breakdown: `call_reps` marked passes over every input set; a
     # call's time per step is the median over the passes of its summed

@@ -296,10 +296,11 @@ int slope_linear_bwd_input(const void* dY, int64_t T, int64_t in, int64_t out, c
  * launch's waves of tiles in step, so the tiles in flight share their
  * slabs of dY and X in L2 and DRAM re-reads fall; its contents on entry do
  * not matter, and it must not be used by another call until this one's
- * work on `stream` is done.  The waves wait for each other, so the launch
- * expects its CTAs to become resident together (kernels that hold SMs for
- * seconds on other streams make it report SLOPE_ERR_TIMEOUT).  Size rules
- * as slope_linear_fwd.
+ * work on `stream` is done.  The waiting is advisory: a wave that does not
+ * come together within about 50 µs (e.g. when other kernels hold SMs so
+ * that the launch's CTAs are not resident together) ends it for the rest of
+ * the launch, without error and with the same results.  Size rules as
+ * slope_linear_fwd.
  */
 int slope_linear_bwd_weight(const void* dY, const void* X, int64_t T, int64_t in, int64_t out,
                             const uint8_t* Wm, const void* XL, const void* G, int r, float* dW,

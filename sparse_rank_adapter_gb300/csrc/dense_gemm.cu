@@ -650,16 +650,17 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       // producer of the grid waits until all have issued wave w - 1's.  The
       // units in flight then stay one compact raster block, whose slabs of
       // dY and X the pairs share in L2.  Only waves in which every pair has
-      // a unit take part.
+      // a unit take part.  The wait only saves DRAM traffic: it is bounded
+      // at about 50 µs, after which this producer stops waiting for the
+      // rest of the launch (e.g. when CTAs of the grid cannot be resident
+      // together because other kernels hold SMs).
       const int full_waves = units / ustep;
+      bool in_step = p.wave_ctr != nullptr;
       int wave = 0;
       for (int u = unit0; u < units && !stop; u += ustep, ++wave) {
-        if (p.wave_ctr != nullptr && wave >= 1 && wave < full_waves) {
+        if (in_step && wave >= 1 && wave < full_waves) {
           atomicAdd(p.wave_ctr, 1u);
-          if (!counter_wait_geq(p.wave_ctr, static_cast<unsigned int>(wave) * gridDim.x, abort_flag, p.status)) {
-            stop = true;
-            break;
-          }
+          in_step = counter_wait_geq(p.wave_ctr, static_cast<unsigned int>(wave) * gridDim.x, 100000);
         }
         int m0, n0, z, kind;
         decode(u, m0, n0, z, kind);

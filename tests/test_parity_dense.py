@@ -96,3 +96,49 @@ def test_weight_grad_with_waves_in_step(S, T, inp, out, r):
             assert_close_rel("dR", dR.double().cpu().numpy(), dRr)
     if T <= 4096:  # no split of K: the same tiles, the same sums
         assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[1][0], outs[2][0])
+
+
+def test_weight_grads_with_workspaces_on_two_streams(S):
+    """Two weight-gradient calls with their own workspaces, issued on two
+    streams so that their launches can overlap: waves that cannot come
+    together (the two grids share the SMs) stop waiting, and both results
+    still match the oracle with no device-side error."""
+    import torch
+
+    T, inp, out, r = 2048, 4096, 4096, 16
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    cases = []
+    for k, st in enumerate(streams):
+        d = synth.layer_inputs(0, 80 + k, T, inp, out, r)
+        X, dY, W = to_dev(d["X"]), to_dev(d["dY"]), to_dev(d["W"])
+        Wv = torch.empty(out, inp // 2, dtype=torch.bfloat16, device="cuda")
+        Wm = torch.empty(out, inp // 8, dtype=torch.uint8, device="cuda")
+        S.slope_prune_nm(W, Wv, Wm)
+        XL = torch.empty(T, 2 * r, dtype=torch.bfloat16, device="cuda")
+        G = torch.empty(T, 2 * r, dtype=torch.bfloat16, device="cuda")
+        S.slope_linear_fwd(X, Wv, Wm, to_dev(d["L"]), to_dev(d["R"]), torch.empty(T, out, device="cuda"), XL)
+        Dv = torch.empty(inp, out // 2, dtype=torch.bfloat16, device="cuda")
+        Dm = torch.empty(inp, out // 8, dtype=torch.uint8, device="cuda")
+        S.slope_double_prune(Wv, Wm, out, inp, Dv, Dm)
+        S.slope_linear_bwd_input(dY, Dv, Dm, to_dev(d["L"]), to_dev(d["R"]), torch.empty(T, inp, device="cuda"), G)
+        cases.append((d, X, dY, Wm, XL, G))
+    torch.cuda.synchronize()
+    outs = []
+    for (d, X, dY, Wm, XL, G), st in zip(cases, streams):
+        dW = torch.full((out, inp // 2), float("nan"), device="cuda")
+        dL = torch.empty(inp, r, device="cuda")
+        dR = torch.empty(r, out, device="cuda")
+        ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(st):
+            for _ in range(3):  # several launches in flight on each stream
+                S.slope_linear_bwd_weight(dY, X, Wm, XL, G, dW, dL, dR, workspace=ws, stream=st)
+        outs.append((dW, dL, dR, ws))
+    torch.cuda.synchronize()
+    S.slope_device_status()
+    for (d, *_), (dW, dL, dR, _) in zip(cases, outs):
+        vals, meta, _ = O.prune24(d["W"])
+        dWc, _, dLr, dRr = O.linear_bwd_weight(d["dY"], d["X"], meta, d["L"], d["R"])
+        assert_close_rel("dW", dW.double().cpu().numpy(), dWc)
+        assert_close_rel("dL", dL.double().cpu().numpy(), dLr)
+        assert_close_rel("dR", dR.double().cpu().numpy(), dRr)
