@@ -65,20 +65,23 @@ template <int BN>
 struct SpCfg {
   static constexpr int B_BYTES = BN * 256;  // two 64-column SW128 atoms of BN rows
   static constexpr int STAGE = kA_BYTES + B_BYTES + kMETA_BYTES;
-  // fp32 partial tile a cluster peer hands to its leader when a narrow tile's
-  // K is split over a cluster (column-major: [BN][128])
-  static constexpr int RED_BYTES = BN <= 64 ? kBM * BN * 4 : 0;
-  static constexpr int STAGES_FIT = (200 * 1024 - RED_BYTES) / STAGE;
+  // fp32 partial tile a cluster peer hands to its leader when a tile's K is
+  // split over a cluster (column-major: [BN][128]).  A split cluster owns
+  // exactly one tile, so by the time the partial exists every stage fill has
+  // been consumed: the partial lives in the stage ring.
+  static constexpr int RED_BYTES = kBM * BN * 4;
+  static constexpr int STAGES_FIT = 200 * 1024 / STAGE;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int ACC_COLS = BN < 32 ? 32 : BN;  // one accumulator buffer
   static constexpr int META_COL = 2 * ACC_COLS;        // after the two buffers
   static constexpr int TMEM_NEED = META_COL + 16 * STAGES;
   static constexpr int TMEM_COLS =
       TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
-  static constexpr int SMEM = STAGES * STAGE + 1024 /*barriers*/ + RED_BYTES + 1024 /*align slack*/;
+  static constexpr int SMEM = STAGES * STAGE + 1024 /*barriers*/ + 1024 /*align slack*/;
   static_assert(STAGE % 1024 == 0, "stage must keep 1024-byte alignment");
   static_assert(TMEM_NEED <= 512, "TMEM budget");
   static_assert(STAGES >= 2, "pipeline depth");
+  static_assert(STAGES * STAGE >= RED_BYTES, "the split partial fits in the stage ring");
 };
 
 // Row-major metadata word of this lane's row -> the word the sparse MMA
@@ -122,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* red_empty = red_full + 1;  // split peer: the leader has read this CTA's partial
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(red_empty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  float* red = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE + 1024);
+  float* red = reinterpret_cast<float*>(smem);  // split partial, over the drained stage ring
 
   const int warp = warp_id(), lane = lane_id();
   // Cluster split of K (narrow tiles): CTA `crank` of the
@@ -349,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[buf]);
         }
-        if constexpr (C::RED_BYTES > 0) {
+        if (cs > 1) {
           const int row = 32 * q + lane;
           if (peer) {  // hand the partial over; the leader stores
 #pragma unroll
@@ -454,6 +457,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (cs > 1) cluster_sync();
 }
 
+// Tiles that leave SMs idle split K over a cluster of up to 8 CTAs; the
+// partials meet in the leader's registers.  The hand-over costs about 2.5 us,
+// so each CTA keeps at least 16 sparse K-blocks.  Returns the CTAs per tile
+// (1 = no split) and the sparse K-blocks each takes.
+int split_of(int num_tiles, int num_kb, int* kb_per_split) {
+  *kb_per_split = num_kb;
+  if (num_tiles <= 0) return 1;
+  int want = sm_count() / num_tiles;
+  want = want < 8 ? want : 8;
+  want = want < num_kb / 16 ? want : num_kb / 16;
+  if (want < 2) return 1;
+  *kb_per_split = (num_kb + want - 1) / want;
+  return (num_kb + *kb_per_split - 1) / *kb_per_split;  // each CTA >= 1 block
+}
+
+// CTAs the one-CTA kernel keeps busy with BN-token tiles.
+int busy_ctas(int64_t M, int64_t N, int64_t K, int bn) {
+  const int tiles = static_cast<int>((M / kBM) * ((N + bn - 1) / bn));
+  int per = 0;
+  const int cs = split_of(tiles, static_cast<int>(K / 128), &per);
+  if (cs > 1) return tiles * cs;
+  return tiles < sm_count() ? tiles : sm_count();
+}
+
 template <int BN, bool A2_MN>
 cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
   using C = SpCfg<BN>;
@@ -506,20 +533,7 @@ cudaError_t run(const SparseGemmArgs& a, cudaStream_t stream) {
     p.group_m = g < 1 ? 1 : (g > p.tiles_m ? p.tiles_m : g);
   }
   p.out_bf16 = a.out_bf16 ? 1 : 0;
-  // Narrow tiles that leave SMs idle split K over a cluster of up to 8 CTAs;
-  // the partials meet in the leader's registers.  The hand-over costs about
-  // 2.5 us, so each CTA keeps at least 16 sparse K-blocks.
-  p.csplit = 1;
-  p.kb_per_split = p.num_kb;
-  if (C::RED_BYTES > 0) {
-    int want = sm_count() / p.num_tiles;
-    want = want < 8 ? want : 8;
-    want = want < p.num_kb / 16 ? want : p.num_kb / 16;
-    if (want >= 2) {
-      p.kb_per_split = (p.num_kb + want - 1) / want;
-      p.csplit = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;  // each CTA >= 1 block
-    }
-  }
+  p.csplit = split_of(p.num_tiles, p.num_kb, &p.kb_per_split);
   p.out = a.out;
   p.status = device_status_ptr();
   if (!p.status) return cudaErrorInvalidDevicePointer;
@@ -1001,8 +1015,9 @@ cudaError_t run_pair2(const SparseGemmArgs& a, cudaStream_t stream) {
 }
 
 // N tile by token count: the smallest tile that covers small batches (up to
-// 128 tokens, 64-wide tiles while the weight has fewer 128-row tiles than
-// there are SMs, so that its stream spreads over more of them); for large
+// 128 tokens; while the weight has fewer 128-row tiles than there are SMs,
+// 128-token tiles with K split over a cluster, unless 64-token tiles keep
+// more SMs busy); for large
 // batches CTA pairs with 224- or 128-token tiles (an even number of weight
 // tiles), else one CTA with 192 (the widest that still double-buffers in
 // TMEM beside the metadata) unless 128 gives the grid noticeably more tiles.
@@ -1012,7 +1027,12 @@ cudaError_t dispatch(const SparseGemmArgs& a, cudaStream_t stream) {
   if (a.N <= 64) return run<64, A2_MN>(a, stream);
   const int64_t tiles_m = a.M / kBM;
   const bool pair = tiles_m % 2 == 0;  // clusters pair M-adjacent tiles
-  if (a.N <= 128 && tiles_m < sm_count()) return run<64, A2_MN>(a, stream);
+  if (a.N <= 128 && tiles_m < sm_count()) {
+    // 128-token tiles read each weight row once; 64-token ones twice, but
+    // they give twice the tiles when K is too short to split over a cluster
+    const bool wide = busy_ctas(a.M, a.N, a.K, 128) >= busy_ctas(a.M, a.N, a.K, 64);
+    return wide ? run<128, A2_MN>(a, stream) : run<64, A2_MN>(a, stream);
+  }
   if (a.N <= 128)
     return pair ? run_pair2<128, A2_MN>(a, stream) : run<128, A2_MN>(a, stream);
   if (pair) {

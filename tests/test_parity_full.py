@@ -136,8 +136,9 @@ def test_opt66b_inference_fc1(S, T):
     check_layer(S, 4, T, 9216, 36864, 64, forward_only=True, n_t=64, n_o=512)
 
 
-@pytest.mark.parametrize("name,T,inp,out", [("q", 16, 9216, 9216), ("fc2", 1, 36864, 9216)])
+@pytest.mark.parametrize("name,T,inp,out", [("q", 16, 9216, 9216), ("fc2", 1, 36864, 9216),
+                                             ("q", 128, 9216, 9216), ("fc2", 128, 36864, 9216)])
 def test_opt66b_inference_split_k(S, name, T, inp, out):
-    """72 weight tiles: the sparse product splits K over CTA pairs and XL over
-    clusters of eight."""
+    """72 weight tiles: the sparse product splits K over CTA pairs (16- and
+    128-token tiles) and XL over clusters of eight."""
     check_layer(S, 0 if name == "q" else 5, T, inp, out, 64, forward_only=True, n_t=16, n_o=512)
