@@ -325,8 +325,10 @@ class BlockStep:
         pre-compressed weights."""
         S = self.S
         # the block's linears are independent: with extra streams, linear i
-        # goes to stream i % n (forked from and joined back into `stream`)
-        lanes = [stream] + (list(self.extra_streams) if only is None else [])
+        # goes to stream i % n (forked from and joined back into `stream`).
+        # A marked pass stays on `stream`, so that each call's events time
+        # that call alone.
+        lanes = [stream] + (list(self.extra_streams) if only is None and marks is None else [])
         for x in lanes[1:]:
             x.wait_stream(stream)
         for li, b in enumerate(self.layers if only is None else [self.layers[only]]):
@@ -645,7 +647,8 @@ def gpu_arm(args):
 
     # Per-call breakdown: `call_reps` marked passes over every input set; a
     # call's time per step is the median over the passes of its summed
-    # event times in that pass.
+    # event times in that pass.  The marked passes issue every call on the
+    # step's own stream (with --streams, so that calls do not overlap).
     reps = max(1, args.call_reps)
     per_rep = []  # one {call: ms per step} per pass
     obs = {}  # call -> [(in, out)] of one step
@@ -733,7 +736,8 @@ def gpu_arm(args):
             roof["algorithmic_bytes"] = sum(dw_bytes(T, i, o, r) for i, o in obs[dom]) / n_launch
     roof.update({"kernel": kernel_of.get(dom, dom), "traffic": traffic, "launches_per_step": n_launch,
                  "call_ms_per_step": round(calls_ms[dom], 4),
-                 "call_time": f"median over {reps} marked passes of the step"})
+                 "call_time": f"median over {reps} marked passes of the step"
+                              + (", its calls on one stream" if args.streams > 1 else "")})
 
     rates = mma_rates(stream) if args.mma_rate else None
     if rates and roof["bound"] == "tensor":
