@@ -593,17 +593,25 @@ struct Sp2Cfg {
   // output staging for the TMA stores: two 1 KB buffers per epilogue warp,
   // so one store can read its buffer while the next is filled
   static constexpr int STG_BYTES = 2048;
-  static constexpr int SMEM = STAGES * STAGE + 1024 /*barriers*/ + kEpiWarps * STG_BYTES +
+  // Stage s goes to metadata group s % 4, so with three stages or fewer the
+  // fourth group (warps 22..25) has no stage: it joins the epilogue as a
+  // third set, which drains the accumulators in two thirds of the time.
+  static constexpr int EPI_SETS = STAGES <= 3 ? 3 : 2;
+  static constexpr int EPI_WARPS = 4 * EPI_SETS;
+  static constexpr int SMEM = STAGES * STAGE + 1024 /*barriers*/ + EPI_WARPS * STG_BYTES +
                               1024 /*align slack*/;
   static_assert(STAGE % 1024 == 0 && (HB * 128) % 1024 == 0, "1024-byte aligned atoms");
   static_assert(TMEM_NEED <= 512, "TMEM budget");
   static_assert(STAGES >= 2, "pipeline depth");
   static_assert(MT == 1 || MT == 2, "one or two weight tiles per CTA");
+  static_assert(BN > 32 * (EPI_SETS - 1), "every epilogue warp has a chunk");
+  static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
 // 26 warps: the 18 roles of the one-CTA kernel plus two more groups of four
 // metadata warps (warps 18..25), so that four stages' metadata move into
-// TMEM at once (stage s goes to group s % 4).
+// TMEM at once (stage s goes to group s % 4).  With three stages or fewer,
+// warps 22..25 are a third set of epilogue warps instead.
 constexpr int kThreadsPair = 832;
 
 template <int BN, bool A2_MN, int MT>
@@ -658,7 +666,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 2 * kEpiWarps);  // the epilogue warps of both CTAs
+      mbar_init(&acc_empty[b], 2 * C::EPI_WARPS);  // the epilogue warps of both CTAs
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -805,10 +813,10 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       }
       mma_commit_pair_mc(mma_done, 3);
     }
-  } else if (warp < 6 || (warp >= 14 && warp < 18)) {
+  } else if (warp < 6 || (warp >= 14 && warp < 18) || (C::EPI_SETS == 3 && warp >= 22)) {
     // ------------------------------------------------ epilogue -----------
     const int q = warp & 3;
-    const int half = warp >= 14 ? 1 : 0;
+    const int half = warp < 6 ? 0 : warp < 18 ? 1 : 2;  // this warp's set: chunks half, half + EPI_SETS, ...
     const uint32_t acc_empty0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
     // this warp's two 1 KB staging buffers: [token][32 weight rows] of the
     // output, 16 tokens (bf16) or 8 (fp32) at a time, each written out by a
@@ -828,11 +836,11 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       const uint32_t trow = tmem + (buf * MT + t) * C::ACC_COLS + (static_cast<uint32_t>(32 * q) << 16);
       const int mt = m0 + 256 * t;  // this tile's rows in this CTA
 #pragma unroll 1
-      for (int c0 = 32 * half; c0 < BN; c0 += 64) {
+      for (int c0 = 32 * half; c0 < BN; c0 += 32 * C::EPI_SETS) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(trow + c0, v);
         tmem_ld_wait();
-        if (t == MT - 1 && c0 + 64 >= BN) {  // this warp's last chunk read: hand the buffer back
+        if (t == MT - 1 && c0 + 32 * C::EPI_SETS >= BN) {  // this warp's last chunk read: hand the buffer back
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8 * buf);
