@@ -69,6 +69,7 @@ CASES = [
     (16, 4096, 2048, 64),   # few token tiles: K split over clusters (4 and 2 CTAs)
     (48, 6144, 3072, 32),   # odd cluster sizes (6 and 3 CTAs), ragged T
     (100, 4096, 5120, 16),  # 128-token tiles with K split over CTA pairs (forward), ragged T
+    (100, 4736, 5120, 16),  # the same with 37 K-blocks: 19 and 18 per CTA; 37 weight tiles in dX
     (4096, 1024, 1024, 16),  # OPT-350M block linears
     (4096, 1024, 4096, 16),
     (4096, 4096, 1024, 16),
