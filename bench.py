@@ -37,7 +37,10 @@ Step variants (the default is the five path calls per linear):
   --streams N        the block's linears (independent in this synthetic
                      step) issued on N streams, linear i on stream i % N,
                      forked from and joined into the step's stream; the
-                     default, one stream, runs them as a dependent chain.
+                     default, one stream, runs them as a dependent chain;
+  --fuse-qkv         inference blocks: Q, K and V read one X and run as one
+                     forward call on their stacked compressed weights, with
+                     one rank-3r adapter (L side by side, R block-diagonal).
 Every memory-bound call's achieved bandwidth is reported in `hbm_calls`, and
 the library's tensor-pipe rate self test in `mma_rate_selftest`.
 """
@@ -239,7 +242,7 @@ class BlockStep:
     """Device buffers and the ordered ABI calls of one block step."""
 
     def __init__(self, wl, seed: int, device, fused_prune: bool = False, optimizer: bool = False,
-                 frozen_columns: bool = False, pattern: str = "2:4"):
+                 frozen_columns: bool = False, pattern: str = "2:4", fuse_qkv: bool = False):
         import torch
 
         from sparse_rank_adapter_gb300 import slope
@@ -290,6 +293,34 @@ class BlockStep:
                 Wmaster=torch.empty(out, inp // 2, dtype=torch.float32, device=device) if optimizer else None,
                 inp=inp, out=out)
             self.layers.append(b)
+        if fuse_qkv:
+            self.layers = [self._stack_qkv(self.layers[:3], device)] + self.layers[3:]
+
+    @staticmethod
+    def _stack_qkv(parts, device):
+        """Q, K and V of one block read the same X: one call computes all
+        three with their weights stacked (3·out x in; A1 prunes rows on their
+        own, so the stack prunes to the three compressed weights stacked) and
+        one rank-3r adapter, L side by side and R block-diagonal, whose
+        product is each linear's own (X·L)·R on its columns."""
+        import torch
+
+        inp, out = parts[0]["inp"], parts[0]["out"]
+        assert all(p["inp"] == inp and p["out"] == out for p in parts), "Q, K, V of one shape"
+        T = parts[0]["X"].shape[0]
+        r = 0 if parts[0]["L"] is None else parts[0]["L"].shape[1]
+        n = len(parts)
+        b = dict(W=torch.cat([p["W"] for p in parts]), X=parts[0]["X"], dY=None,
+                 L=torch.cat([p["L"] for p in parts], dim=1) if r else None,
+                 R=torch.block_diag(*[p["R"] for p in parts]).contiguous() if r else None,
+                 Wv=torch.empty(n * out, inp // 2, dtype=torch.bfloat16, device=device),
+                 Wm=torch.empty(n * out, inp // 8, dtype=torch.uint8, device=device),
+                 Y=torch.empty(T, n * out, dtype=torch.bfloat16, device=device),
+                 XL=torch.empty(T, 2 * n * r, dtype=torch.bfloat16, device=device) if r else None,
+                 inp=inp, out=n * out, parts=[(inp, out)] * n)
+        for k in ("Dv", "Dm", "dX", "G", "dW", "Wv8", "Wm8", "Dv8", "Dm8", "dL", "dR", "Wmaster"):
+            b[k] = None
+        return b
 
     def input_names(self):
         if self.wl.forward_only:  # weights stay resident (pre-compressed); a request brings X
@@ -443,7 +474,8 @@ class Marks:
         # external: inside a captured graph these become event-record nodes
         e0 = torch.cuda.Event(enable_timing=True, external=True)
         e1 = torch.cuda.Event(enable_timing=True, external=True)
-        self.pairs.append((name, b["inp"], b["out"], e0, e1))
+        # the linears the call computes: one, or Q, K and V stacked
+        self.pairs.append((name, b.get("parts", [(b["inp"], b["out"])]), e0, e1))
         return e0, e1
 
 
@@ -587,7 +619,8 @@ def gpu_arm(args):
     stream = torch.cuda.Stream(device=dev)
     n_sets = max(1, args.sets)
     sets = [BlockStep(wl, seed=s + 10 * rank, device=dev, fused_prune=args.fused_prune, optimizer=args.optimizer,
-                      frozen_columns=args.frozen_columns, pattern=args.pattern) for s in range(n_sets)]
+                      frozen_columns=args.frozen_columns, pattern=args.pattern, fuse_qkv=args.fuse_qkv)
+            for s in range(n_sets)]
     extra = [torch.cuda.Stream(device=dev) for _ in range(min(max(1, args.streams), 8) - 1)]
     for st in sets:
         st.extra_streams = extra
@@ -651,7 +684,8 @@ def gpu_arm(args):
     # step's own stream (with --streams, so that calls do not overlap).
     reps = max(1, args.call_reps)
     per_rep = []  # one {call: ms per step} per pass
-    obs = {}  # call -> [(in, out)] of one step
+    obs = {}  # call -> [(in, out)] of one step, one per linear
+    n_calls = {}  # call -> launches of it in one step
     for rep in range(reps):
         with torch.cuda.stream(stream):
             for i in range(n_sets):
@@ -663,10 +697,11 @@ def gpu_arm(args):
         stream.synchronize()
         tot = {}
         for m in marks:
-            for name, inp, out, e0, e1 in m.pairs:
+            for name, parts, e0, e1 in m.pairs:
                 tot[name] = tot.get(name, 0.0) + e0.elapsed_time(e1)
                 if rep == 0 and m is marks[0]:
-                    obs.setdefault(name, []).append((inp, out))
+                    obs.setdefault(name, []).extend(parts)  # per linear (algorithmic work and bytes)
+                    n_calls[name] = n_calls.get(name, 0) + 1
         per_rep.append({k: v / n_sets for k, v in tot.items()})
     calls_ms = {k: statistics.median(r[k] for r in per_rep) for k in per_rep[0]}
     if world > 1:
@@ -681,7 +716,7 @@ def gpu_arm(args):
     hbm, bf16, bf16_sus, src = peaks()
     dense_peak, peak_why = pick_peak(clocks, bf16, bf16_sus)
     dom = max(calls_ms, key=calls_ms.get)
-    n_launch = len(obs[dom])
+    n_launch = n_calls[dom]
     if dom == "fwd" and wl.forward_only and T <= 128:
         # small-batch inference streams the compressed weights: bytes-bound
         byts = sum(fwd_bytes(T, i, o, r) for i, o in obs[dom])
@@ -762,6 +797,7 @@ def gpu_arm(args):
                        "l2": f"{n_sets} rotating input sets of {set_bytes(sets[0]) / 2**20:.0f} MiB (> L2 {L2_BYTES // 2**20} MiB)",
                        "graph": bool(args.graph), "parallelism": f"replicas x{world}",
                        "streams": max(1, min(args.streams, 8)),
+                       "fuse_qkv": bool(args.fuse_qkv),
                        "prune": ("both masks kept: re-compression, then beta*A + gamma*B"
                                  if args.optimizer and args.frozen_columns
                                  else "kept mask: re-compression + A2, then beta*A + gamma*B" if args.optimizer
@@ -1172,6 +1208,9 @@ def main():
     ap.add_argument("--frozen-columns", action="store_true",
                     help="with --optimizer: the column mask kept from initialisation too "
                          "(slope_recompress_frozen in place of the re-compression + A2)")
+    ap.add_argument("--fuse-qkv", action="store_true",
+                    help="inference workloads: Q, K and V of the block read one X and run as one call on "
+                         "their stacked weights (rank-3r adapter, block-diagonal R)")
     ap.add_argument("--fused-prune", action="store_true",
                     help="A1 and A2 through the one-call slope_prune_and_double_prune")
     ap.add_argument("--streams", type=int, default=1,
@@ -1183,6 +1222,10 @@ def main():
     args = ap.parse_args()
     if args.pattern != "2:4" and (args.fused_prune or args.optimizer):
         ap.error("--pattern 1:2 / 2:8 runs the plain training step (no --fused-prune, --optimizer)")
+    if args.fuse_qkv:
+        wl0 = synth.WORKLOADS[args.workload]
+        if not wl0.forward_only or args.linear or [x.name for x in wl0.linears[:3]] != ["q", "k", "v"]:
+            ap.error("--fuse-qkv applies to a whole inference block (Q, K, V first)")
     if args.warmup < 3:
         args.warmup = 3
     if args.oracle_sample > 0:

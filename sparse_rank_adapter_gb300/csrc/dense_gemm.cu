@@ -59,19 +59,22 @@ template <int BN>
 struct DnCfg {
   static constexpr int B_BYTES = BN * kBK * 2;
   static constexpr int STAGE = kA_BYTES + B_BYTES;
-  // fp32 partial tile that a cluster peer hands to its leader when a narrow
-  // tile's K is split over a cluster (column-major: [BN][128])
-  static constexpr int RED_BYTES = BN <= 64 ? kBM * BN * 4 : 0;
-  static constexpr int STAGES_FIT = (192 * 1024 - RED_BYTES) / STAGE;
+  // fp32 partial tile that each CTA of a cluster leaves for the others when
+  // a tile's K is split over the cluster (column-major: [BN][128]).  A
+  // split cluster owns one tile, so by then every stage fill has been
+  // consumed: the partial lives in the stage ring.
+  static constexpr int RED_BYTES = kBM * BN * 4;
+  static constexpr int STAGES_FIT = 192 * 1024 / STAGE;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int ACC_COLS = BN < 32 ? 32 : BN;  // one accumulator buffer
   static constexpr int TMEM_COLS = 2 * ACC_COLS;       // double-buffered
-  // stages | barriers (1 KB) | partial tile | alignment slack
-  static constexpr int SMEM = STAGES * STAGE + 1024 + RED_BYTES + 1024;
+  // stages | barriers (1 KB) | alignment slack
+  static constexpr int SMEM = STAGES * STAGE + 1024 + 1024;
   // MN-major B: swizzle atom width in elements (64 for SW128) and its code.
   static constexpr int B_ATOM = BN >= 64 ? 64 : BN;
   static constexpr uint32_t B_SWZ = BN >= 64 ? kSwizzle128 : BN == 32 ? kSwizzle64 : kSwizzle32;
   static_assert(STAGE % 1024 == 0, "stage must keep 1024-byte alignment");
+  static_assert(RED_BYTES <= STAGES * STAGE, "the split partial fits in the stage ring");
 };
 
 struct DnParams {
@@ -253,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* red_empty = red_full + 1;  // cluster split: every CTA has read this CTA's partial
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(red_empty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  float* red = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE + 1024);
+  float* red = reinterpret_cast<float*>(smem);  // split partial, over the drained stage ring
 
   const int warp = warp_id(), lane = lane_id();
   const int cs = p.csplit;
@@ -391,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t trow = tmem + buf * C::ACC_COLS + (static_cast<uint32_t>(32 * q) << 16);
       constexpr int CH = BN < 32 ? BN : 32;
-      if constexpr (C::RED_BYTES > 0 && EPI == DenseEpi::StoreBf16HiLo) {
+      if constexpr (EPI == DenseEpi::StoreBf16HiLo) {
         if (cs > 1) {
           // Cluster split of K, reduce-scatter: every CTA leaves its fp32
           // partial in its own shared memory ([column][row]); then each
@@ -958,7 +961,7 @@ cudaError_t run(const DenseGemmArgs& a, cudaStream_t stream) {
     int want = sm_count() / tiles;
     want = want < 8 ? want : 8;
     want = want < num_kb / 16 ? want : num_kb / 16;
-    if (C::RED_BYTES > 0 && want >= 2) {
+    if (want >= 2) {
       const int kbs = (num_kb + want - 1) / want;
       csplit = (num_kb + kbs - 1) / kbs;  // every CTA of the cluster owns >= 1 K-block
     }
