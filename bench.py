@@ -38,9 +38,11 @@ Step variants (the default is the five path calls per linear):
                      step) issued on N streams, linear i on stream i % N,
                      forked from and joined into the step's stream; the
                      default, one stream, runs them as a dependent chain;
-  --fuse-qkv         inference blocks: Q, K and V read one X and run as one
-                     forward call on their stacked compressed weights, with
-                     one rank-3r adapter (L side by side, R block-diagonal).
+  --fuse-qkv         Q, K and V read one X and run as one call each on their
+                     stacked compressed weights, with one rank-3r adapter (L
+                     side by side, R block-diagonal); in training their input
+                     gradients are summed by the stacked dX call, as the
+                     block's shared X needs.
 Every memory-bound call's achieved bandwidth is reported in `hbm_calls`, and
 the library's tensor-pipe rate self test in `mma_rate_selftest`.
 """
@@ -294,15 +296,20 @@ class BlockStep:
                 inp=inp, out=out)
             self.layers.append(b)
         if fuse_qkv:
-            self.layers = [self._stack_qkv(self.layers[:3], device)] + self.layers[3:]
+            self.layers = [self._stack_qkv(self.layers[:3], device, not wl.forward_only)] + self.layers[3:]
 
     @staticmethod
-    def _stack_qkv(parts, device):
+    def _stack_qkv(parts, device, training):
         """Q, K and V of one block read the same X: one call computes all
         three with their weights stacked (3·out x in; A1 prunes rows on their
         own, so the stack prunes to the three compressed weights stacked) and
         one rank-3r adapter, L side by side and R block-diagonal, whose
-        product is each linear's own (X·L)·R on its columns."""
+        product is each linear's own (X·L)·R on its columns.  Backward, the
+        stacked dY (T x 3·out) against the stacked double-pruned weight (its
+        2:4 groups along 3·out never straddle two linears) sums the three
+        input gradients, as the block's shared X needs; the weight gradient
+        call gives the three dW and dL blocks, and dR on its diagonal blocks
+        (the off-diagonal ones are computed and not used)."""
         import torch
 
         inp, out = parts[0]["inp"], parts[0]["out"]
@@ -310,15 +317,23 @@ class BlockStep:
         T = parts[0]["X"].shape[0]
         r = 0 if parts[0]["L"] is None else parts[0]["L"].shape[1]
         n = len(parts)
-        b = dict(W=torch.cat([p["W"] for p in parts]), X=parts[0]["X"], dY=None,
+        bf, f32 = torch.bfloat16, torch.float32
+
+        def new(shape, dt, cond=True):
+            return torch.empty(shape, dtype=dt, device=device) if cond else None
+
+        b = dict(W=torch.cat([p["W"] for p in parts]), X=parts[0]["X"],
+                 dY=torch.cat([p["dY"] for p in parts], dim=1) if training else None,
                  L=torch.cat([p["L"] for p in parts], dim=1) if r else None,
                  R=torch.block_diag(*[p["R"] for p in parts]).contiguous() if r else None,
-                 Wv=torch.empty(n * out, inp // 2, dtype=torch.bfloat16, device=device),
-                 Wm=torch.empty(n * out, inp // 8, dtype=torch.uint8, device=device),
-                 Y=torch.empty(T, n * out, dtype=torch.bfloat16, device=device),
-                 XL=torch.empty(T, 2 * n * r, dtype=torch.bfloat16, device=device) if r else None,
+                 Wv=new((n * out, inp // 2), bf), Wm=new((n * out, inp // 8), torch.uint8),
+                 Dv=new((inp, n * out // 2), bf, training), Dm=new((inp, n * out // 8), torch.uint8, training),
+                 Y=new((T, n * out), bf), XL=new((T, 2 * n * r), bf, r > 0),
+                 dX=new((T, inp), bf, training), G=new((T, 2 * n * r), bf, training and r > 0),
+                 dW=new((n * out, inp // 2), f32, training),
+                 dL=new((inp, n * r), f32, training and r > 0), dR=new((n * r, n * out), f32, training and r > 0),
                  inp=inp, out=n * out, parts=[(inp, out)] * n)
-        for k in ("Dv", "Dm", "dX", "G", "dW", "Wv8", "Wm8", "Dv8", "Dm8", "dL", "dR", "Wmaster"):
+        for k in ("Wv8", "Wm8", "Dv8", "Dm8", "Wmaster"):
             b[k] = None
         return b
 
@@ -436,14 +451,20 @@ class BlockStep:
             n += 0 if self.wl.forward_only else (1 if self.fused_prune or self.optimizer else 2)  # prune(s)
             n += 2 if self.m == 8 and not self.wl.forward_only else 0  # the two 2:4 forms
             n += 1 if self.optimizer else 0  # beta·A + gamma·B
-            n += 2 if self.wl.rank else 1  # fwd: (XL) + sparse
+            r = 0 if b["L"] is None else b["L"].shape[1]  # the layer's own rank (3r when Q, K, V are stacked)
+            n += 2 if r else 1  # fwd: (XL) + sparse
             if not self.wl.forward_only:
-                n += 2 if self.wl.rank else 1  # bwd_input: (G) + sparse
-                n += 1  # dW with dL, dR alongside
-                # the zero-fill of the outputs the launch adds into: the adapter
-                # gradients always, dW when its K is split
-                if self.wl.rank or dw_splits(self.wl.tokens, b["inp"], b["out"], slots) > 1:
+                n += 2 if r else 1  # bwd_input: (G) + sparse
+                pair = (b["out"] // 128) % 2 == 0  # the dW GEMM on CTA pairs
+                fuse = r > 0 and r <= 128 and pair  # dL, dR inside the dW launch
+                n += 1  # dW
+                # the zero-fill before it: on CTA pairs always (the workspace's
+                # wave counter, and the outputs the launch adds into); otherwise
+                # when its K is split
+                if pair or dw_splits(self.wl.tokens, b["inp"], b["out"], slots) > 1:
                     n += 1
+                if r and not fuse:
+                    n += 3  # zero-fill of dL, dR, then their two GEMMs
         return n
 
 
@@ -1209,8 +1230,8 @@ def main():
                     help="with --optimizer: the column mask kept from initialisation too "
                          "(slope_recompress_frozen in place of the re-compression + A2)")
     ap.add_argument("--fuse-qkv", action="store_true",
-                    help="inference workloads: Q, K and V of the block read one X and run as one call on "
-                         "their stacked weights (rank-3r adapter, block-diagonal R)")
+                    help="Q, K and V of the block read one X and run as one call each on their stacked "
+                         "weights (rank-3r adapter, block-diagonal R; in training the dX call sums theirs)")
     ap.add_argument("--fused-prune", action="store_true",
                     help="A1 and A2 through the one-call slope_prune_and_double_prune")
     ap.add_argument("--streams", type=int, default=1,
@@ -1224,8 +1245,10 @@ def main():
         ap.error("--pattern 1:2 / 2:8 runs the plain training step (no --fused-prune, --optimizer)")
     if args.fuse_qkv:
         wl0 = synth.WORKLOADS[args.workload]
-        if not wl0.forward_only or args.linear or [x.name for x in wl0.linears[:3]] != ["q", "k", "v"]:
-            ap.error("--fuse-qkv applies to a whole inference block (Q, K, V first)")
+        if args.linear or [x.name for x in wl0.linears[:3]] != ["q", "k", "v"]:
+            ap.error("--fuse-qkv applies to a whole block (Q, K, V first)")
+        if args.optimizer or args.pattern != "2:4":
+            ap.error("--fuse-qkv runs the plain 2:4 step (no --optimizer, --pattern)")
     if args.warmup < 3:
         args.warmup = 3
     if args.oracle_sample > 0:
