@@ -30,13 +30,14 @@
 //
 // The hi/lo store needs the whole sum before it rounds, so its split-K goes
 // through a thread-block cluster instead of atomics: the cluster's CTAs take
-// K ranges of the same tile; each writes its fp32 partial into its own
-// shared memory and arrives (release, cluster scope) on every other CTA's
-// barrier; then each adds one slice of the tile's rows over all the
-// partials (distributed shared memory), stores it, and arrives on every
-// other CTA's second barrier, after which partials may be overwritten with
-// the next tile's.  This is what gives a handful of token tiles (small T)
-// more than one SM each.
+// K ranges of the one tile the cluster owns; each writes its fp32 partial
+// into its own stage ring (drained: its last MMA has completed) and arrives
+// (release, cluster scope) on every other CTA's barrier; then each adds one
+// slice of the tile's rows over all the partials (distributed shared
+// memory), stores it, and arrives on every other CTA's second barrier, so
+// that no CTA leaves while another still reads its partial.  This is what
+// gives a handful of token tiles (small T) more than one SM each, at every
+// tile width.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
