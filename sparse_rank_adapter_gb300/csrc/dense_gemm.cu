@@ -34,8 +34,9 @@
 // into its own stage ring (drained: its last MMA has completed) and arrives
 // (release, cluster scope) on every other CTA's barrier; then each adds one
 // slice of the tile's rows over all the partials (distributed shared
-// memory), stores it, and arrives on every other CTA's second barrier, so
-// that no CTA leaves while another still reads its partial.  This is what
+// memory), stores it, and arrives on every other CTA's second barrier; a
+// cluster barrier at the end keeps each CTA until the others have read its
+// partial.  This is what
 // gives a handful of token tiles (small T) more than one SM each, at every
 // tile width.
 #include <cuda.h>
