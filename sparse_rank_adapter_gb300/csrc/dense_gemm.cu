@@ -524,10 +524,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (cs > 1) cluster_sync();
 }
 
-// Zeroes up to three fp32 arrays, the outputs a split launch adds into, in
-// one launch.  Unlike memset nodes it is a programmatic dependent of the
-// kernel before it (set-up overlaps that kernel's tail) and lets the next
-// kernel launch early; it writes only after the previous kernel is done.
+// Zeroes up to four fp32 arrays (the outputs a launch adds into and its
+// wave counter) in one launch.  Unlike memset nodes it is a programmatic
+// dependent of the kernel before it (set-up overlaps that kernel's tail) and
+// lets the next kernel launch early; it writes only after the previous
+// kernel is done.
 __global__ void __launch_bounds__(256) zero3_kernel(float4* a, int64_t na, float4* b, int64_t nb, float4* c,
                                                     int64_t nc, float4* d, int64_t nd) {
   grid_dependency_wait();
