@@ -609,3 +609,45 @@ def test_weight_grad28_is_an_explicit_gather():
     _, _, dL24, dR24 = O.linear_bwd_weight(d["dY"], d["X"], O.prune24(d["W"])[1], d["L"], d["R"])
     np.testing.assert_allclose(dL, dL24, rtol=1e-12)  # the adapter gradients ignore the mask
     np.testing.assert_allclose(dR, dR24, rtol=1e-12)
+
+
+def test_stacked_linears_decompose_block_by_block():
+    """The identities a caller relies on when stacking Q, K and V: A1 of the
+    stacked weights is each weight's A1 stacked (rows prune alone); A2 of the
+    stack is each A2 side by side (groups along 3·out never straddle two
+    linears); with L side by side and R block-diagonal, the forward's column
+    blocks, the weight gradient's row blocks, dL's column blocks and dR's
+    diagonal blocks are each linear's own, and the stacked input gradient is
+    the sum of the three."""
+    T, inp, out, r = 12, 32, 16, 4
+    ds = [synth.layer_inputs(0, 40 + j, T, inp, out, r) for j in range(3)]
+    X = ds[0]["X"]
+    W = np.concatenate([d["W"] for d in ds])
+    dY = np.concatenate([d["dY"] for d in ds], axis=1)
+    L = np.concatenate([d["L"] for d in ds], axis=1)
+    R = np.zeros((3 * r, 3 * out), np.uint16)  # bf16 bits; +0 off the diagonal blocks
+    for j, d in enumerate(ds):
+        R[j * r:(j + 1) * r, j * out:(j + 1) * out] = d["R"]
+    vals, meta, _ = O.prune24(W)
+    tv, tm, _ = O.double_prune24(vals, meta, 3 * out, inp)
+    Y, _ = O.linear_fwd(X, vals, meta, L, R)
+    dX, _ = O.linear_bwd_input(dY, tv, tm, L, R)
+    dWc, _, dL, dR = O.linear_bwd_weight(dY, X, meta, L, R)
+    dX_sum = 0.0
+    for j, d in enumerate(ds):
+        vj, mj, _ = O.prune24(d["W"])
+        tvj, tmj, _ = O.double_prune24(vj, mj, out, inp)
+        rows, cols = slice(j * out, (j + 1) * out), slice(j * r, (j + 1) * r)
+        np.testing.assert_array_equal(vals[rows], vj)
+        np.testing.assert_array_equal(meta[rows], mj)
+        np.testing.assert_array_equal(tv[:, j * out // 2:(j + 1) * out // 2], tvj)
+        np.testing.assert_array_equal(tm[:, j * out // 8:(j + 1) * out // 8], tmj)
+        Yj, _ = O.linear_fwd(X, vj, mj, d["L"], d["R"])
+        np.testing.assert_allclose(Y[:, rows], Yj, rtol=1e-12, atol=1e-12)
+        dXj, _ = O.linear_bwd_input(d["dY"], tvj, tmj, d["L"], d["R"])
+        dX_sum = dX_sum + dXj
+        dWj, _, dLj, dRj = O.linear_bwd_weight(d["dY"], X, mj, d["L"], d["R"])
+        np.testing.assert_allclose(dWc[rows], dWj, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(dL[:, cols], dLj, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(dR[cols, rows], dRj, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dX, dX_sum, rtol=1e-12, atol=1e-12)
