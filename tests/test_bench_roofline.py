@@ -51,3 +51,19 @@ def test_oracle_slabs_cover_each_weight_exactly_once():
     tot = sum(s.unit_flops(lin, n) for _, lin, _, n in s.units)
     wl_T = synth.Workload("x", s.T, s.wl.rank, s.wl.linears)
     assert abs(tot - bench.flops_per_step(wl_T)) <= 1e-9 * tot
+
+
+def test_fuse_qkv_rejects_what_it_cannot_stack():
+    """--fuse-qkv stacks the block's Q, K and V: it refuses a single linear,
+    the optimizer step and the other N:M patterns (argparse error, exit 2)."""
+    import os
+    import subprocess
+    import sys
+
+    here = os.path.dirname(os.path.dirname(os.path.abspath(bench.__file__)))
+    script = os.path.join(here, "bench.py")
+    for extra in (["--linear", "q"], ["--optimizer"], ["--pattern", "1:2"]):
+        res = subprocess.run([sys.executable, script, "--fuse-qkv", *extra], capture_output=True, text=True,
+                             timeout=120)
+        assert res.returncode == 2, (extra, res.stderr[-500:])
+        assert "--fuse-qkv" in res.stderr
