@@ -60,8 +60,7 @@ def test_fuse_qkv_rejects_what_it_cannot_stack():
     import subprocess
     import sys
 
-    here = os.path.dirname(os.path.dirname(os.path.abspath(bench.__file__)))
-    script = os.path.join(here, "bench.py")
+    script = os.path.abspath(bench.__file__)
     for extra in (["--linear", "q"], ["--optimizer"], ["--pattern", "1:2"]):
         res = subprocess.run([sys.executable, script, "--fuse-qkv", *extra], capture_output=True, text=True,
                              timeout=120)
